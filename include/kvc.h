@@ -1,0 +1,163 @@
+/*
+ * kvc.h - C ABI of the B300 Attention Matching KV-cache compaction library.
+ *
+ * The method is the one described on "Fast KV Compaction via Attention
+ * Matching" (gist.science explainer of arXiv 2602.16284), section 2
+ * ("Objectif principal", "Pipeline algorithmique"): for every KV head, a cache
+ * of T keys/values and n reference queries Q_ref are reduced to t < T entries
+ * (C_k = selected original keys, a per-key scalar bias beta, refitted values
+ * C_v) so that softmax(q C_k^T/sqrt(d) + beta) C_v and
+ * sum_i exp(q C_k[i]/sqrt(d) + beta_i) reproduce the full cache's attention
+ * output and attention mass for the reference queries.
+ *
+ * Conventions shared by every entry point
+ *  - All pointers marked "device" are CUDA device pointers on the current
+ *    device; "host" pointers are ordinary host memory.
+ *  - The caller owns every buffer.  kvc_compact / kvc_attend allocate nothing
+ *    and free nothing; scratch comes from the caller's workspace.
+ *  - Work is enqueued asynchronously on `stream`; no call synchronises the
+ *    stream.  Outputs are valid once the stream reaches that point.
+ *  - Tensors are row-major with the head dimension d contiguous; heads are
+ *    packed back to back (head h of Q starts at element h*n*d).
+ *  - Q/K/V/C_k are `dtype` (bf16 or fp32); every other float is fp32.
+ *  - The return value reports argument, alignment, workspace and launch
+ *    errors only (nothing is enqueued when it is not KVC_OK).  Numerical
+ *    outcomes are written per head into `head_status` (device int32 [H]);
+ *    a head whose status is not KVC_OK has unspecified outputs.
+ *  - No C++ exception crosses this interface.
+ */
+#ifndef KVC_H_
+#define KVC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kvc_stream_t;  /* cudaStream_t; NULL = legacy default stream */
+
+typedef enum kvc_status {
+    KVC_OK = 0,
+    /* call-level errors (return value) */
+    KVC_ERR_INVALID_ARG = 1,   /* bad size, null pointer, unsupported d/dtype     */
+    KVC_ERR_ALIGN = 2,         /* a tensor pointer is not 16-byte aligned          */
+    KVC_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required       */
+    KVC_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed       */
+    /* per-head outcomes (head_status) */
+    KVC_ERR_BAD_BUDGET = 16,   /* t_h outside [1, min(T, max_t)], offsets not the
+                                  exclusive prefix sum of budgets, or more forced
+                                  keys than t_h                                     */
+    KVC_ERR_NOT_SPD = 17,      /* a Cholesky pivot was not positive                 */
+    KVC_ERR_NNLS_MAXITER = 18, /* NNLS pivoting hit its iteration or set-size cap;
+                                  outputs hold the last (clamped) iterate           */
+    KVC_ERR_NONFINITE = 19     /* NaN/Inf in the inputs or an intermediate          */
+} kvc_status;
+
+typedef enum kvc_dtype { KVC_DTYPE_BF16 = 0, KVC_DTYPE_F32 = 1 } kvc_dtype;
+
+/* Shape of one call.  H independent KV heads, each with n reference queries
+ * (for GQA, the group's query heads stacked), T cached tokens, head dim d
+ * (64 or 128).  max_t bounds every per-head budget. */
+typedef struct kvc_problem {
+    int32_t H;
+    int32_t n;
+    int32_t T;
+    int32_t d;
+    int32_t dtype;     /* kvc_dtype */
+    int32_t max_t;
+} kvc_problem;
+
+/* Tuning / reading parameters.  kvc_default_params fills the defaults. */
+typedef struct kvc_params {
+    float scale;          /* logit scale; 0 -> 1/sqrt(d)                          */
+    float eps_mu;         /* NNLS ridge toward w = 1: mu = eps_mu * tr(G)/t (1e-2) */
+    float eps_lambda;     /* C_v ridge toward V[idx]: lambda = eps_lambda *
+                             tr(X^T X)/t (1e-2)                                   */
+    int32_t nnls_max_iter;  /* block-pivoting iterations (default 32)             */
+    int32_t nnls_max_zero;  /* cap on weights held at zero (default 512)          */
+    int32_t refine_iters;   /* NNLS iterative-refinement steps (default 2)        */
+    int32_t keep_first;     /* positions [0, keep_first) are always kept          */
+    int32_t keep_last;      /* positions [T-keep_last, T) are always kept         */
+    uint32_t flags;         /* reserved, must be 0                                */
+} kvc_params;
+
+/* Fill *prm with the defaults listed above.  Returns KVC_ERR_INVALID_ARG for a
+ * null pointer. */
+kvc_status kvc_default_params(kvc_params* prm);
+
+/* Bytes of device workspace kvc_compact needs for problem *p (independent of
+ * the budgets' values; sized by max_t).  Host-only; enqueues nothing. */
+kvc_status kvc_workspace_size(const kvc_problem* p, const kvc_params* prm, size_t* bytes);
+
+/* Byte offset, inside the workspace of kvc_compact for the same *p and *prm,
+ * of an intermediate a caller may inspect after the call completes:
+ *   0 O      fp32 [H][n][d]   reference outputs softmax(S) V
+ *   1 LSE2   fp32 [H][n]      log2 of each query's attention mass
+ *                             (lse in natural log = LSE2 * ln 2)
+ *   2 SCORE  fp32 [H][T]      RMS attention score of every key
+ *   3 W      fp32 [sum t]     NNLS weights w = exp(beta), offsets-indexed
+ *   4 HEAD   32-byte records per head (ridges mu, lambda; NNLS zero-set
+ *            size and iterations)
+ * Host-only.  Errors: INVALID_ARG (bad problem/params or unknown item). */
+kvc_status kvc_workspace_offset(const kvc_problem* p, const kvc_params* prm, int32_t item, size_t* offset);
+
+/* Compact H KV heads (page section 2, "Pipeline algorithmique"):
+ *   1. S = Q_ref K^T * scale, lse_q = log sum_j exp(S_qj), O = softmax(S) V;
+ *   2. score_j = sqrt(mean_q exp(S_qj - lse_q)^2) (attention aggregated by RMS);
+ *   3. idx = the t_h keys of largest float32 score (ties -> lower index;
+ *      forced positions first), ascending; C_k = K[idx];
+ *   4. w = exp(beta) >= 0 by NNLS on A'_qi = exp(S_q,idx_i - lse_q) against
+ *      the relative mass target 1, with ridge mu ||w - 1||^2;
+ *   5. C_v by least squares X C_v ~ O, X = softmax_i(S_q,idx_i + beta_i), with
+ *      ridge lambda ||C_v - V[idx]||^2, through X^T X, X^T O and Cholesky.
+ *
+ * Arguments (device unless stated):
+ *   p, prm     host; problem shape and parameters (prm NULL -> defaults)
+ *   Q_ref      [H][n][d] dtype          K, V  [H][T][d] dtype   (16B aligned)
+ *   budgets    int32 [H]: t_h, 1 <= t_h <= min(T, max_t)
+ *   offsets    int32 [H+1]: exclusive prefix sum of budgets (offsets[0] = 0);
+ *              head h's outputs occupy rows [offsets[h], offsets[h+1])
+ *   idx_out    int32 [sum t]: kept positions, ascending within a head
+ *   C_k        [sum t][d] dtype: exact copies of the kept K rows
+ *   beta       fp32 [sum t]: log w, -INFINITY where w = 0
+ *   C_v        fp32 [sum t][d]
+ *   head_status int32 [H]: KVC_OK or a per-head outcome above
+ *   workspace  device scratch of at least kvc_workspace_size bytes, 256B aligned
+ * Errors: INVALID_ARG, ALIGN, WORKSPACE, CUDA (nothing enqueued on the first
+ * three).  Calls that share a workspace must not overlap on the GPU. */
+kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm,
+                       const void* Q_ref, const void* K, const void* V,
+                       const int32_t* budgets, const int32_t* offsets,
+                       int32_t* idx_out, void* C_k, float* beta, float* C_v,
+                       int32_t* head_status,
+                       void* workspace, size_t workspace_bytes, kvc_stream_t stream);
+
+/* Read a compacted cache with a per-key bias (page section 2 objective, and
+ * section 5 on use with standard attention kernels):
+ *   O_out[h][q] = softmax_i(Q[h][q] . C_k[i] * scale + beta[i]) C_v[i]
+ * over head h's rows i in [offsets[h], offsets[h+1]).
+ *   p          host; H, d, dtype are read (n, T, max_t ignored)
+ *   Q          [H][n_q][d] dtype;  C_k [sum t][d] dtype;  beta fp32 [sum t];
+ *   C_v        fp32 [sum t][d];  offsets int32 [H+1] (device)
+ *   O_out      fp32 [H][n_q][d]
+ *   head_status int32 [H]: KVC_OK, BAD_BUDGET (empty or inconsistent range),
+ *              NONFINITE (every bias -inf for some query)
+ *   scale      logit scale; 0 -> 1/sqrt(d)
+ * Errors: INVALID_ARG, ALIGN, CUDA. */
+kvc_status kvc_attend(const kvc_problem* p, const void* Q, int32_t n_q,
+                      const void* C_k, const float* beta, const float* C_v,
+                      const int32_t* offsets, float* O_out, int32_t* head_status,
+                      float scale, kvc_stream_t stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char* kvc_status_string(kvc_status s);
+
+/* Library version string, e.g. "kvc 0.1.0 sm_103a". */
+const char* kvc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVC_H_ */

@@ -1,0 +1,256 @@
+// extern "C" entry points of libkvc: argument checks, workspace carving and
+// the launch sequence of the compaction steps ("Fast KV Compaction via
+// Attention Matching", section 2).  Everything is enqueued on the caller's
+// stream; nothing here allocates, frees or synchronises.
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace kvc {
+cudaError_t launch_validate(const int32_t*, const int32_t*, int, int, int, int, int32_t*, HeadScalars*, cudaStream_t);
+cudaError_t launch_attn_fwd_simt(int, int, const void*, const void*, const void*, int, int, int, float, float*, float*,
+                                 const int32_t*, cudaStream_t);
+cudaError_t launch_colscore_simt(int, int, const void*, const void*, const float*, int, int, int, float, float*,
+                                 const int32_t*, cudaStream_t);
+cudaError_t launch_select(const float*, int, int, const int32_t*, int, int, int32_t*, int32_t*, cudaStream_t);
+cudaError_t launch_gather(int, int, const void*, const void*, int, int, int, const int32_t*, const int32_t*, void*,
+                          float*, const int32_t*, cudaStream_t);
+cudaError_t launch_masslogits(int, int, const void*, const void*, const float*, const int32_t*, int, int, int, int64_t,
+                              float, float*, const int32_t*, cudaStream_t);
+cudaError_t launch_attend(int, int, const void*, int, const void*, const float*, const float*, const int32_t*, int,
+                          float, float*, int32_t*, cudaStream_t);
+cudaError_t launch_gram(bool, const float*, const int32_t*, int, int, int, int64_t, float*, float*, const int32_t*,
+                        cudaStream_t);
+cudaError_t launch_xto(int, const float*, const float*, const int32_t*, int, int, int, int64_t, float*,
+                       const int32_t*, cudaStream_t);
+cudaError_t launch_ridge_g(float*, const float*, const int32_t*, int, int64_t, float, float*, HeadScalars*, int32_t*,
+                           cudaStream_t);
+cudaError_t launch_ridge_m(int, float*, float*, const float*, const int32_t*, int, int64_t, float, HeadScalars*,
+                           int32_t*, cudaStream_t);
+cudaError_t launch_xsoftmax(float*, const float*, const int32_t*, int, int, int64_t, const int32_t*, cudaStream_t);
+cudaError_t launch_chol(float*, const int32_t*, int, int, int64_t, int32_t*, cudaStream_t);
+cudaError_t launch_cholsolve(int, const float*, const float*, const int32_t*, int, int64_t, float*, const int32_t*,
+                             cudaStream_t);
+cudaError_t launch_nnls(const NnlsArgs&, int, cudaStream_t);
+cudaError_t launch_nnls_refine(const NnlsArgs&, const float*, float*, float*, int, int, int, cudaStream_t);
+cudaError_t launch_beta_out(float*, const int32_t*, int, int, float*, const int32_t*, cudaStream_t);
+
+constexpr int kMaxT = 4096;     // largest budget the per-head solvers support
+
+struct Layout {
+    int64_t ldA;
+    int zmax;
+    size_t O, lse2, score, L2, Vsel, G, b, f, x, u, r, R, zflag, W, S, hs, total;
+};
+
+static size_t carve(size_t& cur, size_t bytes) {
+    size_t at = (size_t)round_up((int64_t)cur, 256);
+    cur = at + bytes;
+    return at;
+}
+
+static Layout make_layout(const kvc_problem& p, const kvc_params& prm) {
+    Layout L{};
+    const size_t H = p.H, n = p.n, T = p.T, d = p.d, mt = p.max_t;
+    L.ldA = round_up(p.max_t, 64);
+    L.zmax = std::max(1, std::min(prm.nnls_max_zero, p.max_t));
+    const size_t ldA = (size_t)L.ldA, zm = (size_t)L.zmax;
+    size_t c = 0;
+    L.O = carve(c, H * n * d * 4);
+    L.lse2 = carve(c, H * n * 4);
+    L.score = carve(c, H * T * 4);
+    L.L2 = carve(c, H * n * ldA * 4);
+    L.Vsel = carve(c, H * mt * d * 4);
+    L.G = carve(c, H * ldA * ldA * 4);
+    L.b = carve(c, H * mt * 4);
+    L.f = carve(c, H * mt * 4);
+    L.x = carve(c, H * mt * 4);
+    L.u = carve(c, H * n * 4);
+    L.r = carve(c, H * mt * 4);
+    L.R = carve(c, H * mt * d * 4);
+    L.zflag = carve(c, H * mt);
+    L.W = carve(c, H * ldA * zm * 4);
+    L.S = carve(c, H * zm * zm * 4);
+    L.hs = carve(c, H * sizeof(HeadScalars));
+    L.total = (size_t)round_up((int64_t)c, 256);
+    return L;
+}
+
+static bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
+
+static kvc_status check_problem(const kvc_problem* p) {
+    if (!p) return KVC_ERR_INVALID_ARG;
+    if (p->H < 1 || p->n < 1 || p->T < 1) return KVC_ERR_INVALID_ARG;
+    if (p->d != 64 && p->d != 128) return KVC_ERR_INVALID_ARG;
+    if (p->dtype != KVC_DTYPE_BF16 && p->dtype != KVC_DTYPE_F32) return KVC_ERR_INVALID_ARG;
+    if (p->max_t < 1 || p->max_t > p->T || p->max_t > kMaxT) return KVC_ERR_INVALID_ARG;
+    return KVC_OK;
+}
+
+static kvc_status check_params(const kvc_params& q, const kvc_problem& p) {
+    if (!(q.scale >= 0.f) || !std::isfinite(q.scale)) return KVC_ERR_INVALID_ARG;
+    if (!(q.eps_mu > 0.f) || !(q.eps_lambda > 0.f) || !std::isfinite(q.eps_mu) || !std::isfinite(q.eps_lambda))
+        return KVC_ERR_INVALID_ARG;
+    if (q.nnls_max_iter < 1 || q.nnls_max_zero < 1 || q.refine_iters < 0) return KVC_ERR_INVALID_ARG;
+    if (q.keep_first < 0 || q.keep_last < 0 || q.flags != 0) return KVC_ERR_INVALID_ARG;
+    if ((int64_t)q.keep_first + q.keep_last > p.T) return KVC_ERR_INVALID_ARG;
+    return KVC_OK;
+}
+
+static float log2_scale(const kvc_problem& p, float scale) {
+    const double s = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)p.d);
+    return (float)(s * 1.4426950408889634);
+}
+
+}  // namespace kvc
+
+using namespace kvc;
+
+#define KVC_TRY(call)                                  \
+    do {                                               \
+        cudaError_t _e = (call);                       \
+        if (_e != cudaSuccess) return KVC_ERR_CUDA;    \
+    } while (0)
+
+extern "C" {
+
+kvc_status kvc_default_params(kvc_params* prm) {
+    if (!prm) return KVC_ERR_INVALID_ARG;
+    std::memset(prm, 0, sizeof(*prm));
+    prm->scale = 0.f;
+    prm->eps_mu = 1e-2f;
+    prm->eps_lambda = 1e-2f;
+    prm->nnls_max_iter = 32;
+    prm->nnls_max_zero = 512;
+    prm->refine_iters = 2;
+    return KVC_OK;
+}
+
+kvc_status kvc_workspace_size(const kvc_problem* p, const kvc_params* prm, size_t* bytes) {
+    kvc_status s = check_problem(p);
+    if (s != KVC_OK || !bytes) return KVC_ERR_INVALID_ARG;
+    kvc_params q;
+    if (prm) q = *prm; else kvc_default_params(&q);
+    if ((s = check_params(q, *p)) != KVC_OK) return s;
+    *bytes = make_layout(*p, q).total;
+    return KVC_OK;
+}
+
+kvc_status kvc_workspace_offset(const kvc_problem* p, const kvc_params* prm, int32_t item, size_t* offset) {
+    kvc_status s = check_problem(p);
+    if (s != KVC_OK || !offset) return KVC_ERR_INVALID_ARG;
+    kvc_params q;
+    if (prm) q = *prm; else kvc_default_params(&q);
+    if ((s = check_params(q, *p)) != KVC_OK) return s;
+    const Layout L = make_layout(*p, q);
+    switch (item) {
+        case 0: *offset = L.O; break;
+        case 1: *offset = L.lse2; break;
+        case 2: *offset = L.score; break;
+        case 3: *offset = L.x; break;
+        case 4: *offset = L.hs; break;
+        default: return KVC_ERR_INVALID_ARG;
+    }
+    return KVC_OK;
+}
+
+kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* Q_ref, const void* K, const void* V,
+                       const int32_t* budgets, const int32_t* offsets, int32_t* idx_out, void* C_k, float* beta,
+                       float* C_v, int32_t* head_status, void* workspace, size_t workspace_bytes,
+                       kvc_stream_t stream) {
+    kvc_status s = check_problem(p);
+    if (s != KVC_OK) return s;
+    kvc_params q;
+    if (prm) q = *prm; else kvc_default_params(&q);
+    if ((s = check_params(q, *p)) != KVC_OK) return s;
+    if (!Q_ref || !K || !V || !budgets || !offsets || !idx_out || !C_k || !beta || !C_v || !head_status)
+        return KVC_ERR_INVALID_ARG;
+    if (!aligned(Q_ref, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(C_k, 16) || !aligned(C_v, 16) ||
+        !aligned(beta, 4) || !aligned(idx_out, 4) || !aligned(budgets, 4) || !aligned(offsets, 4) ||
+        !aligned(head_status, 4))
+        return KVC_ERR_ALIGN;
+    const Layout L = make_layout(*p, q);
+    if (!workspace || workspace_bytes < L.total) return KVC_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return KVC_ERR_ALIGN;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    float* O = (float*)(ws + L.O);
+    float* lse2 = (float*)(ws + L.lse2);
+    float* score = (float*)(ws + L.score);
+    float* L2 = (float*)(ws + L.L2);
+    float* Vsel = (float*)(ws + L.Vsel);
+    float* G = (float*)(ws + L.G);
+    float* b = (float*)(ws + L.b);
+    float* f = (float*)(ws + L.f);
+    float* x = (float*)(ws + L.x);
+    float* u = (float*)(ws + L.u);
+    float* r = (float*)(ws + L.r);
+    float* R = (float*)(ws + L.R);
+    int8_t* zflag = (int8_t*)(ws + L.zflag);
+    float* W = (float*)(ws + L.W);
+    float* S = (float*)(ws + L.S);
+    HeadScalars* hs = (HeadScalars*)(ws + L.hs);
+
+    const int H = p->H, n = p->n, T = p->T, d = p->d, dt = p->dtype, mt = p->max_t;
+    const int forced = std::min(T, q.keep_first + q.keep_last);
+    const float c2 = log2_scale(*p, q.scale);
+
+    KVC_TRY(launch_validate(budgets, offsets, H, T, mt, forced, head_status, hs, st));
+    KVC_TRY(launch_attn_fwd_simt(dt, d, Q_ref, K, V, H, n, T, c2, O, lse2, head_status, st));
+    KVC_TRY(launch_colscore_simt(dt, d, Q_ref, K, lse2, H, n, T, c2, score, head_status, st));
+    KVC_TRY(launch_select(score, H, T, offsets, q.keep_first, q.keep_last, idx_out, head_status, st));
+    KVC_TRY(launch_gather(dt, d, K, V, H, T, mt, offsets, idx_out, C_k, Vsel, head_status, st));
+    KVC_TRY(launch_masslogits(dt, d, Q_ref, C_k, lse2, offsets, H, n, mt, L.ldA, c2, L2, head_status, st));
+    KVC_TRY(launch_gram(true, L2, offsets, H, n, mt, L.ldA, G, b, head_status, st));
+    KVC_TRY(launch_ridge_g(G, b, offsets, H, L.ldA, q.eps_mu, f, hs, head_status, st));
+    KVC_TRY(launch_chol(G, offsets, H, mt, L.ldA, head_status, st));
+    NnlsArgs na{G, f, offsets, L.ldA, x, zflag, W, S, nullptr, hs, head_status, L.zmax, q.nnls_max_iter};
+    KVC_TRY(launch_nnls(na, H, st));
+    for (int it = 0; it < q.refine_iters; ++it) KVC_TRY(launch_nnls_refine(na, L2, u, r, H, n, mt, st));
+    KVC_TRY(launch_beta_out(x, offsets, H, mt, beta, head_status, st));
+    KVC_TRY(launch_xsoftmax(L2, x, offsets, H, n, L.ldA, head_status, st));
+    KVC_TRY(launch_gram(false, L2, offsets, H, n, mt, L.ldA, G, nullptr, head_status, st));
+    KVC_TRY(launch_xto(d, L2, O, offsets, H, n, mt, L.ldA, R, head_status, st));
+    KVC_TRY(launch_ridge_m(d, G, R, Vsel, offsets, H, L.ldA, q.eps_lambda, hs, head_status, st));
+    KVC_TRY(launch_chol(G, offsets, H, mt, L.ldA, head_status, st));
+    KVC_TRY(launch_cholsolve(d, G, R, offsets, H, L.ldA, C_v, head_status, st));
+    return KVC_OK;
+}
+
+kvc_status kvc_attend(const kvc_problem* p, const void* Q, int32_t n_q, const void* C_k, const float* beta,
+                      const float* C_v, const int32_t* offsets, float* O_out, int32_t* head_status, float scale,
+                      kvc_stream_t stream) {
+    if (!p || p->H < 1 || (p->d != 64 && p->d != 128) || n_q < 1 ||
+        (p->dtype != KVC_DTYPE_BF16 && p->dtype != KVC_DTYPE_F32) || !(scale >= 0.f) || !std::isfinite(scale))
+        return KVC_ERR_INVALID_ARG;
+    if (!Q || !C_k || !beta || !C_v || !offsets || !O_out || !head_status) return KVC_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(C_k, 16) || !aligned(C_v, 16) || !aligned(O_out, 16) || !aligned(beta, 4) ||
+        !aligned(offsets, 4) || !aligned(head_status, 4))
+        return KVC_ERR_ALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    KVC_TRY(cudaMemsetAsync(head_status, 0, sizeof(int32_t) * p->H, st));
+    KVC_TRY(launch_attend(p->dtype, p->d, Q, n_q, C_k, beta, C_v, offsets, p->H, log2_scale(*p, scale), O_out,
+                          head_status, st));
+    return KVC_OK;
+}
+
+const char* kvc_status_string(kvc_status s) {
+    switch (s) {
+        case KVC_OK: return "ok";
+        case KVC_ERR_INVALID_ARG: return "invalid argument";
+        case KVC_ERR_ALIGN: return "pointer not aligned";
+        case KVC_ERR_WORKSPACE: return "workspace missing or too small";
+        case KVC_ERR_CUDA: return "CUDA launch or runtime error";
+        case KVC_ERR_BAD_BUDGET: return "bad budget or offsets for this head";
+        case KVC_ERR_NOT_SPD: return "matrix not positive definite";
+        case KVC_ERR_NNLS_MAXITER: return "NNLS iteration or zero-set cap reached";
+        case KVC_ERR_NONFINITE: return "non-finite value";
+    }
+    return "unknown status";
+}
+
+const char* kvc_version(void) { return "kvc 0.1.0 sm_103a"; }
+
+}  // extern "C"

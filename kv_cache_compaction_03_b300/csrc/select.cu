@@ -1,0 +1,195 @@
+// Budget validation, per-head top-t selection by radix select, and the gather
+// of the kept keys/values ("Fast KV Compaction via Attention Matching",
+// section 2, key selection: the original keys with the highest attention
+// over the reference queries; kept entries are stored contiguously in
+// ascending position order).
+#include "common.cuh"
+
+namespace kvc {
+
+// ---------------------------------------------------------------- validate
+// grid ceil(H/256), block 256.  head_status[h] = OK or BAD_BUDGET.
+__global__ void k_validate(const int32_t* __restrict__ budgets, const int32_t* __restrict__ offsets, int H, int T,
+                           int max_t, int forced, int32_t* __restrict__ status, HeadScalars* __restrict__ hs) {
+    const int h = blockIdx.x * blockDim.x + threadIdx.x;
+    if (h >= H) return;
+    const int t = budgets[h];
+    bool ok = t >= 1 && t <= T && t <= max_t && t >= forced;
+    ok = ok && offsets[h + 1] - offsets[h] == t;
+    // per-head workspace rows are indexed by offsets: keep them inside H*max_t
+    ok = ok && offsets[h] >= 0 && (int64_t)offsets[h + 1] <= (int64_t)H * max_t;
+    if (h == 0) ok = ok && offsets[0] == 0;
+    status[h] = ok ? KVC_OK : KVC_ERR_BAD_BUDGET;
+    hs[h] = HeadScalars{};
+}
+
+// ---------------------------------------------------------------- block scan
+// Exclusive scan of one int per thread over a 1024-thread block; returns the
+// exclusive prefix and writes the block total to *total.
+__device__ int block_exclusive_scan(int v, int* sbuf, int* total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sbuf[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int w = (lane < (int)(blockDim.x >> 5)) ? sbuf[lane] : 0;
+        int z = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, z, o);
+            if (lane >= o) z += y;
+        }
+        sbuf[lane] = z - w;          // exclusive warp offsets
+        if (lane == 31) sbuf[32] = z;
+    }
+    __syncthreads();
+    int res = sbuf[wid] + x - v;
+    *total = sbuf[32];
+    __syncthreads();
+    return res;
+}
+
+__device__ __forceinline__ uint32_t score_key(const float* sc, int j, int T, int keep_first, int keep_last) {
+    if (j < keep_first || j >= T - keep_last) return 0x7f800000u;          // +inf: forced
+    return __float_as_uint(sc[j]) & 0x7fffffffu;
+}
+
+// ---------------------------------------------------------------- select
+// grid H, block 1024.  idx_out[off .. off+t) = kept positions, ascending.
+// The t-th largest key is found by four 8-bit radix passes over the float
+// bit patterns (monotone for non-negative floats); ties at the threshold go
+// to the lowest positions.
+__global__ void __launch_bounds__(1024) k_select(const float* __restrict__ score, int T, const int32_t* __restrict__ offsets,
+                                                 int keep_first, int keep_last, int32_t* __restrict__ idx_out,
+                                                 int32_t* __restrict__ status) {
+    const int h = blockIdx.x;
+    if (!head_ok(status, h)) return;
+    __shared__ int hist[256];
+    __shared__ int sbuf[33];
+    __shared__ uint32_t s_digit;
+    __shared__ int s_krem, s_nan;
+    const float* sc = score + (int64_t)h * T;
+    const int off = offsets[h];
+    const int t = offsets[h + 1] - off;
+    if (threadIdx.x == 0) {
+        s_krem = t;
+        s_nan = 0;
+    }
+    uint32_t prefix = 0, pmask = 0;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+        for (int j = threadIdx.x; j < T; j += blockDim.x) {
+            const uint32_t k = score_key(sc, j, T, keep_first, keep_last);
+            if (shift == 24 && k > 0x7f800000u) s_nan = 1;
+            if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int cum = 0, kr = s_krem;
+            uint32_t dg = 0;
+            for (int b = 255; b >= 0; --b) {
+                if (cum + hist[b] >= kr) {
+                    dg = (uint32_t)b;
+                    kr -= cum;
+                    break;
+                }
+                cum += hist[b];
+            }
+            s_digit = dg;
+            s_krem = kr;
+        }
+        __syncthreads();
+        prefix |= s_digit << shift;
+        pmask |= 255u << shift;
+    }
+    if (s_nan) {
+        if (threadIdx.x == 0) set_status(status, h, KVC_ERR_NONFINITE);
+        return;
+    }
+    const uint32_t tau = prefix;
+    const int krem = s_krem;                 // keys equal to tau still to take
+    const int chunk = (T + blockDim.x - 1) / blockDim.x;
+    const int j0 = min(T, (int)threadIdx.x * chunk), j1 = min(T, j0 + chunk);
+    int gt = 0, eq = 0;
+    for (int j = j0; j < j1; ++j) {
+        const uint32_t k = score_key(sc, j, T, keep_first, keep_last);
+        gt += k > tau;
+        eq += k == tau;
+    }
+    int tot;
+    const int eq_before = block_exclusive_scan(eq, sbuf, &tot);
+    const int take_eq = max(0, min(eq, krem - eq_before));
+    const int pos0 = block_exclusive_scan(gt + take_eq, sbuf, &tot);
+    int pos = pos0, er = eq_before;
+    for (int j = j0; j < j1; ++j) {
+        const uint32_t k = score_key(sc, j, T, keep_first, keep_last);
+        bool take = k > tau;
+        if (k == tau) {
+            take = er < krem;
+            ++er;
+        }
+        if (take) idx_out[off + pos++] = j;
+    }
+}
+
+// ---------------------------------------------------------------- gather
+// grid (ceil(max_t/8), H), block 256 (one warp per kept row).
+// C_k[off+i] = K[h][idx[off+i]] (storage dtype, 16-byte vectors) and
+// Vsel[off+i] = fp32(V[h][idx[off+i]]).
+template <typename TIn, int D>
+__global__ void __launch_bounds__(256) k_gather(const TIn* __restrict__ K, const TIn* __restrict__ V, int T,
+                                                const int32_t* __restrict__ offsets, const int32_t* __restrict__ idx,
+                                                TIn* __restrict__ Ck, float* __restrict__ Vsel,
+                                                const int32_t* __restrict__ status) {
+    const int h = blockIdx.y;
+    if (!head_ok(status, h)) return;
+    const int off = offsets[h];
+    const int t = offsets[h + 1] - off;
+    const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (i >= t) return;
+    const int j = idx[off + i];
+    constexpr int VEC = 16 / sizeof(TIn);          // elements per 16-byte vector
+    constexpr int NV = D / VEC;
+    const uint4* src = reinterpret_cast<const uint4*>(K + ((int64_t)h * T + j) * D);
+    uint4* dst = reinterpret_cast<uint4*>(Ck + ((int64_t)off + i) * D);
+    for (int v = lane; v < NV; v += 32) dst[v] = src[v];
+    const TIn* vr = V + ((int64_t)h * T + j) * D;
+    float* vo = Vsel + ((int64_t)off + i) * D;
+    for (int c = lane; c < D; c += 32) vo[c] = to_f32(vr[c]);
+}
+
+cudaError_t launch_validate(const int32_t* budgets, const int32_t* offsets, int H, int T, int max_t, int forced,
+                            int32_t* status, HeadScalars* hs, cudaStream_t st) {
+    k_validate<<<(H + 255) / 256, 256, 0, st>>>(budgets, offsets, H, T, max_t, forced, status, hs);
+    return cudaGetLastError();
+}
+cudaError_t launch_select(const float* score, int H, int T, const int32_t* offsets, int keep_first, int keep_last,
+                          int32_t* idx_out, int32_t* status, cudaStream_t st) {
+    k_select<<<H, 1024, 0, st>>>(score, T, offsets, keep_first, keep_last, idx_out, status);
+    return cudaGetLastError();
+}
+template <typename TIn, int D>
+static cudaError_t launch_gather_t(const void* K, const void* V, int H, int T, int max_t, const int32_t* offsets,
+                                   const int32_t* idx, void* Ck, float* Vsel, const int32_t* status, cudaStream_t st) {
+    dim3 grid((max_t + 7) / 8, H);
+    k_gather<TIn, D><<<grid, 256, 0, st>>>((const TIn*)K, (const TIn*)V, T, offsets, idx, (TIn*)Ck, Vsel, status);
+    return cudaGetLastError();
+}
+cudaError_t launch_gather(int dtype, int d, const void* K, const void* V, int H, int T, int max_t,
+                          const int32_t* offsets, const int32_t* idx, void* Ck, float* Vsel, const int32_t* status,
+                          cudaStream_t st) {
+    if (dtype == KVC_DTYPE_BF16)
+        return d == 128 ? launch_gather_t<__nv_bfloat16, 128>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, status, st)
+                        : launch_gather_t<__nv_bfloat16, 64>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, status, st);
+    return d == 128 ? launch_gather_t<float, 128>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, status, st)
+                    : launch_gather_t<float, 64>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, status, st);
+}
+
+}  // namespace kvc

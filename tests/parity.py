@@ -1,0 +1,141 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C ABI
+and the float64 oracle on the same seeded inputs, and compare them.
+
+Tolerances (float results) and their source:
+* selected indices: identical sets, except a swap between two keys whose
+  oracle scores differ by less than 1e-6 relative (the stated exemption);
+* beta: |beta_gpu - beta_oracle| <= 1e-3 wherever the oracle weight
+  w_i >= 1e-2 * max w; below that weight, |w_gpu - w_oracle| <= 1e-5 * max w
+  (log w is not a well-conditioned function of a weight 100x below the
+  largest: fp32 inputs of A' already carry ~1e-6 relative error, which the
+  NNLS conditioning amplifies);
+* C_v: relative Frobenius error <= 2e-3 per head;
+* compacted attention on held-out queries: relative Frobenius <= 1e-3 per head;
+* intermediates (O, lse, scores) against fp32 round-off bounds derived in the
+  tests that use them.
+When a head's index set differs within the exemption, beta/C_v/outputs are
+compared with the oracle continued from the GPU's selection.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import oracle
+from workloads import budgets as make_budgets, forced_mask
+from workloads.batch import generate
+
+IDX_REL_GAP = 1e-6
+BETA_ABS = 1e-3
+BETA_W_FLOOR = 1e-2
+W_ABS_BELOW = 1e-5
+CV_REL = 2e-3
+OHAT_REL = 1e-3
+
+
+def to_torch(a, dtype: str, device="cuda"):
+    import torch
+    if dtype == "bf16":
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+
+
+def run_gpu(w, inputs=None, buds=None, params=None):
+    """All heads of workload w through kvc_compact + kvc_attend in one call each."""
+    import torch
+    import kv_cache_compaction_03_b300 as kvc
+    if inputs is None:
+        inputs = generate(w)
+    if buds is None:
+        buds = make_budgets(w)
+    Q = to_torch(inputs["Q"], w.dtype)
+    K = to_torch(inputs["K"], w.dtype)
+    V = to_torch(inputs["V"], w.dtype)
+    Qt = to_torch(inputs["Qt"], w.dtype)
+    b = torch.from_numpy(np.asarray(buds, dtype=np.int32)).cuda()
+    prm = params or kvc.default_params(keep_first=w.keep_first, keep_last=w.keep_last)
+    c = kvc.compact_tensors(Q, K, V, b, prm)
+    Oh, st2 = kvc.attend_tensors(Qt, c)
+    torch.cuda.synchronize()
+    H, n, d, T = w.H, w.n, w.d, w.T
+    total = int(c.offsets[-1].item())
+    out = {
+        "status": c.head_status.cpu().numpy(),
+        "attend_status": st2.cpu().numpy(),
+        "offsets": c.offsets.cpu().numpy().astype(np.int64),
+        "idx": c.idx.cpu().numpy().astype(np.int64),
+        "beta": c.beta.cpu().numpy().astype(np.float64),
+        "Cv": c.C_v.cpu().numpy().astype(np.float64),
+        "Ck": c.C_k.float().cpu().numpy().astype(np.float64),
+        "Ohat": Oh.cpu().numpy().astype(np.float64),
+        "O": kvc.workspace_view(c, kvc.WS_O, H * n * d, torch.float32).cpu().numpy().reshape(H, n, d),
+        "lse": kvc.workspace_view(c, kvc.WS_LSE2, H * n, torch.float32).cpu().numpy().reshape(H, n) * math.log(2),
+        "score": kvc.workspace_view(c, kvc.WS_SCORE, H * T, torch.float32).cpu().numpy().reshape(H, T),
+        "w": kvc.workspace_view(c, kvc.WS_W, total, torch.float32).cpu().numpy().astype(np.float64),
+    }
+    return out, inputs
+
+
+def run_oracle_head(w, inputs, h, t, idx=None):
+    Q = oracle.decode(inputs["Q"][h], w.dtype)
+    K = oracle.decode(inputs["K"][h], w.dtype)
+    V = oracle.decode(inputs["V"][h], w.dtype)
+    Qt = oracle.decode(inputs["Qt"][h], w.dtype)
+    scale = 1.0 / math.sqrt(w.d)
+    forced = forced_mask(w) if (w.keep_first or w.keep_last) else None
+    r = oracle.compact_head(Q, K, V, t, forced=forced)
+    if idx is not None and not np.array_equal(idx, r.idx):
+        # continue the oracle from the given (valid) selection
+        Ck = K[idx]
+        Ap = oracle.mass_matrix(Q, Ck, r.lse, scale)
+        wv, beta, mu, _, _ = oracle.fit_beta(Ap)
+        X = oracle.biased_softmax(Ap, wv)
+        Cv, lam = oracle.fit_values(X, r.O, V[idx])
+        r = oracle.HeadResult(idx=idx, score=r.score, lse=r.lse, O=r.O, Ck=Ck, w=wv, beta=beta, Cv=Cv, mu=mu,
+                              lam=lam, mass=Ap @ wv)
+    Ohat = oracle.attend(Qt, r.Ck, r.beta, r.Cv, scale)
+    return r, Ohat
+
+
+def idx_check(gpu_idx, or_idx, or_score):
+    """(ok, swapped): sets equal, or every differing pair within the exemption."""
+    a, b = set(gpu_idx.tolist()), set(or_idx.tolist())
+    if a == b:
+        return True, False
+    extra, missing = sorted(a - b), sorted(b - a)
+    if len(extra) != len(missing):
+        return False, True
+    key = or_score.astype(np.float32).astype(np.float64)
+    lo = min(key[j] for j in missing)          # weakest oracle-kept key
+    hi = max(key[j] for j in extra)            # strongest GPU-only key
+    ok = abs(lo - hi) <= IDX_REL_GAP * max(abs(lo), abs(hi))
+    return ok, True
+
+
+def compare_head(g, h, r, Ohat_or, report):
+    off0, off1 = g["offsets"][h], g["offsets"][h + 1]
+    gi = g["idx"][off0:off1]
+    ok, swapped = idx_check(gi, r.idx, r.score)
+    report["idx_swapped"] = swapped
+    assert ok, f"head {h}: index sets differ beyond the exemption"
+    assert np.all(np.diff(gi) > 0), "indices not ascending"
+    wg = g["w"][off0:off1]
+    bg = g["beta"][off0:off1]
+    wo, bo = r.w, r.beta
+    wmax = wo.max()
+    big = wo >= BETA_W_FLOOR * wmax
+    db = np.abs(bg[big] - bo[big])
+    report["beta_max_abs"] = float(db.max()) if db.size else 0.0
+    assert np.all(np.isfinite(bg[big])) and report["beta_max_abs"] <= BETA_ABS, f"head {h}: beta {report['beta_max_abs']}"
+    dw = np.abs(wg[~big] - wo[~big])
+    report["w_small_max_abs"] = float(dw.max() / wmax) if dw.size else 0.0
+    assert report["w_small_max_abs"] <= W_ABS_BELOW, f"head {h}: small weights {report['w_small_max_abs']}"
+    np.testing.assert_allclose(np.exp(bg[wg > 0]), wg[wg > 0], rtol=2e-6)
+    assert np.all(np.isneginf(bg[wg == 0]))
+    cv = g["Cv"][off0:off1]
+    report["cv_rel"] = float(np.linalg.norm(cv - r.Cv) / np.linalg.norm(r.Cv))
+    assert report["cv_rel"] <= CV_REL, f"head {h}: C_v rel {report['cv_rel']}"
+    report["ohat_rel"] = float(np.linalg.norm(g["Ohat"][h] - Ohat_or) / np.linalg.norm(Ohat_or))
+    assert report["ohat_rel"] <= OHAT_REL, f"head {h}: held-out rel {report['ohat_rel']}"
+    return report
