@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Throughput of Attention Matching KV compaction on B300.
+
+One step = one kvc_compact call over every head of the workload (all steps
+of the compaction: logits/lse/outputs, key scores, top-t, gather, mass
+matrix, NNLS for beta, least squares for C_v), inputs resident in HBM.
+Metric: compacted head-tokens per second = sum over heads of T / step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+
+N > 1 runs one independent replica per GPU (launched by torch.distributed.run):
+heads are independent, so each rank compacts its own sequences with no
+collective on the data path; only the timing barrier and a max-reduction of
+the step time cross ranks (weak scaling).
+
+--impl reference times the float64 CPU oracle (the only other
+implementation of this method that exists) on the host cores, one head per
+step, in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, budgets as make_budgets  # noqa: E402
+
+# fp32 FFMA peak of a B300 (148 SMs x 128 lanes x 2 flop x 2032 MHz), for
+# kernels that run on the CUDA cores.
+SIMT_F32_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            j = json.load(fh)
+        return j, "measured"
+    except OSError:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.lines: list[str] = []
+        self.proc = None
+        self.th = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 3.0:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=2)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- work model
+def stage_work(w, buds):
+    """Algorithmic work per stage for one call: (kind, amount, unit).
+
+    flops count a multiply-add as 2; symmetric Grams count only the distinct
+    entries; bytes are the minimum the stage must move through HBM."""
+    H, n, T, d = w.H, w.n, w.T, w.d
+    b_in = 2 if w.dtype == "bf16" else 4
+    t = [int(x) for x in buds]
+    st = sum(t)
+    return {
+        "attn_fwd": ("flops", 4.0 * n * T * d * H),
+        "colscore": ("flops", 2.0 * n * T * d * H),
+        "select": ("bytes", 4.0 * T * H + 4.0 * st),
+        "gather": ("bytes", 2.0 * st * d * b_in + st * d * (b_in + 4) + 4.0 * st),
+        "masslogits": ("flops", 2.0 * n * d * st),
+        "gram_a": ("flops", float(sum(n * ti * (ti + 1) for ti in t))),
+        "chol_h": ("flops", float(sum(ti ** 3 / 3.0 for ti in t))),
+        "gram_x": ("flops", float(sum(n * ti * (ti + 1) for ti in t))),
+        "xto": ("flops", 2.0 * n * d * st),
+        "chol_m": ("flops", float(sum(ti ** 3 / 3.0 for ti in t))),
+        "cholsolve": ("flops", float(sum(2.0 * ti * ti * d for ti in t))),
+    }
+
+
+# tensor-core kernels report against the bf16 tensor peak; the others run on
+# the CUDA cores (fp32 FFMA) or are memory-bound
+TENSOR_STAGES: set[str] = set()
+
+
+def roofline_for(stage, per_launch_ms, work, peaks, peak_src, traffic):
+    kind, amount = work
+    if kind == "bytes":
+        ach = amount / (per_launch_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic, "kernel": stage,
+                "peak_source": f"{peak_src} hbm_gbs"}
+    ach = amount / (per_launch_ms * 1e-3) / 1e12
+    if stage in TENSOR_STAGES:
+        pk = peaks["bf16_tflops"]
+        return {"bound": "tensor", "achieved": round(ach, 2), "peak": pk, "unit": "TFLOP/s",
+                "frac": round(ach / pk, 4), "traffic": traffic, "kernel": stage,
+                "peak_source": f"{peak_src} bf16_tflops (burst)"}
+    return {"bound": "alu", "achieved": round(ach, 3), "peak": round(SIMT_F32_PEAK_TFLOPS, 2), "unit": "TFLOP/s",
+            "frac": round(ach / SIMT_F32_PEAK_TFLOPS, 4), "traffic": traffic, "kernel": stage,
+            "peak_source": "derived fp32 FFMA peak 148 SM x 128 lanes x 2 x 2032 MHz"}
+
+
+# --------------------------------------------------------------- CPU oracle
+def time_oracle(w, heads, buds):
+    """Seconds per head of the float64 oracle, and the BLAS threads it used."""
+    import numpy as np
+    import oracle
+    from workloads import forced_mask, head_inputs
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"] or [1])
+    except Exception:  # noqa: BLE001
+        cores = 1
+    forced = forced_mask(w) if (w.keep_first or w.keep_last) else None
+    times = []
+    for h in heads:
+        x = head_inputs(w, h, with_test=False)
+        Q, K, V = (oracle.decode(x[k], w.dtype) for k in "QKV")
+        t0 = time.perf_counter()
+        oracle.compact_head(Q, K, V, int(buds[h]), forced=forced)
+        times.append(time.perf_counter() - t0)
+    return times, cores
+
+
+def config_dict(w, buds, world):
+    return {"workload": w.name, "heads_per_gpu": w.H, "n": w.n, "T": w.T, "d": w.d,
+            "t": (w.t if w.t is not None else f"nonuniform mean {float(sum(buds)) / len(buds):.1f}"),
+            "input_dtype": w.dtype, "keep_first": w.keep_first, "keep_last": w.keep_last,
+            "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"}
+
+
+# --------------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    w = WORKLOADS[args.config]
+    buds = make_budgets(w)
+    n_steps = args.warmup + args.steps
+    heads = [i % w.H for i in range(n_steps)]
+    times, cores = time_oracle(w, heads, buds)
+    timed = times[args.warmup:]
+    sec = sum(timed)
+    value = w.T * len(timed) / sec
+    line = {
+        "impl": "reference", "metric": "compacted KV head-tokens/sec", "value": round(value, 2),
+        "unit": "head-tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sec / len(timed), 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator, workload shapes of the pages)",
+        "config": config_dict(w, buds, 1),
+        "cpu_baseline": {"value": round(value, 2), "unit": "head-tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"one KV head per step ({len(timed)} timed heads of {w.H})"},
+        "e2e": {"value": round(value, 2), "unit": "head-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import dataclasses
+
+    import numpy as np
+    import torch
+
+    import kv_cache_compaction_03_b300 as kvc
+    from workloads.batch import generate
+
+    base = WORKLOADS[args.config]
+    w = dataclasses.replace(base, seq_offset=rank * base.seqs) if world > 1 else base
+    buds = make_budgets(w)
+    inputs = generate(w)                     # spawn pool, before any CUDA call
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+
+    def dev_tensor(a):
+        t = torch.from_numpy(a.view(np.int16) if w.dtype == "bf16" else a)
+        if w.dtype == "bf16":
+            t = t.view(torch.bfloat16)
+        return t.to(dev)
+
+    Q, K, V = dev_tensor(inputs["Q"]), dev_tensor(inputs["K"]), dev_tensor(inputs["V"])
+    b_dev = torch.from_numpy(buds.astype(np.int32)).to(dev)
+    offsets = torch.zeros(w.H + 1, dtype=torch.int32, device=dev)
+    offsets[1:] = torch.cumsum(b_dev.to(torch.int64), 0).to(torch.int32)
+    total = int(buds.sum())
+    max_t = int(buds.max())
+    prob = kvc.make_problem(w.H, w.n, w.T, w.d, kvc.DTYPE_BF16 if w.dtype == "bf16" else kvc.DTYPE_F32, max_t)
+    prm = kvc.default_params(keep_first=w.keep_first, keep_last=w.keep_last, flags=kvc.FLAG_STAGE_TIMING)
+    ws_bytes = kvc.workspace_size(prob, prm)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    idx = torch.empty(total, dtype=torch.int32, device=dev)
+    Ck = torch.empty(total, w.d, dtype=tdt, device=dev)
+    beta = torch.empty(total, dtype=torch.float32, device=dev)
+    Cv = torch.empty(total, w.d, dtype=torch.float32, device=dev)
+    status = torch.empty(w.H, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        rc = kvc.compact(prob, prm, Q, K, V, b_dev, offsets, idx, Ck, beta, Cv, status, ws, ws_bytes, stream)
+        if rc:
+            raise kvc.KvcError(rc, "kvc_compact")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st_host = status.cpu().numpy()
+    if not np.all(st_host == 0):
+        raise RuntimeError(f"head status not OK after warm-up: {st_host.tolist()}")
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms, stage_acc, launches = [], {}, 0
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        stages, nl = kvc.stage_times()          # waits for this step's last stage
+        launches += nl
+        e1.synchronize()
+        step_ms.append(e0.elapsed_time(e1))
+        for name, ms, cnt in stages:
+            a = stage_acc.setdefault(name, [0.0, 0])
+            a[0] += ms
+            a[1] += cnt
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * w.H * w.T / (ms_per_step * 1e-3)
+
+    # ---- end to end: pinned host inputs in, compacted cache out, every step
+    hQ, hK, hV = (torch.from_numpy(inputs[k].view(np.int16) if w.dtype == "bf16" else inputs[k]).pin_memory()
+                  for k in "QKV")
+    hb = torch.from_numpy(buds.astype(np.int32)).pin_memory()
+    o_idx = torch.empty(total, dtype=torch.int32).pin_memory()
+    o_Ck = torch.empty(total * w.d * (2 if w.dtype == "bf16" else 4), dtype=torch.uint8).pin_memory()
+    o_beta = torch.empty(total, dtype=torch.float32).pin_memory()
+    o_Cv = torch.empty(total, w.d, dtype=torch.float32).pin_memory()
+    o_st = torch.empty(w.H, dtype=torch.int32).pin_memory()
+    Qr = Q.view(torch.int16) if w.dtype == "bf16" else Q
+    Kr = K.view(torch.int16) if w.dtype == "bf16" else K
+    Vr = V.view(torch.int16) if w.dtype == "bf16" else V
+    h2d = sum(x.numel() * x.element_size() for x in (hQ, hK, hV, hb))
+    d2h = sum(x.numel() * x.element_size() for x in (o_idx, o_Ck, o_beta, o_Cv, o_st))
+    e2e_ms = []
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        Qr.copy_(hQ, non_blocking=True)
+        Kr.copy_(hK, non_blocking=True)
+        Vr.copy_(hV, non_blocking=True)
+        b_dev.copy_(hb, non_blocking=True)
+        step()
+        o_idx.copy_(idx, non_blocking=True)
+        o_Ck.copy_(Ck.view(torch.uint8).view(-1), non_blocking=True)
+        o_beta.copy_(beta, non_blocking=True)
+        o_Cv.copy_(Cv, non_blocking=True)
+        o_st.copy_(status, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_total = sum(e2e_ms)
+    if dist:
+        t = torch.tensor([e2e_total], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_value = world * w.H * w.T / (e2e_total / args.steps * 1e-3)
+    if not np.all(o_st.numpy() == 0):
+        raise RuntimeError("head status not OK in the end-to-end loop")
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = _peaks()
+    work = stage_work(w, buds)
+    per_stage = {}
+    for name, (ms, cnt) in stage_acc.items():
+        entry = {"ms_per_step": round(ms / args.steps, 4), "share": round(ms / max(1e-9, sum(a[0] for a in stage_acc.values())), 4),
+                 "launches_per_step": cnt // args.steps}
+        if name in work:
+            r = roofline_for(name, ms / args.steps, work[name], peaks, peak_src, None)
+            entry.update({"bound": r["bound"], "achieved": r["achieved"], "unit": r["unit"], "frac": r["frac"]})
+        per_stage[name] = entry
+    dom = max((n for n in stage_acc if n in work), key=lambda n: stage_acc[n][0])
+    traffic = _traffic_for(dom, args.config)
+    roof = roofline_for(dom, stage_acc[dom][0] / args.steps, work[dom], peaks, peak_src, traffic)
+
+    # ---- CPU oracle on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        sample_heads = list(range(min(w.H, 8)))
+        times, cores = time_oracle(w, sample_heads, buds)
+        per_head = sum(times) / len(times)
+        cpu = {"value": round(w.T / per_head, 2), "unit": "head-tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{len(times)} of {w.H} KV heads, {per_head:.2f} s per head (float64 numpy)"}
+
+    line = {
+        "metric": "compacted KV head-tokens/sec", "value": round(value, 1), "unit": "head-tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if not TENSOR_STAGES else "bf16",
+        "data": "synthetic (seeded generator, workload shapes of the pages)",
+        "config": config_dict(w, buds, world),
+        "e2e": {"value": round(e2e_value, 1), "unit": "head-tokens/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(launches),
+        "roofline": roof,
+        "stages": per_stage,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def _traffic_for(stage, cfg):
+    """DRAM bytes per launch of `stage` from a committed ncu summary, if any."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            j = json.load(fh)
+        return j.get(f"{stage}/config{cfg}")
+    except (OSError, ValueError):
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -75,13 +75,18 @@ typedef struct kvc_params {
     float eps_mu;         /* NNLS ridge toward w = 1: mu = eps_mu * tr(G)/t (1e-2) */
     float eps_lambda;     /* C_v ridge toward V[idx]: lambda = eps_lambda *
                              tr(X^T X)/t (1e-2)                                   */
-    int32_t nnls_max_iter;  /* block-pivoting iterations (default 32)             */
+    int32_t nnls_max_iter;  /* block-pivoting iterations (default 12)             */
     int32_t nnls_max_zero;  /* cap on weights held at zero (default 512)          */
     int32_t refine_iters;   /* NNLS iterative-refinement steps (default 2)        */
     int32_t keep_first;     /* positions [0, keep_first) are always kept          */
     int32_t keep_last;      /* positions [T-keep_last, T) are always kept         */
-    uint32_t flags;         /* reserved, must be 0                                */
+    uint32_t flags;         /* KVC_FLAG_* bits; other bits must be 0              */
 } kvc_params;
+
+/* kvc_params.flags: record a CUDA event on the stream after every stage of
+ * kvc_compact, readable with kvc_stage_times (the events are created once per
+ * host thread on first use and kept until exit). */
+#define KVC_FLAG_STAGE_TIMING 1u
 
 /* Fill *prm with the defaults listed above.  Returns KVC_ERR_INVALID_ARG for a
  * null pointer. */
@@ -150,6 +155,18 @@ kvc_status kvc_attend(const kvc_problem* p, const void* Q, int32_t n_q,
                       const void* C_k, const float* beta, const float* C_v,
                       const int32_t* offsets, float* O_out, int32_t* head_status,
                       float scale, kvc_stream_t stream);
+
+/* Device time of each stage of the last kvc_compact call made on this host
+ * thread with KVC_FLAG_STAGE_TIMING (measuring instrumentation; no
+ * counterpart on the page).  Blocks until that call's last stage finished.
+ *   n_stages  out: number of stages recorded (0 if no timed call yet)
+ *   ms, names, counts  out, host arrays of `cap` entries: stage duration in
+ *             milliseconds, static stage name, kernel launches in the stage
+ *   launches  out (may be NULL): kernel launches of the last kvc_compact call
+ *             (timed or not) on this thread
+ * Errors: INVALID_ARG (null n_stages, or null arrays with cap > 0), CUDA. */
+kvc_status kvc_stage_times(int32_t* n_stages, float* ms, const char** names, int32_t* counts,
+                           int32_t* launches, int32_t cap);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* kvc_status_string(kvc_status s);

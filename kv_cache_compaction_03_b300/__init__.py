@@ -59,7 +59,8 @@ class KvcError(RuntimeError):
 
 _lib = None
 EXPORTS = ("kvc_default_params", "kvc_workspace_size", "kvc_workspace_offset", "kvc_compact",
-           "kvc_attend", "kvc_status_string", "kvc_version")
+           "kvc_attend", "kvc_stage_times", "kvc_status_string", "kvc_version")
+FLAG_STAGE_TIMING = 1
 
 
 def lib() -> ctypes.CDLL:
@@ -77,6 +78,9 @@ def lib() -> ctypes.CDLL:
     L.kvc_workspace_offset.argtypes = [P, PP, i32, ctypes.POINTER(sz)]
     L.kvc_compact.argtypes = [P, PP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.kvc_attend.argtypes = [P, vp, i32, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp]
+    L.kvc_stage_times.argtypes = [ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_float),
+                                  ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i32), ctypes.POINTER(i32), i32]
+    L.kvc_stage_times.restype = ctypes.c_int
     L.kvc_status_string.argtypes = [ctypes.c_int]
     L.kvc_status_string.restype = ctypes.c_char_p
     L.kvc_version.restype = ctypes.c_char_p
@@ -157,6 +161,20 @@ def attend(problem: Problem, Q, n_q: int, C_k, beta, C_v, offsets, O_out, head_s
     """kvc_attend on caller-owned buffers.  Returns the call-level status."""
     return lib().kvc_attend(ctypes.byref(problem), _ptr(Q), int(n_q), _ptr(C_k), _ptr(beta), _ptr(C_v),
                             _ptr(offsets), _ptr(O_out), _ptr(head_status), float(scale), _stream(stream))
+
+
+def stage_times(cap: int = 32):
+    """[(name, ms, kernel_launches)] of the last timed kvc_compact on this thread,
+    and the launch count of the last kvc_compact call."""
+    n = ctypes.c_int32()
+    ms = (ctypes.c_float * cap)()
+    names = (ctypes.c_char_p * cap)()
+    counts = (ctypes.c_int32 * cap)()
+    launches = ctypes.c_int32()
+    rc = lib().kvc_stage_times(ctypes.byref(n), ms, names, counts, ctypes.byref(launches), cap)
+    if rc:
+        raise KvcError(rc, "kvc_stage_times")
+    return [(names[i].decode(), float(ms[i]), int(counts[i])) for i in range(min(n.value, cap))], launches.value
 
 
 # ------------------------------------------------------------------ helpers

@@ -94,21 +94,5 @@ struct HeadScalars {
 };
 
 
-// Arguments of the NNLS kernels (per-head buffers carved from the workspace).
-struct NnlsArgs {
-    const float* L;        // factor of H per head [H][ldA][ldA]
-    const float* f;        // rhs, off-indexed
-    const int32_t* offsets;
-    int64_t ldA;
-    float* x;              // solution, off-indexed
-    int8_t* zflag;         // zero-set flags, off-indexed
-    float* W;              // [H][ldA][zmax] columns of H^{-1} on the zero set
-    float* S;              // [H][zmax][zmax] factor of (H^{-1})_ZZ
-    int32_t* zlist;        // unused (the zero-set list lives in shared memory)
-    HeadScalars* hs;
-    int32_t* status;
-    int zmax;
-    int max_iter;
-};
 
 }  // namespace kvc

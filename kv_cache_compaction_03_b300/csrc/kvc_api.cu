@@ -29,19 +29,72 @@ cudaError_t launch_ridge_g(float*, const float*, const int32_t*, int, int64_t, f
 cudaError_t launch_ridge_m(int, float*, float*, const float*, const int32_t*, int, int64_t, float, HeadScalars*,
                            int32_t*, cudaStream_t);
 cudaError_t launch_xsoftmax(float*, const float*, const int32_t*, int, int, int64_t, const int32_t*, cudaStream_t);
-cudaError_t launch_chol(float*, const int32_t*, int, int, int64_t, int32_t*, cudaStream_t);
+cudaError_t launch_chol(float*, const int32_t*, int, int, int64_t, float*, int32_t*, cudaStream_t);
+int chol_launches(int max_t);
 cudaError_t launch_cholsolve(int, const float*, const float*, const int32_t*, int, int64_t, float*, const int32_t*,
                              cudaStream_t);
-cudaError_t launch_nnls(const NnlsArgs&, int, cudaStream_t);
-cudaError_t launch_nnls_refine(const NnlsArgs&, const float*, float*, float*, int, int, int, cudaStream_t);
+cudaError_t launch_nnls_all(const float* L, const float* f, const int32_t* offsets, int H, int n, int max_t,
+                            int64_t ldA, const float* L2, float* x, float* x0, int8_t* zflag, int32_t* zlist,
+                            int32_t* nz, float* W, float* S, int32_t* piv, float* u, float* r, float* d0,
+                            HeadScalars* hs, int zmax, int max_iter, int refine_iters, int32_t* status,
+                            cudaStream_t st, int* launches);
 cudaError_t launch_beta_out(float*, const int32_t*, int, int, float*, const int32_t*, cudaStream_t);
 
 constexpr int kMaxT = 4096;     // largest budget the per-head solvers support
+constexpr int kMaxStages = 32;
+
+// Optional per-stage CUDA events (KVC_FLAG_STAGE_TIMING), recorded on the
+// caller's stream between stages; read back by kvc_stage_times.  One record
+// per host thread (the last timed call).
+struct StageLog {
+    bool created = false;
+    int n = 0;
+    int launches = 0;
+    const char* names[kMaxStages];
+    int counts[kMaxStages];
+    cudaEvent_t ev[kMaxStages + 1];
+};
+static thread_local StageLog g_log;
+static thread_local int g_last_launches = 0;
+
+struct StageClock {
+    bool on;
+    cudaStream_t st;
+    int launches = 0;
+    StageClock(bool enable, cudaStream_t s) : on(enable), st(s) {
+        if (!on) return;
+        if (!g_log.created) {
+            for (int i = 0; i <= kMaxStages; ++i) cudaEventCreate(&g_log.ev[i]);
+            g_log.created = true;
+        }
+        g_log.n = 0;
+        cudaEventRecord(g_log.ev[0], st);
+    }
+    void stage(const char* name, int count) {
+        launches += count;
+        if (!on || g_log.n >= kMaxStages) return;
+        g_log.names[g_log.n] = name;
+        g_log.counts[g_log.n] = count;
+        cudaEventRecord(g_log.ev[g_log.n + 1], st);
+        ++g_log.n;
+    }
+    void finish() {
+        g_last_launches = launches;
+        if (on) g_log.launches = launches;
+    }
+};
+
+#define KVC_STAGE(name, count, call)                   \
+    do {                                               \
+        cudaError_t _e = (call);                       \
+        if (_e != cudaSuccess) return KVC_ERR_CUDA;    \
+        clk.stage(name, count);                        \
+    } while (0)
 
 struct Layout {
     int64_t ldA;
     int zmax;
-    size_t O, lse2, score, L2, Vsel, G, b, f, x, u, r, R, zflag, W, S, hs, total;
+    size_t O, lse2, score, L2, Vsel, G, dscr, b, f, x, x0, d0, u, r, R, zflag, zlist, nz, piv, W, S, hs, total;
 };
 
 static size_t carve(size_t& cur, size_t bytes) {
@@ -63,14 +116,20 @@ static Layout make_layout(const kvc_problem& p, const kvc_params& prm) {
     L.L2 = carve(c, H * n * ldA * 4);
     L.Vsel = carve(c, H * mt * d * 4);
     L.G = carve(c, H * ldA * ldA * 4);
+    L.dscr = carve(c, H * 64 * 64 * 4);
     L.b = carve(c, H * mt * 4);
     L.f = carve(c, H * mt * 4);
     L.x = carve(c, H * mt * 4);
+    L.x0 = carve(c, H * mt * 4);
+    L.d0 = carve(c, H * mt * 4);
     L.u = carve(c, H * n * 4);
     L.r = carve(c, H * mt * 4);
     L.R = carve(c, H * mt * d * 4);
     L.zflag = carve(c, H * mt);
-    L.W = carve(c, H * ldA * zm * 4);
+    L.zlist = carve(c, H * zm * 4);
+    L.nz = carve(c, H * 4);
+    L.piv = carve(c, H * 16);
+    L.W = carve(c, H * zm * ldA * 4);
     L.S = carve(c, H * zm * zm * 4);
     L.hs = carve(c, H * sizeof(HeadScalars));
     L.total = (size_t)round_up((int64_t)c, 256);
@@ -93,7 +152,7 @@ static kvc_status check_params(const kvc_params& q, const kvc_problem& p) {
     if (!(q.eps_mu > 0.f) || !(q.eps_lambda > 0.f) || !std::isfinite(q.eps_mu) || !std::isfinite(q.eps_lambda))
         return KVC_ERR_INVALID_ARG;
     if (q.nnls_max_iter < 1 || q.nnls_max_zero < 1 || q.refine_iters < 0) return KVC_ERR_INVALID_ARG;
-    if (q.keep_first < 0 || q.keep_last < 0 || q.flags != 0) return KVC_ERR_INVALID_ARG;
+    if (q.keep_first < 0 || q.keep_last < 0 || (q.flags & ~KVC_FLAG_STAGE_TIMING) != 0) return KVC_ERR_INVALID_ARG;
     if ((int64_t)q.keep_first + q.keep_last > p.T) return KVC_ERR_INVALID_ARG;
     return KVC_OK;
 }
@@ -121,7 +180,7 @@ kvc_status kvc_default_params(kvc_params* prm) {
     prm->scale = 0.f;
     prm->eps_mu = 1e-2f;
     prm->eps_lambda = 1e-2f;
-    prm->nnls_max_iter = 32;
+    prm->nnls_max_iter = 12;
     prm->nnls_max_zero = 512;
     prm->refine_iters = 2;
     return KVC_OK;
@@ -182,6 +241,7 @@ kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* 
     float* L2 = (float*)(ws + L.L2);
     float* Vsel = (float*)(ws + L.Vsel);
     float* G = (float*)(ws + L.G);
+    float* dscr = (float*)(ws + L.dscr);
     float* b = (float*)(ws + L.b);
     float* f = (float*)(ws + L.f);
     float* x = (float*)(ws + L.x);
@@ -189,6 +249,11 @@ kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* 
     float* r = (float*)(ws + L.r);
     float* R = (float*)(ws + L.R);
     int8_t* zflag = (int8_t*)(ws + L.zflag);
+    int32_t* zlist = (int32_t*)(ws + L.zlist);
+    int32_t* nzv = (int32_t*)(ws + L.nz);
+    int32_t* piv = (int32_t*)(ws + L.piv);
+    float* x0 = (float*)(ws + L.x0);
+    float* d0 = (float*)(ws + L.d0);
     float* W = (float*)(ws + L.W);
     float* S = (float*)(ws + L.S);
     HeadScalars* hs = (HeadScalars*)(ws + L.hs);
@@ -197,25 +262,29 @@ kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* 
     const int forced = std::min(T, q.keep_first + q.keep_last);
     const float c2 = log2_scale(*p, q.scale);
 
-    KVC_TRY(launch_validate(budgets, offsets, H, T, mt, forced, head_status, hs, st));
-    KVC_TRY(launch_attn_fwd_simt(dt, d, Q_ref, K, V, H, n, T, c2, O, lse2, head_status, st));
-    KVC_TRY(launch_colscore_simt(dt, d, Q_ref, K, lse2, H, n, T, c2, score, head_status, st));
-    KVC_TRY(launch_select(score, H, T, offsets, q.keep_first, q.keep_last, idx_out, head_status, st));
-    KVC_TRY(launch_gather(dt, d, K, V, H, T, mt, offsets, idx_out, C_k, Vsel, head_status, st));
-    KVC_TRY(launch_masslogits(dt, d, Q_ref, C_k, lse2, offsets, H, n, mt, L.ldA, c2, L2, head_status, st));
-    KVC_TRY(launch_gram(true, L2, offsets, H, n, mt, L.ldA, G, b, head_status, st));
-    KVC_TRY(launch_ridge_g(G, b, offsets, H, L.ldA, q.eps_mu, f, hs, head_status, st));
-    KVC_TRY(launch_chol(G, offsets, H, mt, L.ldA, head_status, st));
-    NnlsArgs na{G, f, offsets, L.ldA, x, zflag, W, S, nullptr, hs, head_status, L.zmax, q.nnls_max_iter};
-    KVC_TRY(launch_nnls(na, H, st));
-    for (int it = 0; it < q.refine_iters; ++it) KVC_TRY(launch_nnls_refine(na, L2, u, r, H, n, mt, st));
-    KVC_TRY(launch_beta_out(x, offsets, H, mt, beta, head_status, st));
-    KVC_TRY(launch_xsoftmax(L2, x, offsets, H, n, L.ldA, head_status, st));
-    KVC_TRY(launch_gram(false, L2, offsets, H, n, mt, L.ldA, G, nullptr, head_status, st));
-    KVC_TRY(launch_xto(d, L2, O, offsets, H, n, mt, L.ldA, R, head_status, st));
-    KVC_TRY(launch_ridge_m(d, G, R, Vsel, offsets, H, L.ldA, q.eps_lambda, hs, head_status, st));
-    KVC_TRY(launch_chol(G, offsets, H, mt, L.ldA, head_status, st));
-    KVC_TRY(launch_cholsolve(d, G, R, offsets, H, L.ldA, C_v, head_status, st));
+    StageClock clk(q.flags & KVC_FLAG_STAGE_TIMING, st);
+    KVC_STAGE("validate", 1, launch_validate(budgets, offsets, H, T, mt, forced, head_status, hs, st));
+    KVC_STAGE("attn_fwd", 1, launch_attn_fwd_simt(dt, d, Q_ref, K, V, H, n, T, c2, O, lse2, head_status, st));
+    KVC_STAGE("colscore", 1, launch_colscore_simt(dt, d, Q_ref, K, lse2, H, n, T, c2, score, head_status, st));
+    KVC_STAGE("select", 1, launch_select(score, H, T, offsets, q.keep_first, q.keep_last, idx_out, head_status, st));
+    KVC_STAGE("gather", 1, launch_gather(dt, d, K, V, H, T, mt, offsets, idx_out, C_k, Vsel, head_status, st));
+    KVC_STAGE("masslogits", 1,
+              launch_masslogits(dt, d, Q_ref, C_k, lse2, offsets, H, n, mt, L.ldA, c2, L2, head_status, st));
+    KVC_STAGE("gram_a", 1, launch_gram(true, L2, offsets, H, n, mt, L.ldA, G, b, head_status, st));
+    KVC_STAGE("ridge_g", 1, launch_ridge_g(G, b, offsets, H, L.ldA, q.eps_mu, f, hs, head_status, st));
+    KVC_STAGE("chol_h", chol_launches(mt), launch_chol(G, offsets, H, mt, L.ldA, dscr, head_status, st));
+    int nnls_launches = 0;
+    KVC_STAGE("nnls", nnls_launches,
+              launch_nnls_all(G, f, offsets, H, n, mt, L.ldA, L2, x, x0, zflag, zlist, nzv, W, S, piv, u, r, d0, hs,
+                              L.zmax, q.nnls_max_iter, q.refine_iters, head_status, st, &nnls_launches));
+    KVC_STAGE("beta", 1, launch_beta_out(x, offsets, H, mt, beta, head_status, st));
+    KVC_STAGE("xsoftmax", 1, launch_xsoftmax(L2, x, offsets, H, n, L.ldA, head_status, st));
+    KVC_STAGE("gram_x", 1, launch_gram(false, L2, offsets, H, n, mt, L.ldA, G, nullptr, head_status, st));
+    KVC_STAGE("xto", 1, launch_xto(d, L2, O, offsets, H, n, mt, L.ldA, R, head_status, st));
+    KVC_STAGE("ridge_m", 1, launch_ridge_m(d, G, R, Vsel, offsets, H, L.ldA, q.eps_lambda, hs, head_status, st));
+    KVC_STAGE("chol_m", chol_launches(mt), launch_chol(G, offsets, H, mt, L.ldA, dscr, head_status, st));
+    KVC_STAGE("cholsolve", 1, launch_cholsolve(d, G, R, offsets, H, L.ldA, C_v, head_status, st));
+    clk.finish();
     return KVC_OK;
 }
 
@@ -233,6 +302,27 @@ kvc_status kvc_attend(const kvc_problem* p, const void* Q, int32_t n_q, const vo
     KVC_TRY(cudaMemsetAsync(head_status, 0, sizeof(int32_t) * p->H, st));
     KVC_TRY(launch_attend(p->dtype, p->d, Q, n_q, C_k, beta, C_v, offsets, p->H, log2_scale(*p, scale), O_out,
                           head_status, st));
+    return KVC_OK;
+}
+
+kvc_status kvc_stage_times(int32_t* n_stages, float* ms, const char** names, int32_t* counts, int32_t* launches,
+                           int32_t cap) {
+    if (!n_stages || cap < 0 || (cap > 0 && (!ms || !names || !counts))) return KVC_ERR_INVALID_ARG;
+    if (launches) *launches = g_last_launches;
+    if (!g_log.created || g_log.n == 0) {
+        *n_stages = 0;
+        return KVC_OK;
+    }
+    if (cudaEventSynchronize(g_log.ev[g_log.n]) != cudaSuccess) return KVC_ERR_CUDA;
+    const int m = g_log.n < cap ? g_log.n : cap;
+    for (int i = 0; i < m; ++i) {
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, g_log.ev[i], g_log.ev[i + 1]) != cudaSuccess) return KVC_ERR_CUDA;
+        ms[i] = t;
+        names[i] = g_log.names[i];
+        counts[i] = g_log.counts[i];
+    }
+    *n_stages = g_log.n;
     return KVC_OK;
 }
 

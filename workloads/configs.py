@@ -43,6 +43,7 @@ class Workload:
     n_test: int = 256          # held-out queries per head
     noise_k: float = 0.3       # K = G U + noise_k * N(0,1)
     q_noise_var: float = 0.5   # Q = K[j] + N(0, q_noise_var)
+    seq_offset: int = 0        # first sequence index (replicas draw distinct sequences)
 
     @property
     def H(self) -> int:
@@ -53,7 +54,7 @@ class Workload:
         per_seq = self.layers * self.kv_heads
         s, r = divmod(h, per_seq)
         layer, kv = divmod(r, self.kv_heads)
-        return s, layer, kv
+        return s + self.seq_offset, layer, kv
 
 
 WORKLOADS: dict[int, Workload] = {
