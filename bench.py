@@ -130,8 +130,18 @@ def stage_work(w, buds):
     }
 
 
-# tensor-core kernels report against the bf16 tensor peak; the others run on
-# the CUDA cores (fp32 FFMA) or are memory-bound
+# MUFU ex2 rate of a B300 (148 SMs x 16 per clock x 2032 MHz): the attention
+# passes take one exponential per logit and are co-bound by it.
+MUFU_PEAK_TEXP = 148 * 16 * 2.032e9 / 1e12
+
+
+def tensor_stages(w) -> set[str]:
+    """Stages that run on the tensor cores (bf16 operands, fp32 accumulation)
+    for this workload; the others run on the CUDA cores (fp32 FFMA) or are
+    memory-bound."""
+    return {"attn_fwd", "colscore"} if w.dtype == "bf16" else set()
+
+
 TENSOR_STAGES: set[str] = set()
 
 
@@ -164,6 +174,8 @@ def time_oracle(w, heads, buds):
         cores = max([i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"] or [1])
     except Exception:  # noqa: BLE001
         cores = 1
+    # BLAS threads cannot exceed the cores this process may run on
+    cores = min(cores, len(os.sched_getaffinity(0)))
     forced = forced_mask(w) if (w.keep_first or w.keep_last) else None
     times = []
     for h in heads:
@@ -209,18 +221,39 @@ def run_reference(args, rank, world):
     return 0
 
 
+# --------------------------------------------------------------- sharding
+def rank_workload(base, rank: int, world: int):
+    """The workload replica of `rank`: the same shapes, its own sequences.
+
+    Heads are independent problems, so N ranks compact N disjoint sets of
+    sequences (weak scaling) and exchange nothing on the data path."""
+    import dataclasses
+    if world <= 1:
+        return base
+    return dataclasses.replace(base, seq_offset=base.seq_offset + rank * base.seqs)
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """Largest value of x over all ranks (the job's time is its slowest rank's)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # --------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
-    import dataclasses
-
     import numpy as np
     import torch
 
     import kv_cache_compaction_03_b300 as kvc
     from workloads.batch import generate
 
-    base = WORKLOADS[args.config]
-    w = dataclasses.replace(base, seq_offset=rank * base.seqs) if world > 1 else base
+    w = rank_workload(WORKLOADS[args.config], rank, world)
+    TENSOR_STAGES.clear()
+    TENSOR_STAGES.update(tensor_stages(w))
     buds = make_budgets(w)
     inputs = generate(w)                     # spawn pool, before any CUDA call
 
@@ -293,11 +326,7 @@ def run_ours(args, rank, world, local_rank):
     if dist:
         dist.barrier()
     clocks = sampler.stop()
-    total_ms = sum(step_ms)
-    if dist:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     ms_per_step = total_ms / args.steps
     value = world * w.H * w.T / (ms_per_step * 1e-3)
 
@@ -336,11 +365,7 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    e2e_total = sum(e2e_ms)
-    if dist:
-        t = torch.tensor([e2e_total], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
+    e2e_total = max_over_ranks(sum(e2e_ms), dist, dev)
     e2e_value = world * w.H * w.T / (e2e_total / args.steps * 1e-3)
     if not np.all(o_st.numpy() == 0):
         raise RuntimeError("head status not OK in the end-to-end loop")
@@ -359,6 +384,9 @@ def run_ours(args, rank, world, local_rank):
         if name in work:
             r = roofline_for(name, ms / args.steps, work[name], peaks, peak_src, None)
             entry.update({"bound": r["bound"], "achieved": r["achieved"], "unit": r["unit"], "frac": r["frac"]})
+        if name in ("attn_fwd", "colscore"):
+            texp = w.H * w.n * w.T / (ms / args.steps * 1e-3) / 1e12
+            entry["exp_frac_of_mufu"] = round(texp / MUFU_PEAK_TEXP, 4)
         per_stage[name] = entry
     dom = max((n for n in stage_acc if n in work), key=lambda n: stage_acc[n][0])
     traffic = _traffic_for(dom, args.config)
@@ -377,7 +405,8 @@ def run_ours(args, rank, world, local_rank):
         "metric": "compacted KV head-tokens/sec", "value": round(value, 1), "unit": "head-tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32" if not TENSOR_STAGES else "bf16",
+        "dtype": "bf16" if TENSOR_STAGES else "f32",
+        "solver_dtype": "f32",
         "data": "synthetic (seeded generator, workload shapes of the pages)",
         "config": config_dict(w, buds, world),
         "e2e": {"value": round(e2e_value, 1), "unit": "head-tokens/s", "h2d_bytes_per_step": int(h2d),

@@ -52,7 +52,10 @@ typedef enum kvc_status {
     KVC_ERR_NOT_SPD = 17,      /* a Cholesky pivot was not positive                 */
     KVC_ERR_NNLS_MAXITER = 18, /* NNLS pivoting hit its iteration or set-size cap;
                                   outputs hold the last (clamped) iterate           */
-    KVC_ERR_NONFINITE = 19     /* NaN/Inf in the inputs or an intermediate          */
+    KVC_ERR_NONFINITE = 19,    /* NaN/Inf in the inputs or an intermediate          */
+    KVC_ERR_TIMEOUT = 20       /* a bounded device-side wait gave up (about one
+                                  second without progress); the kernel released
+                                  its resources and left the head unfinished       */
 } kvc_status;
 
 typedef enum kvc_dtype { KVC_DTYPE_BF16 = 0, KVC_DTYPE_F32 = 1 } kvc_dtype;

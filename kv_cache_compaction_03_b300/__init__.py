@@ -27,6 +27,7 @@ ERR_BAD_BUDGET = 16
 ERR_NOT_SPD = 17
 ERR_NNLS_MAXITER = 18
 ERR_NONFINITE = 19
+ERR_TIMEOUT = 20
 
 DTYPE_BF16 = 0
 DTYPE_F32 = 1

@@ -38,6 +38,11 @@ cudaError_t launch_nnls_all(const float* L, const float* f, const int32_t* offse
                             int32_t* nz, float* W, float* S, int32_t* piv, float* u, float* r, float* d0,
                             HeadScalars* hs, int zmax, int max_iter, int refine_iters, int32_t* status,
                             cudaStream_t st, int* launches);
+cudaError_t launch_attn_fwd_tc(int d, const void* Q, const void* K, const void* V, int H, int n, int T, float c2,
+                               float* O, float* lse2, int32_t* status, cudaStream_t st);
+cudaError_t launch_colscore_tc(int d, const void* Q, const void* K, const float* lse2, int H, int n, int T,
+                               float c2, float* score, int32_t* status, cudaStream_t st);
+bool tc_maps_available();
 cudaError_t launch_beta_out(float*, const int32_t*, int, int, float*, const int32_t*, cudaStream_t);
 
 constexpr int kMaxT = 4096;     // largest budget the per-head solvers support
@@ -264,8 +269,15 @@ kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* 
 
     StageClock clk(q.flags & KVC_FLAG_STAGE_TIMING, st);
     KVC_STAGE("validate", 1, launch_validate(budgets, offsets, H, T, mt, forced, head_status, hs, st));
-    KVC_STAGE("attn_fwd", 1, launch_attn_fwd_simt(dt, d, Q_ref, K, V, H, n, T, c2, O, lse2, head_status, st));
-    KVC_STAGE("colscore", 1, launch_colscore_simt(dt, d, Q_ref, K, lse2, H, n, T, c2, score, head_status, st));
+    // bf16 inputs take the tensor-core passes (tcgen05/TMEM/TMA); fp32 inputs
+    // the FFMA passes (a tf32 contraction would not keep fp32 accuracy).
+    if (dt == KVC_DTYPE_BF16) {
+        KVC_STAGE("attn_fwd", 1, launch_attn_fwd_tc(d, Q_ref, K, V, H, n, T, c2, O, lse2, head_status, st));
+        KVC_STAGE("colscore", 1, launch_colscore_tc(d, Q_ref, K, lse2, H, n, T, c2, score, head_status, st));
+    } else {
+        KVC_STAGE("attn_fwd", 1, launch_attn_fwd_simt(dt, d, Q_ref, K, V, H, n, T, c2, O, lse2, head_status, st));
+        KVC_STAGE("colscore", 1, launch_colscore_simt(dt, d, Q_ref, K, lse2, H, n, T, c2, score, head_status, st));
+    }
     KVC_STAGE("select", 1, launch_select(score, H, T, offsets, q.keep_first, q.keep_last, idx_out, head_status, st));
     KVC_STAGE("gather", 1, launch_gather(dt, d, K, V, H, T, mt, offsets, idx_out, C_k, Vsel, head_status, st));
     KVC_STAGE("masslogits", 1,
@@ -337,6 +349,7 @@ const char* kvc_status_string(kvc_status s) {
         case KVC_ERR_NOT_SPD: return "matrix not positive definite";
         case KVC_ERR_NNLS_MAXITER: return "NNLS iteration or zero-set cap reached";
         case KVC_ERR_NONFINITE: return "non-finite value";
+        case KVC_ERR_TIMEOUT: return "device-side wait timed out";
     }
     return "unknown status";
 }
