@@ -45,6 +45,8 @@ typedef enum kvc_status {
     KVC_ERR_ALIGN = 2,         /* a tensor pointer is not 16-byte aligned          */
     KVC_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required       */
     KVC_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed       */
+    KVC_ERR_NOALLOC_LIMIT = 5, /* kvc_compact_noalloc: the problem needs more
+                                  scratch than KVC_NOALLOC_SCRATCH_BYTES           */
     /* per-head outcomes (head_status) */
     KVC_ERR_BAD_BUDGET = 16,   /* t_h outside [1, min(T, max_t)], offsets not the
                                   exclusive prefix sum of budgets, or more forced
@@ -141,6 +143,41 @@ kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm,
                        int32_t* idx_out, void* C_k, float* beta, float* C_v,
                        int32_t* head_status,
                        void* workspace, size_t workspace_bytes, kvc_stream_t stream);
+
+/* Size of the fixed device scratch array behind kvc_compact_noalloc (64 MiB).
+ * Every GPU that loads this library holds one such array until the process
+ * exits. */
+#define KVC_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* kvc_compact without a workspace argument, for callers that cannot allocate
+ * device memory: an engine whose allocator has reserved the device's memory
+ * and forbids other allocations, a latency-critical path where cudaMalloc /
+ * cudaFree would synchronise the device, or a C program with no device
+ * allocator.  The page has no counterpart of this entry point; it is an
+ * interface convenience only.
+ *
+ * Arguments, outputs, per-head statuses and results are those of
+ * kvc_compact.  Differences:
+ *  - The scratch is a library-owned device array of KVC_NOALLOC_SCRATCH_BYTES.
+ *    A problem whose kvc_workspace_size exceeds it is rejected with
+ *    KVC_ERR_NOALLOC_LIMIT, and nothing is enqueued.
+ *  - The call allocates and frees nothing: no cudaMalloc, no cudaFree and no
+ *    allocating library routine.  prm->flags must not ask for stage timing,
+ *    since that creates events (INVALID_ARG).
+ *  - The first call on a device looks up the array's device address with
+ *    that device current, and caches it. Make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array, which keeps the last call's
+ *    contents.  The kernels write every scratch value before reading it.
+ *    Calls whose work overlaps on the GPU (different streams, or different
+ *    host threads without ordering) race on the array: order them, or use
+ *    kvc_compact with separate workspaces.
+ * Errors: those of kvc_compact, plus NOALLOC_LIMIT. */
+kvc_status kvc_compact_noalloc(const kvc_problem* p, const kvc_params* prm,
+                               const void* Q_ref, const void* K, const void* V,
+                               const int32_t* budgets, const int32_t* offsets,
+                               int32_t* idx_out, void* C_k, float* beta, float* C_v,
+                               int32_t* head_status, kvc_stream_t stream);
 
 /* Read a compacted cache with a per-key bias (page section 2 objective, and
  * section 5 on use with standard attention kernels):

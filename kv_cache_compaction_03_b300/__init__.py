@@ -23,6 +23,8 @@ ERR_INVALID_ARG = 1
 ERR_ALIGN = 2
 ERR_WORKSPACE = 3
 ERR_CUDA = 4
+ERR_NOALLOC_LIMIT = 5
+NOALLOC_SCRATCH_BYTES = 64 << 20
 ERR_BAD_BUDGET = 16
 ERR_NOT_SPD = 17
 ERR_NNLS_MAXITER = 18
@@ -60,7 +62,7 @@ class KvcError(RuntimeError):
 
 _lib = None
 EXPORTS = ("kvc_default_params", "kvc_workspace_size", "kvc_workspace_offset", "kvc_compact",
-           "kvc_attend", "kvc_stage_times", "kvc_status_string", "kvc_version")
+           "kvc_compact_noalloc", "kvc_attend", "kvc_stage_times", "kvc_status_string", "kvc_version")
 FLAG_STAGE_TIMING = 1
 
 
@@ -78,6 +80,7 @@ def lib() -> ctypes.CDLL:
     L.kvc_workspace_size.argtypes = [P, PP, ctypes.POINTER(sz)]
     L.kvc_workspace_offset.argtypes = [P, PP, i32, ctypes.POINTER(sz)]
     L.kvc_compact.argtypes = [P, PP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.kvc_compact_noalloc.argtypes = [P, PP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.kvc_attend.argtypes = [P, vp, i32, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp]
     L.kvc_stage_times.argtypes = [ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_float),
                                   ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i32), ctypes.POINTER(i32), i32]
@@ -85,7 +88,8 @@ def lib() -> ctypes.CDLL:
     L.kvc_status_string.argtypes = [ctypes.c_int]
     L.kvc_status_string.restype = ctypes.c_char_p
     L.kvc_version.restype = ctypes.c_char_p
-    for f in ("kvc_default_params", "kvc_workspace_size", "kvc_workspace_offset", "kvc_compact", "kvc_attend"):
+    for f in ("kvc_default_params", "kvc_workspace_size", "kvc_workspace_offset", "kvc_compact",
+              "kvc_compact_noalloc", "kvc_attend"):
         getattr(L, f).restype = ctypes.c_int
     _lib = L
     return L
@@ -155,6 +159,16 @@ def compact(problem: Problem, params: Params | None, Q_ref, K, V, budgets, offse
                              _ptr(Q_ref), _ptr(K), _ptr(V), _ptr(budgets), _ptr(offsets), _ptr(idx_out),
                              _ptr(C_k), _ptr(beta), _ptr(C_v), _ptr(head_status), _ptr(workspace),
                              int(workspace_bytes), _stream(stream))
+
+
+def compact_noalloc(problem: Problem, params: Params | None, Q_ref, K, V, budgets, offsets, idx_out, C_k, beta,
+                    C_v, head_status, stream=None) -> int:
+    """kvc_compact_noalloc: kvc_compact with the library's fixed device scratch
+    (no workspace argument; for callers that cannot allocate device memory).
+    Returns the call-level status (0 = enqueued)."""
+    return lib().kvc_compact_noalloc(ctypes.byref(problem), ctypes.byref(params) if params else None,
+                                     _ptr(Q_ref), _ptr(K), _ptr(V), _ptr(budgets), _ptr(offsets), _ptr(idx_out),
+                                     _ptr(C_k), _ptr(beta), _ptr(C_v), _ptr(head_status), _stream(stream))
 
 
 def attend(problem: Problem, Q, n_q: int, C_k, beta, C_v, offsets, O_out, head_status, scale: float = 0.0,

@@ -345,6 +345,7 @@ const char* kvc_status_string(kvc_status s) {
         case KVC_ERR_ALIGN: return "pointer not aligned";
         case KVC_ERR_WORKSPACE: return "workspace missing or too small";
         case KVC_ERR_CUDA: return "CUDA launch or runtime error";
+        case KVC_ERR_NOALLOC_LIMIT: return "problem needs more scratch than the fixed no-allocation array holds";
         case KVC_ERR_BAD_BUDGET: return "bad budget or offsets for this head";
         case KVC_ERR_NOT_SPD: return "matrix not positive definite";
         case KVC_ERR_NNLS_MAXITER: return "NNLS iteration or zero-set cap reached";

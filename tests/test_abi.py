@@ -37,7 +37,7 @@ def test_exports_every_declared_symbol():
 
 def test_version_and_status_strings():
     assert "sm_103a" in kvc.version()
-    for code in (0, 1, 2, 3, 4, 16, 17, 18, 19, 20):
+    for code in (0, 1, 2, 3, 4, 5, 16, 17, 18, 19, 20):
         assert kvc.status_string(code) not in ("", "unknown status")
     assert kvc.status_string(12345) == "unknown status"
 
