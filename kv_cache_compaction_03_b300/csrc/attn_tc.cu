@@ -9,17 +9,20 @@
 //                   log-mass lse_q (log2 units).  A single bf16 term would
 //                   leave O with ~1e-3 relative error, which the least-squares
 //                   fit of C_v amplifies past its tolerance.
+//   k_masslogits_tc log2 of the relative mass matrix A' for the kept keys,
+//                   S = Q C_k^T on the tensor cores.
 //   k_colscore_tc   K-major pass: S^T = K Q^T per key tile, then every key
 //                   row sums exp(2 (S - lse)) over all queries: the RMS
 //                   attention score of each key (key selection aggregated
 //                   by RMS).
 //
-// bf16 inputs, fp32 accumulation.  One CTA = 6 warps:
+// bf16 inputs, fp32 accumulation.  One CTA = 10 warps and two 128-row
+// tiles (query tiles for the forward pass, key tiles for the scores):
 //   warp 0       TMA producer (one elected thread)
 //   warp 1       tcgen05.mma issuer (one elected thread); owns the TMEM
-//                allocation
-//   warps 2..5   consumers, one tile row (query or key) per thread; warp w
-//                reads TMEM lanes 32*(w%4) .. 32*(w%4)+31
+//                allocation (all 512 columns)
+//   warps 2..9   two consumer warpgroups, one per tile, one tile row per
+//                thread; warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31
 // Operand tiles are [128 rows][64 bf16] TMA boxes with 128-byte swizzle; a
 // d = 128 row is two boxes.  Every wait is bounded: a wait that runs out
 // raises a CTA-wide abort flag, writes KVC_ERR_TIMEOUT for the head, lets
@@ -29,12 +32,12 @@
 namespace kvc {
 using namespace tc;
 
+bool make_map(CUtensorMap* m, const void* base, int d, int rows, int H);   // tmap.cu
+
 namespace {
 
 constexpr int TB = 128;                 // tile rows (queries or keys) and keys per tile
 constexpr int kBox = 128 * 128;         // bytes of one [128][64] bf16 box
-constexpr int kThreads = 192;
-constexpr int kConsumer0 = 2;           // first consumer warp
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -57,15 +60,26 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_addr, int kk) {
 template <int D, int NS>
 struct FwdLayout {
     static constexpr int kTile = (D / 64) * kBox;
-    static constexpr int kQ = 0;
-    static constexpr int kK = kQ + kTile;
+    static constexpr int kQ = 0;                  // two query tiles
+    static constexpr int kK = kQ + 2 * kTile;
     static constexpr int kV = kK + NS * kTile;
     static constexpr int kBar = kV + NS * kTile;
     static constexpr int kBytes = kBar + 256 + 1024;     // + alignment slack
 };
+constexpr int kFwdThreads = 320;          // TMA warp, MMA warp, two softmax warpgroups
 
+// One CTA = two query tiles g = 0, 1 of 128 rows (rows q0 + 128 g ..).  TMEM
+// columns: tile g owns S_g at 256 g (128 columns; after the softmax P_hi
+// sits in its first 64 columns and P_lo in the next 64) and O_g at
+// 256 g + 128.  The MMA thread interleaves the tiles so that one tile's
+// softmax overlaps the other tile's products:
+//   QK_0[j], PV_1[j-1], QK_1[j], PV_0[j], QK_0[j+1], PV_1[j], ...
+// tcgen05 operations of one thread complete in issue order, so when S_g[j]
+// is complete every earlier P V product of tile g is too: the softmax may
+// rescale O_g in place without another wait, and QK_g[j+1] may overwrite
+// the P_g[j] that PV_g[j] read.
 template <int D, int NS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kFwdThreads, 1)
     k_attn_fwd_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                   const __grid_constant__ CUtensorMap mV, int n, int T, float c2, float* __restrict__ O,
                   float* __restrict__ lse2, int32_t* __restrict__ status) {
@@ -80,11 +94,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* k_full = bars + 1;
     uint64_t* v_full = k_full + NS;
     uint64_t* kv_empty = v_full + NS;
-    uint64_t* s_full = kv_empty + NS;     // [2]
+    uint64_t* s_full = kv_empty + NS;     // [2] one per query tile
     uint64_t* p_full = s_full + 2;        // [2]
-    uint64_t* o_done = p_full + 2;        // one phase per P V product
-    uint64_t* o_final = o_done + 1;       // the last P V product
-    uint64_t* mma_done = o_final + 1;     // everything the MMA thread issued
+    uint64_t* o_final = p_full + 2;       // [2]
+    uint64_t* mma_done = o_final + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -95,12 +108,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(v_full + s, 1);
             mbar_init(kv_empty + s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(s_full + b, 1);
-            mbar_init(p_full + b, 128);
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(s_full + g, 1);
+            mbar_init(p_full + g, 128);
+            mbar_init(o_final + g, 1);
         }
-        mbar_init(o_done, 1);
-        mbar_init(o_final, 1);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -110,9 +122,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_O = tmem + 256;
     const int nt = (T + TB - 1) / TB;
-    const int q0 = blockIdx.x * TB;
+    const int q0 = blockIdx.x * 2 * TB;
     constexpr uint32_t kTileBytes = (uint32_t)L::kTile;
 
     if (warp == 0) {
@@ -120,8 +131,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&mQ);
             prefetch_tmap(&mK);
             prefetch_tmap(&mV);
-            mbar_expect_tx(q_full, kTileBytes);
-            for (int c = 0; c < D / 64; ++c) tma_load_3d(sm + L::kQ + c * kBox, &mQ, q_full, c * 64, q0, h);
+            mbar_expect_tx(q_full, 2 * kTileBytes);
+            for (int g = 0; g < 2; ++g)
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_3d(sm + L::kQ + g * L::kTile + c * kBox, &mQ, q_full, c * 64, q0 + g * TB, h);
             int issued = 0;
             for (int j = 0; j < nt; ++j) {
                 const int s = j % NS;
@@ -146,36 +159,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
-            const uint32_t aQ = smem_addr(sm + L::kQ);
+            const uint32_t aQ0 = smem_addr(sm + L::kQ);
+            auto qk = [&](int g, int j) {
+                const uint32_t aQ = aQ0 + (uint32_t)(g * L::kTile);
+                const uint32_t aK = smem_addr(sm + L::kK + (j % NS) * L::kTile);
+                const uint32_t dS = tmem + (uint32_t)g * 256;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(dS, kmajor_desc(aQ, kk), kmajor_desc(aK, kk), idesc_qk, kk > 0);
+                mma_commit(s_full + g);
+            };
+            auto pv = [&](int g, int j) {
+                const uint32_t aV = smem_addr(sm + L::kV + (j % NS) * L::kTile);
+                const uint32_t aP = tmem + (uint32_t)g * 256;
+                const uint32_t dO = aP + 128;
+#pragma unroll
+                for (int kk = 0; kk < TB / 16; ++kk) {
+                    const uint64_t bV = sdesc_sw128(aV + kk * 2048, kBox, 1024);
+                    mma_ts(dO, aP + kk * 8, bV, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(dO, aP + 64 + kk * 8, bV, idesc_pv, 1u);
+                }
+                if (j == nt - 1) mma_commit(o_final + g);
+            };
             bool ok = mbar_wait(q_full, 0, abort_flag);
             for (int j = 0; ok && j <= nt; ++j) {
                 if (j < nt) {
-                    const int s = j % NS;
-                    if (!mbar_wait(k_full + s, (uint32_t)(j / NS) & 1u, abort_flag)) break;
+                    if (!mbar_wait(k_full + j % NS, (uint32_t)(j / NS) & 1u, abort_flag)) break;
                     fence_after_sync();
-                    const uint32_t aK = smem_addr(sm + L::kK + s * L::kTile);
-                    const uint32_t dS = tmem + (uint32_t)(j & 1) * 128;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(dS, kmajor_desc(aQ, kk), kmajor_desc(aK, kk), idesc_qk, kk > 0);
-                    mma_commit(s_full + (j & 1));
+                    qk(0, j);
                 }
                 if (j >= 1) {
-                    const int jp = j - 1, sp = jp % NS;
-                    if (!mbar_wait(p_full + (jp & 1), (uint32_t)(jp >> 1) & 1u, abort_flag)) break;
-                    if (!mbar_wait(v_full + sp, (uint32_t)(jp / NS) & 1u, abort_flag)) break;
+                    const int jp = j - 1;
+                    if (!mbar_wait(p_full + 1, (uint32_t)jp & 1u, abort_flag)) break;
+                    if (!mbar_wait(v_full + jp % NS, (uint32_t)(jp / NS) & 1u, abort_flag)) break;
                     fence_after_sync();
-                    const uint32_t aV = smem_addr(sm + L::kV + sp * L::kTile);
-                    const uint32_t aP = tmem + (uint32_t)(jp & 1) * 128;
-#pragma unroll
-                    for (int kk = 0; kk < TB / 16; ++kk) {
-                        const uint64_t bV = sdesc_sw128(aV + kk * 2048, kBox, 1024);
-                        mma_ts(tmem_O, aP + kk * 8, bV, idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
-                        mma_ts(tmem_O, aP + 64 + kk * 8, bV, idesc_pv, 1u);
-                    }
-                    mma_commit(o_done);
-                    if (jp == nt - 1) mma_commit(o_final);
-                    mma_commit(kv_empty + sp);
+                    pv(1, jp);
+                    mma_commit(kv_empty + jp % NS);      // both tiles are done with K, V [jp]
+                }
+                if (j < nt) {
+                    qk(1, j);
+                    if (!mbar_wait(p_full + 0, (uint32_t)j & 1u, abort_flag)) break;
+                    if (!mbar_wait(v_full + j % NS, (uint32_t)(j / NS) & 1u, abort_flag)) break;
+                    fence_after_sync();
+                    pv(0, j);
                 }
             }
             mma_commit(mma_done);
@@ -183,36 +209,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // consumers: one query row per thread
+        // softmax warpgroup g: one query row per thread
+        const int g = (warp - 2) >> 2;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_off + (uint32_t)g * 256;
+        const uint32_t tO = tS + 128;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(s_full + (j & 1), (uint32_t)(j >> 1) & 1u, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full + g, (uint32_t)j & 1u, abort_flag));
             if (!ok) break;
             fence_after_sync();
-            const uint32_t sbase = tmem + lane_off + (uint32_t)(j & 1) * 128;
             float s[128];
             {
                 uint32_t r[32];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(sbase + c * 32, r);
+                    tmem_ld32(tS + c * 32, r);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
                 }
             }
             const int kv = T - j * TB;          // valid keys in this tile (>= 1)
-            float mx = -INFINITY;
+            if (kv < TB) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                const float v = (c < kv) ? s[c] * c2 : -INFINITY;
-                s[c] = v;
-                mx = fmaxf(mx, v);
+                for (int c = 0; c < 128; ++c)
+                    if (c >= kv) s[c] = -INFINITY;
             }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+            mx *= c2;                           // c2 > 0: the maximum commutes with the scale
             // Conditional rescaling: the reference maximum only moves when a
             // row's maximum grows by more than 2^8, so P stays <= 256.
             const bool need = mx > m_used + 8.f;
@@ -222,7 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 corr = ex2(m_used - mx);
                 m_used = mx;
             }
-            // P_hi overwrites columns 0..63 of this S buffer, P_lo columns 64..127
+            const float nm = -m_used;
+            // P_hi overwrites columns 0..63 of S, P_lo columns 64..127
             float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
@@ -230,8 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 32; c += 4) {
                     const int k = cc * 32 + c;
-                    const float p0 = ex2(s[k] - m_used), p1 = ex2(s[k + 1] - m_used);
-                    const float p2 = ex2(s[k + 2] - m_used), p3 = ex2(s[k + 3] - m_used);
+                    const float p0 = ex2(fmaf(s[k], c2, nm)), p1 = ex2(fmaf(s[k + 1], c2, nm));
+                    const float p2 = ex2(fmaf(s[k + 2], c2, nm)), p3 = ex2(fmaf(s[k + 3], c2, nm));
                     ps0 += p0;
                     ps1 += p1;
                     ps2 += p2;
@@ -242,40 +273,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                     lo[c / 2] = pack_bf16(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
                     lo[c / 2 + 1] = pack_bf16(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
                 }
-                tmem_st16(sbase + cc * 16, hi);
-                tmem_st16(sbase + 64 + cc * 16, lo);
+                tmem_st16(tS + cc * 16, hi);
+                tmem_st16(tS + 64 + cc * 16, lo);
             }
             l = l * corr + ((ps0 + ps1) + (ps2 + ps3));
-            tmem_st_wait();
             if (any && j > 0) {
-                // O must hold every earlier P V product before it is rescaled
-                ok = __all_sync(0xffffffffu, mbar_wait(o_done, (uint32_t)(j - 1) & 1u, abort_flag));
-                if (!ok) break;
-                fence_after_sync();
+                // S_g[j] complete => every earlier P V product of this tile is too
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
-                    tmem_ld32(tmem_O + lane_off + c * 32, r);
+                    tmem_ld32(tO + c * 32, r);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
-                    tmem_st32(tmem_O + lane_off + c * 32, r);
+                    tmem_st32(tO + c * 32, r);
                 }
-                tmem_st_wait();
             }
+            tmem_st_wait();
             fence_before_sync();
-            mbar_arrive(p_full + (j & 1));
+            mbar_arrive(p_full + g);
         }
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final, 0, abort_flag));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final + g, 0, abort_flag));
         if (ok) {
             fence_after_sync();
-            const int q = q0 + row;
+            const int q = q0 + g * TB + row;
             const float inv = 1.f / l;
             float* orow = O + ((int64_t)h * n + q) * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tmem_O + lane_off + c * 32, r);
+                tmem_ld32(tO + c * 32, r);
                 tmem_ld_wait();
                 if (q < n) {
 #pragma unroll
@@ -298,19 +325,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------ key scores
 constexpr int kLseChunk = 8192;     // queries whose lse sits in shared memory at once
+constexpr int kColThreads = 320;    // TMA warp, MMA warp, two consumer warpgroups
 
 template <int D, int NS>
 struct ColLayout {
     static constexpr int kTile = (D / 64) * kBox;
-    static constexpr int kK = 0;
-    static constexpr int kQ = kK + kTile;
+    static constexpr int kK = 0;                  // two key tiles
+    static constexpr int kQ = kK + 2 * kTile;
     static constexpr int kLse = kQ + NS * kTile;
     static constexpr int kBar = kLse + kLseChunk * 4;
     static constexpr int kBytes = kBar + 256 + 1024;
 };
 
+// One CTA = two key tiles g = 0, 1 of 128 keys.  For every query tile i the
+// MMA thread computes S^T_g = K_g Q_i^T into TMEM buffer (g, i % 2) (columns
+// 256 g + 128 (i % 2)); consumer warpgroup g reads its row (one key per
+// thread), frees the buffer and adds exp2(2 (S c2 - lse2_q)) over the 128
+// queries.  The log-masses are kept doubled in shared memory so that one
+// FFMA forms the exponent.
 template <int D, int NS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kColThreads, 1)
     k_colscore_tc(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
                   const float* __restrict__ lse2, int n, int T, float c2, float* __restrict__ score,
                   int32_t* __restrict__ status) {
@@ -325,9 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* k_full = bars;
     uint64_t* q_full = bars + 1;          // [NS]
     uint64_t* q_empty = q_full + NS;      // [NS]
-    uint64_t* s_full = q_empty + NS;      // [2]
-    uint64_t* s_empty = s_full + 2;       // [2]
-    uint64_t* mma_done = s_empty + 2;
+    uint64_t* s_full = q_empty + NS;      // [2 tiles][2 buffers]
+    uint64_t* s_empty = s_full + 4;       // [2][2]
+    uint64_t* mma_done = s_empty + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -337,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(q_full + s, 1);
             mbar_init(q_empty + s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < 4; ++b) {
             mbar_init(s_full + b, 1);
             mbar_init(s_empty + b, 128);
         }
@@ -345,21 +379,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(tmem_slot, 256);
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const int nq = (n + TB - 1) / TB;
-    const int k0 = blockIdx.x * TB;
+    const int k0 = blockIdx.x * 2 * TB;
     constexpr uint32_t kTileBytes = (uint32_t)L::kTile;
 
     if (warp == 0) {
         if (lane == 0) {
             prefetch_tmap(&mK);
             prefetch_tmap(&mQ);
-            mbar_expect_tx(k_full, kTileBytes);
-            for (int c = 0; c < D / 64; ++c) tma_load_3d(sm + L::kK + c * kBox, &mK, k_full, c * 64, k0, h);
+            mbar_expect_tx(k_full, 2 * kTileBytes);
+            for (int g = 0; g < 2; ++g)
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_3d(sm + L::kK + g * L::kTile + c * kBox, &mK, k_full, c * 64, k0 + g * TB, h);
             int issued = 0;
             for (int i = 0; i < nq; ++i) {
                 const int s = i % NS;
@@ -377,19 +413,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
-            const uint32_t aK = smem_addr(sm + L::kK);
+            const uint32_t aK0 = smem_addr(sm + L::kK);
             bool ok = mbar_wait(k_full, 0, abort_flag);
             for (int i = 0; ok && i < nq; ++i) {
                 const int s = i % NS;
                 if (!mbar_wait(q_full + s, (uint32_t)(i / NS) & 1u, abort_flag)) break;
-                if (i >= 2 && !mbar_wait(s_empty + (i & 1), (uint32_t)((i >> 1) - 1) & 1u, abort_flag)) break;
-                fence_after_sync();
                 const uint32_t aQ = smem_addr(sm + L::kQ + s * L::kTile);
-                const uint32_t dS = tmem + (uint32_t)(i & 1) * 128;
+                for (int g = 0; g < 2; ++g) {
+                    const int b = g * 2 + (i & 1);
+                    if (i >= 2 && !mbar_wait(s_empty + b, (uint32_t)((i >> 1) - 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after_sync();
+                    const uint32_t aK = aK0 + (uint32_t)(g * L::kTile);
+                    const uint32_t dS = tmem + (uint32_t)(g * 256 + (i & 1) * 128);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(dS, kmajor_desc(aK, kk), kmajor_desc(aQ, kk), idesc, kk > 0);
-                mma_commit(s_full + (i & 1));
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(dS, kmajor_desc(aK, kk), kmajor_desc(aQ, kk), idesc, kk > 0);
+                    mma_commit(s_full + b);
+                }
+                if (!ok) break;
                 mma_commit(q_empty + s);
             }
             mma_commit(mma_done);
@@ -397,31 +441,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // consumers: one key row per thread
+        // consumer warpgroup g: one key row per thread
+        const int g = (warp - 2) >> 2;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const int ct = threadIdx.x - kConsumer0 * 32;       // 0..127
+        const int ct = threadIdx.x - 64;            // 0..255 over both warpgroups
+        const float c2x = 2.f * c2;
         double acc = 0.0;
         bool ok = true;
         // Every consumer warp runs all iterations (after an abort it only
         // skips the work) so that the named barrier around the log-mass
-        // reload is always reached by all four warps.
+        // reload is always reached by all eight warps.
         for (int i = 0; i < nq; ++i) {
             const int qb = i * TB;
             if (qb % kLseChunk == 0) {
-                // log-masses of the next chunk of queries; +inf past n zeroes those columns
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                for (int e = ct; e < kLseChunk; e += 128) {
+                // doubled log-masses of the next chunk; +inf past n zeroes those columns
+                const int cnt = min(kLseChunk, ((n - qb + TB - 1) / TB) * TB);
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                for (int e = ct; e < cnt; e += 256) {
                     const int q = qb + e;
-                    lse_s[e] = (q < n) ? lse2[(int64_t)h * n + q] : INFINITY;
+                    lse_s[e] = (q < n) ? 2.f * lse2[(int64_t)h * n + q] : INFINITY;
                 }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                asm volatile("bar.sync 1, 256;" ::: "memory");
             }
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full + (i & 1), (uint32_t)(i >> 1) & 1u, abort_flag));
+            const int b = g * 2 + (i & 1);
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (uint32_t)(i >> 1) & 1u, abort_flag));
             if (!ok) continue;
             fence_after_sync();
-            const uint32_t sbase = tmem + lane_off + (uint32_t)(i & 1) * 128;
+            const uint32_t sbase = tmem + lane_off + (uint32_t)(g * 256 + (i & 1) * 128);
             float s[128];
             {
                 uint32_t r[32];
@@ -434,65 +482,138 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             fence_before_sync();
-            mbar_arrive(s_empty + (i & 1));
-            const float* ls = lse_s + (qb % kLseChunk);
+            mbar_arrive(s_empty + b);
+            const float4* ls = reinterpret_cast<const float4*>(lse_s + (qb % kLseChunk));
             float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
             for (int c = 0; c < 128; c += 4) {
-                const float x0 = fmaf(s[c], c2, -ls[c]);
-                const float x1 = fmaf(s[c + 1], c2, -ls[c + 1]);
-                const float x2 = fmaf(s[c + 2], c2, -ls[c + 2]);
-                const float x3 = fmaf(s[c + 3], c2, -ls[c + 3]);
-                a0 += ex2(x0 + x0);
-                a1 += ex2(x1 + x1);
-                a2 += ex2(x2 + x2);
-                a3 += ex2(x3 + x3);
+                const float4 l4 = ls[c / 4];
+                a0 += ex2(fmaf(s[c], c2x, -l4.x));
+                a1 += ex2(fmaf(s[c + 1], c2x, -l4.y));
+                a2 += ex2(fmaf(s[c + 2], c2x, -l4.z));
+                a3 += ex2(fmaf(s[c + 3], c2x, -l4.w));
             }
             acc += (double)((a0 + a1) + (a2 + a3));
         }
-        const int key = k0 + row;
+        const int key = k0 + g * TB + row;
         if (ok && key < T) score[(int64_t)h * T + key] = (float)sqrt(acc / (double)n);
     }
     if (threadIdx.x == 0 && *abort_flag) set_status(status, h, KVC_ERR_TIMEOUT);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    if (warp == 1) tmem_dealloc(tmem, 256);
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------ mass logits
+// l2[h][q][i] = S_q,idx_i c2 - lse2_q (log2 of A'_qi) for i < t_h and -inf
+// for t_h <= i < roundup(t_h, 64): one 128 x 128 tile per CTA, S = Q C_k^T on
+// the tensor cores.  The kept keys come from their per-head copy Ckw
+// [H][ldA][d] (bf16) that the gather writes.
+template <int D>
+struct MassLayout {
+    static constexpr int kTile = (D / 64) * kBox;
+    static constexpr int kQ = 0;
+    static constexpr int kC = kTile;
+    static constexpr int kBar = 2 * kTile;
+    static constexpr int kBytes = kBar + 256 + 1024;
+};
+constexpr int kMassThreads = 192;
+
+template <int D>
+__global__ void __launch_bounds__(kMassThreads, 1)
+    k_masslogits_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mC,
+                    const float* __restrict__ lse2, const int32_t* __restrict__ offsets, int n, int64_t ldA,
+                    float c2, float* __restrict__ L2, int32_t* __restrict__ status) {
+    using L = MassLayout<D>;
+    const int h = blockIdx.z;
+    if (!head_ok(status, h)) return;
+    const int off = offsets[h];
+    const int th = offsets[h + 1] - off;
+    const int i0 = blockIdx.x * TB;
+    const int q0 = blockIdx.y * TB;
+    const int tpad = (int)round_up(th, 64);
+    if (i0 >= tpad) return;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
+    uint64_t* full = bars;
+    uint64_t* done = bars + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    if (threadIdx.x == 0) {
+        mbar_init(full, 1);
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 128);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_expect_tx(full, 2u * L::kTile);
+            for (int c = 0; c < D / 64; ++c) {
+                tma_load_3d(sm + L::kQ + c * kBox, &mQ, full, c * 64, q0, h);
+                tma_load_3d(sm + L::kC + c * kBox, &mC, full, c * 64, i0, h);
+            }
+            drain_wait(full, 0);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            if (mbar_wait(full, 0, abort_flag)) {
+                fence_after_sync();
+                constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
+                const uint32_t aQ = smem_addr(sm + L::kQ), aC = smem_addr(sm + L::kC);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem, kmajor_desc(aQ, kk), kmajor_desc(aC, kk), idesc, kk > 0);
+            }
+            mma_commit(done);
+            drain_wait(done, 0);
+        }
+        __syncwarp();
+    } else {
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag));
+        const int q = q0 + row;
+        if (ok) {
+            fence_after_sync();
+            const float lq = (q < n) ? lse2[(int64_t)h * n + q] : 0.f;
+            float* dst = L2 + ((int64_t)h * n + q) * ldA + i0;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + c * 32, r);
+                tmem_ld_wait();
+                const int ib = i0 + c * 32;
+                if (q < n && ib < tpad) {
+#pragma unroll
+                    for (int k = 0; k < 32; k += 4) {
+                        float4 v;
+                        v.x = (ib + k + 0 < th) ? fmaf(__uint_as_float(r[k + 0]), c2, -lq) : -INFINITY;
+                        v.y = (ib + k + 1 < th) ? fmaf(__uint_as_float(r[k + 1]), c2, -lq) : -INFINITY;
+                        v.z = (ib + k + 2 < th) ? fmaf(__uint_as_float(r[k + 2]), c2, -lq) : -INFINITY;
+                        v.w = (ib + k + 3 < th) ? fmaf(__uint_as_float(r[k + 3]), c2, -lq) : -INFINITY;
+                        *reinterpret_cast<float4*>(dst + c * 32 + k) = v;
+                    }
+                }
+            }
+        }
+    }
+    if (threadIdx.x == 0 && *abort_flag) set_status(status, h, KVC_ERR_TIMEOUT);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (warp == 1) tmem_dealloc(tmem, 128);
 }
 
 // ------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<EncodeTiledFn>(p);
-    }();
-    return fn;
-}
-
-// [H][rows][d] bf16 viewed as a 3-D tensor (d, rows, H); boxes of
-// [128 rows][64 elements] with 128-byte swizzle; rows past the end of a head
-// read as zero.
-bool make_map(CUtensorMap* m, const void* base, int d, int rows, int H) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)H};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
-    cuuint32_t box[3] = {64, 128, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, int NS>
 cudaError_t launch_fwd_t(const void* Q, const void* K, const void* V, int H, int n, int T, float c2, float* O,
                          float* lse2, int32_t* status, cudaStream_t st) {
@@ -503,8 +624,8 @@ cudaError_t launch_fwd_t(const void* Q, const void* K, const void* V, int H, int
     auto kern = k_attn_fwd_tc<D, NS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((n + TB - 1) / TB, H);
-    kern<<<grid, kThreads, smem, st>>>(mQ, mK, mV, n, T, c2, O, lse2, status);
+    dim3 grid((n + 2 * TB - 1) / (2 * TB), H);
+    kern<<<grid, kFwdThreads, smem, st>>>(mQ, mK, mV, n, T, c2, O, lse2, status);
     return cudaGetLastError();
 }
 
@@ -517,24 +638,44 @@ cudaError_t launch_col_t(const void* Q, const void* K, const float* lse2, int H,
     auto kern = k_colscore_tc<D, NS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((T + TB - 1) / TB, H);
-    kern<<<grid, kThreads, smem, st>>>(mK, mQ, lse2, n, T, c2, score, status);
+    dim3 grid((T + 2 * TB - 1) / (2 * TB), H);
+    kern<<<grid, kColThreads, smem, st>>>(mK, mQ, lse2, n, T, c2, score, status);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_mass_t(const void* Q, const void* Ck, const float* lse2, const int32_t* offsets, int H, int n,
+                          int max_t, int64_t ldA, float c2, float* L2, int32_t* status, cudaStream_t st) {
+    CUtensorMap mQ, mC;
+    if (!make_map(&mQ, Q, D, n, H) || !make_map(&mC, Ck, D, (int)ldA, H)) return cudaErrorInvalidValue;
+    constexpr int smem = MassLayout<D>::kBytes;
+    auto kern = k_masslogits_tc<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((max_t + TB - 1) / TB, (n + TB - 1) / TB, H);
+    kern<<<grid, kMassThreads, smem, st>>>(mQ, mC, lse2, offsets, n, ldA, c2, L2, status);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-bool tc_maps_available() { return encode_fn() != nullptr; }
+cudaError_t launch_masslogits_tc(int d, const void* Q, const void* Ck, const float* lse2, const int32_t* offsets,
+                                 int H, int n, int max_t, int sum_t, int64_t ldA, float c2, float* L2,
+                                 int32_t* status, cudaStream_t st) {
+    (void)sum_t;
+    return d == 128 ? launch_mass_t<128>(Q, Ck, lse2, offsets, H, n, max_t, ldA, c2, L2, status, st)
+                    : launch_mass_t<64>(Q, Ck, lse2, offsets, H, n, max_t, ldA, c2, L2, status, st);
+}
 
 cudaError_t launch_attn_fwd_tc(int d, const void* Q, const void* K, const void* V, int H, int n, int T, float c2,
                                float* O, float* lse2, int32_t* status, cudaStream_t st) {
     return d == 128 ? launch_fwd_t<128, 2>(Q, K, V, H, n, T, c2, O, lse2, status, st)
-                    : launch_fwd_t<64, 4>(Q, K, V, H, n, T, c2, O, lse2, status, st);
+                    : launch_fwd_t<64, 3>(Q, K, V, H, n, T, c2, O, lse2, status, st);
 }
 
 cudaError_t launch_colscore_tc(int d, const void* Q, const void* K, const float* lse2, int H, int n, int T,
                                float c2, float* score, int32_t* status, cudaStream_t st) {
-    return d == 128 ? launch_col_t<128, 4>(Q, K, lse2, H, n, T, c2, score, status, st)
+    return d == 128 ? launch_col_t<128, 3>(Q, K, lse2, H, n, T, c2, score, status, st)
                     : launch_col_t<64, 6>(Q, K, lse2, H, n, T, c2, score, status, st);
 }
 

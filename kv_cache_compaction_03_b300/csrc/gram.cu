@@ -1,166 +1,16 @@
-// Gram matrices and the biased softmax X ("Fast KV Compaction via Attention
-// Matching", section 2, fitting beta by NNLS and C_v by least squares through
-// the normal equations):
-//   k_gram<true>   G = A'^T A' with A' = exp2(l2) (l2 = log2 of the relative
-//                  mass matrix), and b = A'^T 1
-//   k_gram<false>  M = X^T X
-//   k_xto          R = X^T O
+// Ridges and the biased softmax X of the two least-squares fits ("Fast KV
+// Compaction via Attention Matching", section 2, fitting beta by NNLS and
+// C_v by least squares through the normal equations; the Gram products
+// themselves are in gram_tc.cu):
 //   k_ridge_*      mu / lambda from the trace, added to the diagonal
 //   k_xsoftmax     X_qi = softmax_i(l2_qi + log2 w_i), in place over l2
 // Matrices are per head, row-major with leading dimension ldA (a multiple
-// of 64); only the lower triangle of G / M is written.
+// of 64); only the lower triangle of G / M is read.
 #include "common.cuh"
 
 namespace kvc {
 
-constexpr int GT = 64;     // Gram tile
-constexpr int GQ = 32;     // rows of A per smem stage
-
-__device__ __forceinline__ void tri_decode(int p, int& I, int& J) {
-    int i = (int)((sqrtf(8.f * (float)p + 1.f) - 1.f) * 0.5f);
-    while (i * (i + 1) / 2 > p) --i;
-    while ((i + 1) * (i + 2) / 2 <= p) ++i;
-    I = i;
-    J = p - i * (i + 1) / 2;
-}
-
-// grid (ntiles*(ntiles+1)/2, H), block 256.
-template <bool EXP>
-__global__ void __launch_bounds__(256) k_gram(const float* __restrict__ A, const int32_t* __restrict__ offsets, int n,
-                                              int64_t ldA, float* __restrict__ G, float* __restrict__ b,
-                                              const int32_t* __restrict__ status) {
-    const int h = blockIdx.y;
-    if (!head_ok(status, h)) return;
-    const int off = offsets[h];
-    const int t = offsets[h + 1] - off;
-    int I, J;
-    tri_decode(blockIdx.x, I, J);
-    if (I * GT >= t) return;
-    __shared__ float Ai[GQ][GT + 1];
-    __shared__ float Aj[GQ][GT + 1];
-    __shared__ double red[16][GT];
-    const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
-    const float* Ah = A + (int64_t)h * n * ldA;
-    float acc[4][4];
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
-    float csum[4] = {0.f, 0.f, 0.f, 0.f};
-    const bool diag = (I == J);
-    for (int q0 = 0; q0 < n; q0 += GQ) {
-        __syncthreads();
-        for (int e = threadIdx.x; e < GQ * GT; e += 256) {
-            const int r = e / GT, c = e % GT;
-            const int q = q0 + r;
-            float vi = 0.f, vj = 0.f;
-            if (q < n) {
-                vi = Ah[(int64_t)q * ldA + I * GT + c];
-                vj = Ah[(int64_t)q * ldA + J * GT + c];
-                if (EXP) {
-                    vi = exp2f(vi);
-                    vj = exp2f(vj);
-                }
-            }
-            Ai[r][c] = vi;
-            Aj[r][c] = vj;
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int r = 0; r < GQ; ++r) {
-            float ai[4], aj[4];
-#pragma unroll
-            for (int a = 0; a < 4; ++a) ai[a] = Ai[r][ty * 4 + a];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) aj[c] = Aj[r][tx + 16 * c];
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) acc[a][c] = fmaf(ai[a], aj[c], acc[a][c]);
-        }
-        if (EXP && diag) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) csum[c] += Aj[ty][tx + 16 * c] + Aj[ty + 16][tx + 16 * c];
-        }
-    }
-    float* Gh = G + (int64_t)h * ldA * ldA;
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-        const int i = I * GT + ty * 4 + a;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int j = J * GT + tx + 16 * c;
-            if (i < t && j < t && j <= i) Gh[(int64_t)i * ldA + j] = acc[a][c];
-        }
-    }
-    if (EXP && diag) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) red[ty][tx + 16 * c] = (double)csum[c];
-        __syncthreads();
-        if (threadIdx.x < GT) {
-            double s = 0.0;
-            for (int r = 0; r < 16; ++r) s += red[r][threadIdx.x];
-            const int j = I * GT + threadIdx.x;
-            if (j < t) b[off + j] = (float)s;
-        }
-    }
-}
-
-// R[off+i][c] = sum_q X[h][q][i] O[h][q][c].  grid (ceil(max_t/64), H), block 256.
-template <int D>
-__global__ void __launch_bounds__(256) k_xto(const float* __restrict__ X, const float* __restrict__ O,
-                                             const int32_t* __restrict__ offsets, int n, int64_t ldA,
-                                             float* __restrict__ R, const int32_t* __restrict__ status) {
-    const int h = blockIdx.y;
-    if (!head_ok(status, h)) return;
-    const int off = offsets[h];
-    const int t = offsets[h + 1] - off;
-    const int i0 = blockIdx.x * GT;
-    if (i0 >= t) return;
-    __shared__ float Xs[GQ][GT + 1];
-    __shared__ float Os[GQ][D];
-    constexpr int DC = D / 16;
-    const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
-    float acc[4][DC];
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int c = 0; c < DC; ++c) acc[a][c] = 0.f;
-    const float* Xh = X + (int64_t)h * n * ldA;
-    const float* Oh = O + (int64_t)h * n * D;
-    for (int q0 = 0; q0 < n; q0 += GQ) {
-        __syncthreads();
-        for (int e = threadIdx.x; e < GQ * GT; e += 256) {
-            const int r = e / GT, c = e % GT;
-            Xs[r][c] = (q0 + r < n) ? Xh[(int64_t)(q0 + r) * ldA + i0 + c] : 0.f;
-        }
-        for (int e = threadIdx.x; e < GQ * D; e += 256) {
-            const int r = e / D, c = e % D;
-            Os[r][c] = (q0 + r < n) ? Oh[(int64_t)(q0 + r) * D + c] : 0.f;
-        }
-        __syncthreads();
-#pragma unroll 4
-        for (int r = 0; r < GQ; ++r) {
-            float x[4];
-#pragma unroll
-            for (int a = 0; a < 4; ++a) x[a] = Xs[r][ty * 4 + a];
-#pragma unroll
-            for (int c = 0; c < DC; ++c) {
-                const float o = Os[r][tx + 16 * c];
-#pragma unroll
-                for (int a = 0; a < 4; ++a) acc[a][c] = fmaf(x[a], o, acc[a][c]);
-            }
-        }
-    }
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-        const int i = i0 + ty * 4 + a;
-        if (i < t) {
-#pragma unroll
-            for (int c = 0; c < DC; ++c) R[((int64_t)off + i) * D + tx + 16 * c] = acc[a][c];
-        }
-    }
-}
+constexpr int GT = 64;     // padding granule of the log-mass rows
 
 // Trace of the lower-stored matrix diagonal, in double.  Block-wide.
 __device__ double block_trace(const float* Gh, int t, int64_t ld, double* sred) {
@@ -249,25 +99,6 @@ __global__ void __launch_bounds__(256) k_xsoftmax(float* __restrict__ L2, const 
 }
 
 // ---------------------------------------------------------------- launchers
-cudaError_t launch_gram(bool exp_mode, const float* A, const int32_t* offsets, int H, int n, int max_t, int64_t ldA,
-                        float* G, float* b, const int32_t* status, cudaStream_t st) {
-    const int nt = (max_t + GT - 1) / GT;
-    dim3 grid(nt * (nt + 1) / 2, H);
-    if (exp_mode)
-        k_gram<true><<<grid, 256, 0, st>>>(A, offsets, n, ldA, G, b, status);
-    else
-        k_gram<false><<<grid, 256, 0, st>>>(A, offsets, n, ldA, G, b, status);
-    return cudaGetLastError();
-}
-cudaError_t launch_xto(int d, const float* X, const float* O, const int32_t* offsets, int H, int n, int max_t,
-                       int64_t ldA, float* R, const int32_t* status, cudaStream_t st) {
-    dim3 grid((max_t + GT - 1) / GT, H);
-    if (d == 128)
-        k_xto<128><<<grid, 256, 0, st>>>(X, O, offsets, n, ldA, R, status);
-    else
-        k_xto<64><<<grid, 256, 0, st>>>(X, O, offsets, n, ldA, R, status);
-    return cudaGetLastError();
-}
 cudaError_t launch_ridge_g(float* G, const float* b, const int32_t* offsets, int H, int64_t ldA, float eps, float* f,
                            HeadScalars* hs, int32_t* status, cudaStream_t st) {
     k_ridge_g<<<H, 256, 0, st>>>(G, b, offsets, ldA, eps, f, hs, status);

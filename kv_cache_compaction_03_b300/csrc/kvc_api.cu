@@ -15,15 +15,18 @@ cudaError_t launch_colscore_simt(int, int, const void*, const void*, const float
                                  const int32_t*, cudaStream_t);
 cudaError_t launch_select(const float*, int, int, const int32_t*, int, int, int32_t*, int32_t*, cudaStream_t);
 cudaError_t launch_gather(int, int, const void*, const void*, int, int, int, const int32_t*, const int32_t*, void*,
-                          float*, const int32_t*, cudaStream_t);
+                          float*, void*, int64_t, const int32_t*, cudaStream_t);
+cudaError_t launch_masslogits_tc(int d, const void* Q, const void* Ck, const float* lse2, const int32_t* offsets,
+                                 int H, int n, int max_t, int sum_t, int64_t ldA, float c2, float* L2,
+                                 int32_t* status, cudaStream_t st);
 cudaError_t launch_masslogits(int, int, const void*, const void*, const float*, const int32_t*, int, int, int, int64_t,
                               float, float*, const int32_t*, cudaStream_t);
 cudaError_t launch_attend(int, int, const void*, int, const void*, const float*, const float*, const int32_t*, int,
                           float, float*, int32_t*, cudaStream_t);
-cudaError_t launch_gram(bool, const float*, const int32_t*, int, int, int, int64_t, float*, float*, const int32_t*,
-                        cudaStream_t);
-cudaError_t launch_xto(int, const float*, const float*, const int32_t*, int, int, int, int64_t, float*,
-                       const int32_t*, cudaStream_t);
+cudaError_t launch_gram_sym_tc(bool exp_mode, const float* A, const int32_t* offsets, int H, int n, int max_t,
+                               int64_t ld, float* C, int64_t ldc, float* colsum, int32_t* status, cudaStream_t st);
+cudaError_t launch_gram_rect_tc(int d, const float* A, const float* B, const int32_t* offsets, int H, int n,
+                                int max_t, int64_t ld, float* C, int32_t* status, cudaStream_t st);
 cudaError_t launch_ridge_g(float*, const float*, const int32_t*, int, int64_t, float, float*, HeadScalars*, int32_t*,
                            cudaStream_t);
 cudaError_t launch_ridge_m(int, float*, float*, const float*, const int32_t*, int, int64_t, float, HeadScalars*,
@@ -31,9 +34,11 @@ cudaError_t launch_ridge_m(int, float*, float*, const float*, const int32_t*, in
 cudaError_t launch_xsoftmax(float*, const float*, const int32_t*, int, int, int64_t, const int32_t*, cudaStream_t);
 cudaError_t launch_chol(float*, const int32_t*, int, int, int64_t, float*, int32_t*, cudaStream_t);
 int chol_launches(int max_t);
-cudaError_t launch_cholsolve(int, const float*, const float*, const int32_t*, int, int64_t, float*, const int32_t*,
+cudaError_t launch_cholsolve(int, const float*, const float*, const float*, const int32_t*, int, int64_t, float*,
+                             const int32_t*,
                              cudaStream_t);
-cudaError_t launch_nnls_all(const float* L, const float* f, const int32_t* offsets, int H, int n, int max_t,
+cudaError_t launch_nnls_all(const float* L, const float* dinv, const float* f, const int32_t* offsets, int H, int n,
+                            int max_t,
                             int64_t ldA, const float* L2, float* x, float* x0, int8_t* zflag, int32_t* zlist,
                             int32_t* nz, float* W, float* S, int32_t* piv, float* u, float* r, float* d0,
                             HeadScalars* hs, int zmax, int max_iter, int refine_iters, int32_t* status,
@@ -99,7 +104,7 @@ struct StageClock {
 struct Layout {
     int64_t ldA;
     int zmax;
-    size_t O, lse2, score, L2, Vsel, G, dscr, b, f, x, x0, d0, u, r, R, zflag, zlist, nz, piv, W, S, hs, total;
+    size_t O, lse2, score, L2, Vsel, Ckw, G, dinv, b, f, x, x0, d0, u, r, R, zflag, zlist, nz, piv, W, S, hs, total;
 };
 
 static size_t carve(size_t& cur, size_t bytes) {
@@ -120,8 +125,9 @@ static Layout make_layout(const kvc_problem& p, const kvc_params& prm) {
     L.score = carve(c, H * T * 4);
     L.L2 = carve(c, H * n * ldA * 4);
     L.Vsel = carve(c, H * mt * d * 4);
+    L.Ckw = carve(c, H * ldA * d * 2);
     L.G = carve(c, H * ldA * ldA * 4);
-    L.dscr = carve(c, H * 64 * 64 * 4);
+    L.dinv = carve(c, H * ldA * 64 * 4);
     L.b = carve(c, H * mt * 4);
     L.f = carve(c, H * mt * 4);
     L.x = carve(c, H * mt * 4);
@@ -246,7 +252,7 @@ kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* 
     float* L2 = (float*)(ws + L.L2);
     float* Vsel = (float*)(ws + L.Vsel);
     float* G = (float*)(ws + L.G);
-    float* dscr = (float*)(ws + L.dscr);
+    float* dinv = (float*)(ws + L.dinv);
     float* b = (float*)(ws + L.b);
     float* f = (float*)(ws + L.f);
     float* x = (float*)(ws + L.x);
@@ -279,23 +285,35 @@ kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* 
         KVC_STAGE("colscore", 1, launch_colscore_simt(dt, d, Q_ref, K, lse2, H, n, T, c2, score, head_status, st));
     }
     KVC_STAGE("select", 1, launch_select(score, H, T, offsets, q.keep_first, q.keep_last, idx_out, head_status, st));
-    KVC_STAGE("gather", 1, launch_gather(dt, d, K, V, H, T, mt, offsets, idx_out, C_k, Vsel, head_status, st));
-    KVC_STAGE("masslogits", 1,
-              launch_masslogits(dt, d, Q_ref, C_k, lse2, offsets, H, n, mt, L.ldA, c2, L2, head_status, st));
-    KVC_STAGE("gram_a", 1, launch_gram(true, L2, offsets, H, n, mt, L.ldA, G, b, head_status, st));
+    void* Ckw = ws + L.Ckw;
+    const bool tc = dt == KVC_DTYPE_BF16;
+    KVC_STAGE("gather", 1,
+              launch_gather(dt, d, K, V, H, T, mt, offsets, idx_out, C_k, Vsel, tc ? Ckw : nullptr, L.ldA,
+                            head_status, st));
+    if (tc) {
+        // the kept keys' per-head copy has ldA rows per head; the map sees H * ldA rows
+        KVC_STAGE("masslogits", 1,
+                  launch_masslogits_tc(d, Q_ref, Ckw, lse2, offsets, H, n, mt, 0, L.ldA, c2, L2, head_status, st));
+    } else {
+        KVC_STAGE("masslogits", 1,
+                  launch_masslogits(dt, d, Q_ref, C_k, lse2, offsets, H, n, mt, L.ldA, c2, L2, head_status, st));
+    }
+    KVC_STAGE("gram_a", 1,
+              launch_gram_sym_tc(true, L2, offsets, H, n, mt, L.ldA, G, L.ldA, b, head_status, st));
     KVC_STAGE("ridge_g", 1, launch_ridge_g(G, b, offsets, H, L.ldA, q.eps_mu, f, hs, head_status, st));
-    KVC_STAGE("chol_h", chol_launches(mt), launch_chol(G, offsets, H, mt, L.ldA, dscr, head_status, st));
+    KVC_STAGE("chol_h", chol_launches(mt), launch_chol(G, offsets, H, mt, L.ldA, dinv, head_status, st));
     int nnls_launches = 0;
     KVC_STAGE("nnls", nnls_launches,
-              launch_nnls_all(G, f, offsets, H, n, mt, L.ldA, L2, x, x0, zflag, zlist, nzv, W, S, piv, u, r, d0, hs,
+              launch_nnls_all(G, dinv, f, offsets, H, n, mt, L.ldA, L2, x, x0, zflag, zlist, nzv, W, S, piv, u, r, d0, hs,
                               L.zmax, q.nnls_max_iter, q.refine_iters, head_status, st, &nnls_launches));
     KVC_STAGE("beta", 1, launch_beta_out(x, offsets, H, mt, beta, head_status, st));
     KVC_STAGE("xsoftmax", 1, launch_xsoftmax(L2, x, offsets, H, n, L.ldA, head_status, st));
-    KVC_STAGE("gram_x", 1, launch_gram(false, L2, offsets, H, n, mt, L.ldA, G, nullptr, head_status, st));
-    KVC_STAGE("xto", 1, launch_xto(d, L2, O, offsets, H, n, mt, L.ldA, R, head_status, st));
+    KVC_STAGE("gram_x", 1,
+              launch_gram_sym_tc(false, L2, offsets, H, n, mt, L.ldA, G, L.ldA, nullptr, head_status, st));
+    KVC_STAGE("xto", 1, launch_gram_rect_tc(d, L2, O, offsets, H, n, mt, L.ldA, R, head_status, st));
     KVC_STAGE("ridge_m", 1, launch_ridge_m(d, G, R, Vsel, offsets, H, L.ldA, q.eps_lambda, hs, head_status, st));
-    KVC_STAGE("chol_m", chol_launches(mt), launch_chol(G, offsets, H, mt, L.ldA, dscr, head_status, st));
-    KVC_STAGE("cholsolve", 1, launch_cholsolve(d, G, R, offsets, H, L.ldA, C_v, head_status, st));
+    KVC_STAGE("chol_m", chol_launches(mt), launch_chol(G, offsets, H, mt, L.ldA, dinv, head_status, st));
+    KVC_STAGE("cholsolve", 1, launch_cholsolve(d, G, dinv, R, offsets, H, L.ldA, C_v, head_status, st));
     clk.finish();
     return KVC_OK;
 }

@@ -4,10 +4,13 @@
 //
 //   k_chol_panel / k_chol_update
 //       blocked right-looking Cholesky of every head's t x t matrix, one
-//       launch pair per 64-wide panel; the trailing update is spread over
-//       64 x 64 tiles so that a handful of heads still fills the GPU
-//   k_trsv_cols
-//       (L L^T) x = b for many right-hand sides, one CTA per column group:
+//       launch pair per 64-wide panel: the diagonal block is factored and
+//       inverted in registers, the panel is a product with that inverse, and
+//       the trailing update is spread over 64 x 64 tiles so that a handful of
+//       heads still fills the GPU
+//   k_solve_cols
+//       (L L^T) x = b for many right-hand sides, one CTA per group of
+//       columns, blocked with the stored inverses of the diagonal blocks:
 //       x0 = H^{-1} f, the zero-set columns H^{-1} e_z, refinement steps and
 //       the C_v columns
 //   k_bpp_step
@@ -98,74 +101,6 @@ __device__ bool cta_chol_small(float* A, int n, int64_t lda, float* smem, int* s
     return true;
 }
 
-// (L L^T) x = x in place for a vector in smem (length n), L in global.
-// Block-wide; Ds: CB*(CB+1) floats of scratch.
-__device__ void cta_cholsolve_vec(const float* L, int n, int64_t lda, float* xs, float* Ds) {
-    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31;
-    // forward: L y = b
-    for (int k0 = 0; k0 < n; k0 += CB) {
-        const int kb = min(CB, n - k0);
-        __syncthreads();
-        for (int e = tid; e < kb * kb; e += nt) {
-            const int i = e / kb, j = e % kb;
-            Ds[i * (CB + 1) + j] = (j <= i) ? L[(int64_t)(k0 + i) * lda + k0 + j] : 0.f;
-        }
-        __syncthreads();
-        if (tid < 32) {
-            for (int j = 0; j < kb; ++j) {
-                const float y = xs[k0 + j] / Ds[j * (CB + 1) + j];
-                __syncwarp();
-                if (lane == 0) xs[k0 + j] = y;
-                for (int i = j + 1 + lane; i < kb; i += 32) xs[k0 + i] -= Ds[i * (CB + 1) + j] * y;
-                __syncwarp();
-            }
-        }
-        __syncthreads();
-        for (int r = k0 + kb + tid; r < n; r += nt) {
-            const float* lr = L + (int64_t)r * lda + k0;
-            float v = xs[r];
-            if (kb == CB) {
-                const float4* l4 = reinterpret_cast<const float4*>(lr);
-#pragma unroll 4
-                for (int p = 0; p < CB / 4; ++p) {
-                    const float4 q = l4[p];
-                    v -= q.x * xs[k0 + 4 * p] + q.y * xs[k0 + 4 * p + 1] + q.z * xs[k0 + 4 * p + 2] +
-                         q.w * xs[k0 + 4 * p + 3];
-                }
-            } else {
-                for (int p = 0; p < kb; ++p) v -= lr[p] * xs[k0 + p];
-            }
-            xs[r] = v;
-        }
-    }
-    // backward: L^T x = y
-    for (int k0 = ((n - 1) / CB) * CB; k0 >= 0; k0 -= CB) {
-        const int kb = min(CB, n - k0);
-        __syncthreads();
-        for (int e = tid; e < kb * kb; e += nt) {
-            const int i = e / kb, j = e % kb;
-            Ds[i * (CB + 1) + j] = (j <= i) ? L[(int64_t)(k0 + i) * lda + k0 + j] : 0.f;
-        }
-        __syncthreads();
-        if (tid < 32) {
-            for (int j = kb - 1; j >= 0; --j) {
-                const float x = xs[k0 + j] / Ds[j * (CB + 1) + j];
-                __syncwarp();
-                if (lane == 0) xs[k0 + j] = x;
-                for (int i = lane; i < j; i += 32) xs[k0 + i] -= Ds[j * (CB + 1) + i] * x;
-                __syncwarp();
-            }
-        }
-        __syncthreads();
-        for (int r = tid; r < k0; r += nt) {
-            float v = xs[r];
-            for (int p = 0; p < kb; ++p) v -= L[(int64_t)(k0 + p) * lda + r] * xs[k0 + p];
-            xs[r] = v;
-        }
-    }
-    __syncthreads();
-}
-
 __device__ float block_max_abs(const float* v, int n, float* sred) {
     float m = 0.f;
     for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, fabsf(v[i]));
@@ -179,15 +114,16 @@ __device__ float block_max_abs(const float* v, int n, float* sred) {
 }
 
 // ------------------------------------------------------------ Cholesky
-// Panel k0: CTA 0 factors the diagonal block; CTA rb >= 1 factors its own
-// copy of the diagonal block (cheaper than another launch) and solves the
-// 64 rows [k0 + 64 rb, ...) of the panel.  grid (1 + row blocks, H), block 128.
-// The factored diagonal block cannot be stored into the matrix by this
-// launch (sibling CTAs read the unfactored block), so CTA 0 parks it in
-// dscr[h] and the next panel launch's CTA 0 copies it into place; the last
-// block of a head has no siblings and is stored directly.
-__global__ void __launch_bounds__(128) k_chol_panel(float* __restrict__ mats, const int32_t* __restrict__ offsets,
-                                                    int64_t ldA, int k0, float* __restrict__ dscr,
+// Panel k0 of the blocked right-looking factorisation.  Every CTA factors
+// the 64 x 64 diagonal block A_kk in registers (one row per 4 threads, 16
+// columns each) and forms its inverse L_kk^{-1}; CTA 0 stores that inverse in
+// dinv[h][k0/64] for the solves, CTA rb >= 1 computes its 64 rows of the
+// panel, L_ik = A_ik L_kk^{-T}, as a small matrix product.  The diagonal
+// blocks of L are never stored in the matrix (only their inverses are used),
+// so no CTA writes what a sibling reads.  Rows past t are padded with the
+// identity.  grid (1 + row blocks, H), block 256.
+__global__ void __launch_bounds__(256) k_chol_panel(float* __restrict__ mats, const int32_t* __restrict__ offsets,
+                                                    int64_t ldA, int k0, float* __restrict__ dinv,
                                                     int32_t* __restrict__ status) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
@@ -196,63 +132,110 @@ __global__ void __launch_bounds__(128) k_chol_panel(float* __restrict__ mats, co
     const int rb = blockIdx.x;
     const int r0 = k0 + CB * rb;
     if (rb > 0 && r0 >= t) return;
-    __shared__ float D[CB * (CB + 1)];
-    __shared__ float P[CB * (CB + 1)];
+    __shared__ float colb[2][CB];
+    __shared__ float sdiag[CB];
+    __shared__ float Ls[CB][CB + 1];     // L_kk, then L_kk^{-1}
+    __shared__ float Ps[CB][CB + 1];     // panel rows (rb >= 1)
     __shared__ int bad;
     float* A = mats + (int64_t)h * ldA * ldA;
-    float* Dh = dscr + (int64_t)h * CB * CB;
     const int kb = min(CB, t - k0);
-    if (rb == 0 && k0 > 0) {
-        // the previous block (k0 - 64) was not this head's last: store its factor
-        for (int e = threadIdx.x; e < CB * CB; e += blockDim.x) {
-            const int i = e / CB, j = e % CB;
-            if (j <= i) A[(int64_t)(k0 - CB + i) * ldA + k0 - CB + j] = Dh[e];
+    const int tid = threadIdx.x;
+    const int i = tid >> 2, cq = tid & 3;   // row i, columns cq + 4m
+    float a[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const int c = cq + 4 * m;
+        a[m] = (c <= i && i < kb) ? A[(int64_t)(k0 + i) * ldA + k0 + c] : (c == i ? 1.f : 0.f);
+    }
+    if (tid == 0) bad = 0;
+    if (rb > 0) {
+        const int nr = min(CB, t - r0);
+        for (int e = tid; e < CB * CB; e += 256) {
+            const int rr = e / CB, c = e % CB;
+            Ps[rr][c] = (rr < nr && c < kb) ? A[(int64_t)(r0 + rr) * ldA + k0 + c] : 0.f;
         }
     }
-    for (int e = threadIdx.x; e < kb * kb; e += blockDim.x) {
-        const int i = e / kb, j = e % kb;
-        D[i * (CB + 1) + j] = (j <= i) ? A[(int64_t)(k0 + i) * ldA + k0 + j] : 0.f;
+    // right-looking elimination on unscaled columns: after step j the
+    // trailing entries hold A - sum_{p<=j} u_p u_p^T / d_p (fully unrolled so
+    // that the register row is indexed statically)
+#pragma unroll
+    for (int j = 0; j < CB; ++j) {
+        float* cb = colb[j & 1];
+        if (cq == (j & 3)) cb[i] = a[j >> 2];
+        __syncthreads();
+        float d = cb[j];
+        if (!(d > 0.f) || !isfinite(d)) {
+            if (tid == 0) bad = 1;
+            d = 1.f;
+        }
+        const float li = cb[i] / d;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const int c = cq + 4 * m;
+            if (c > j && c <= i) a[m] = fmaf(-li, cb[c], a[m]);
+        }
     }
-    const int nr = (rb > 0) ? min(CB, t - r0) : 0;
-    for (int e = threadIdx.x; e < nr * kb; e += blockDim.x) {
-        const int i = e / kb, j = e % kb;
-        P[i * (CB + 1) + j] = A[(int64_t)(r0 + i) * ldA + k0 + j];
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        const bool ok = warp_chol_block(D, kb);
-        if (threadIdx.x == 0) bad = ok ? 0 : 1;
-    }
+#pragma unroll
+    for (int m = 0; m < 16; ++m)
+        if (cq + 4 * m == i) sdiag[i] = a[m];
     __syncthreads();
     if (bad) {
-        if (rb == 0 && threadIdx.x == 0) set_status(status, h, KVC_ERR_NOT_SPD);
+        if (rb == 0 && tid == 0) set_status(status, h, KVC_ERR_NOT_SPD);
         return;
     }
-    if (rb == 0) {
-        const bool last = (k0 + kb >= t);
-        for (int e = threadIdx.x; e < kb * kb; e += blockDim.x) {
-            const int i = e / kb, j = e % kb;
-            if (j > i) continue;
-            if (last)
-                A[(int64_t)(k0 + i) * ldA + k0 + j] = D[i * (CB + 1) + j];
-            else
-                Dh[i * CB + j] = D[i * (CB + 1) + j];
+    // L = u_ic / sqrt(d_c) below the diagonal, sqrt(d_c) on it
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const int c = cq + 4 * m;
+        Ls[i][c] = (c < i) ? a[m] / sqrtf(sdiag[c]) : (c == i ? sqrtf(sdiag[c]) : 0.f);
+    }
+    __syncthreads();
+    // L X = I by forward substitution on the rows: after step j, row j of X is final
+    float x[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) x[m] = (cq + 4 * m == i) ? 1.f : 0.f;
+    for (int j = 0; j < CB; ++j) {
+        float* rbuf = colb[j & 1];
+        if (i == j) {
+            const float inv = 1.f / Ls[j][j];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                x[m] *= inv;
+                rbuf[cq + 4 * m] = x[m];
+            }
         }
-        return;
-    }
-    // X D^T = P, row by row (forward substitution along the columns)
-    if (threadIdx.x < nr) {
-        const int i = threadIdx.x;
-        for (int j = 0; j < kb; ++j) {
-            float v = P[i * (CB + 1) + j];
-            for (int p = 0; p < j; ++p) v -= P[i * (CB + 1) + p] * D[j * (CB + 1) + p];
-            P[i * (CB + 1) + j] = v / D[j * (CB + 1) + j];
+        __syncthreads();
+        if (i > j) {
+            const float lij = Ls[i][j];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) x[m] = fmaf(-lij, rbuf[cq + 4 * m], x[m]);
         }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < nr * kb; e += blockDim.x) {
-        const int i = e / kb, j = e % kb;
-        A[(int64_t)(r0 + i) * ldA + k0 + j] = P[i * (CB + 1) + j];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) Ls[i][cq + 4 * m] = x[m];
+    __syncthreads();
+    if (rb == 0) {
+        float* Dh = dinv + ((int64_t)h * ldA + k0) * CB;
+        for (int e = tid; e < CB * CB; e += 256) Dh[e] = Ls[e / CB][e % CB];
+        return;
+    }
+    // L_ik = P L_kk^{-T}: out[rr][c] = sum_{m <= c} P[rr][m] Linv[c][m]
+    const int nr = min(CB, t - r0);
+    float acc[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) acc[m] = 0.f;
+    for (int p = 0; p < CB; ++p) {
+        const float pv = Ps[i][p];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) acc[m] = fmaf(pv, Ls[cq + 4 * m][p], acc[m]);
+    }
+    if (i < nr) {
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const int c = cq + 4 * m;
+            if (c < kb) A[(int64_t)(r0 + i) * ldA + k0 + c] = acc[m];
+        }
     }
 }
 
@@ -320,7 +303,8 @@ __global__ void __launch_bounds__(256) k_chol_update(float* __restrict__ mats, c
 enum SolveMode : int { SOLVE_VEC = 0, SOLVE_UNIT_Z = 1, SOLVE_RHS_D = 2 };
 
 struct SolveArgs {
-    const float* L;            // [H][ldA][ldA] factors
+    const float* L;            // [H][ldA][ldA] factors (off-diagonal blocks)
+    const float* dinv;         // [H][ldA/64][64][64] inverses of the diagonal blocks
     const int32_t* offsets;
     int64_t ldA;
     int mode;
@@ -338,39 +322,115 @@ struct SolveArgs {
     const int32_t* status;
 };
 
-// grid (column CTAs, H), block 256; smem: ldA + CB*(CB+1) floats.
-__global__ void __launch_bounds__(256) k_trsv_cols(SolveArgs a) {
+// (L L^T) X = B for a group of CG right-hand sides per CTA, blocked by 64
+// rows with the stored inverses of the diagonal blocks: forward
+// y_k = L_kk^{-1} (b_k - sum_{m<k} L_km y_m), then backward
+// x_k = L_kk^{-T} (y_k - sum_{m>k} L_mk^T x_m), both right-looking so every
+// block step is a dense product spread over the CTA.  The CTA keeps its
+// columns of the whole vector in shared memory.
+// grid (ceil(columns / CG), H), block 256; smem: ldA*CG + 64*65 floats.
+template <int CG>
+__global__ void __launch_bounds__(256) k_solve_cols(SolveArgs a) {
     const int h = blockIdx.y;
     if (!head_ok(a.status, h)) return;
     if (a.done && a.done[(int64_t)h * a.done_stride]) return;
-    extern __shared__ float sm[];
-    float* xs = sm;
-    float* Ds = sm + a.ldA;
     const int off = a.offsets[h];
     const int t = a.offsets[h + 1] - off;
-    const float* L = a.L + (int64_t)h * a.ldA * a.ldA;
     int ncol = 1;
     if (a.mode == SOLVE_UNIT_Z) ncol = a.nz[h];
     if (a.mode == SOLVE_RHS_D) ncol = a.d;
-    for (int c = blockIdx.x; c < ncol; c += gridDim.x) {
+    const int c0 = blockIdx.x * CG;
+    if (c0 >= ncol) return;
+    extern __shared__ float sm[];
+    float* Y = sm;                                   // [rows][CG]
+    float* Ds = sm + a.ldA * CG;                     // [64][65]
+    const int tid = threadIdx.x;
+    const int nb = (t + CB - 1) / CB;
+    const int rows = nb * CB;
+    const float* L = a.L + (int64_t)h * a.ldA * a.ldA;
+    const float* Dh = a.dinv + (int64_t)h * a.ldA * CB;
+    for (int e = tid; e < rows * CG; e += 256) {
+        const int r = e / CG, cc = e % CG, c = c0 + cc;
+        float v = 0.f;
+        if (r < t && c < ncol) {
+            if (a.mode == SOLVE_VEC) v = a.vin[off + r];
+            else if (a.mode == SOLVE_UNIT_Z) v = (r == a.zlist[(int64_t)h * a.zmax + c]) ? 1.f : 0.f;
+            else v = a.R[((int64_t)off + r) * a.d + c];
+        }
+        Y[e] = v;
+    }
+    // ---- forward
+    for (int k = 0; k < nb; ++k) {
+        const int k64 = k * CB;
         __syncthreads();
-        if (a.mode == SOLVE_VEC) {
-            for (int i = threadIdx.x; i < t; i += blockDim.x) xs[i] = a.vin[off + i];
-        } else if (a.mode == SOLVE_UNIT_Z) {
-            const int z = a.zlist[(int64_t)h * a.zmax + c];
-            for (int i = threadIdx.x; i < t; i += blockDim.x) xs[i] = (i == z) ? 1.f : 0.f;
-        } else {
-            for (int i = threadIdx.x; i < t; i += blockDim.x) xs[i] = a.R[((int64_t)off + i) * a.d + c];
+        for (int e = tid; e < CB * CB; e += 256) Ds[(e / CB) * (CB + 1) + e % CB] = Dh[(int64_t)k64 * CB + e];
+        __syncthreads();
+        float v[CG > 4 ? CG * CB / 256 + 1 : 1];
+        int nv = 0;
+        for (int e = tid; e < CB * CG; e += 256, ++nv) {
+            const int i = e / CG, cc = e % CG;
+            float s = 0.f;
+            for (int m = 0; m <= i; ++m) s = fmaf(Ds[i * (CB + 1) + m], Y[(k64 + m) * CG + cc], s);
+            v[nv] = s;
         }
-        cta_cholsolve_vec(L, t, a.ldA, xs, Ds);
-        if (a.mode == SOLVE_VEC) {
-            for (int i = threadIdx.x; i < t; i += blockDim.x) a.vout[off + i] = xs[i];
-        } else if (a.mode == SOLVE_UNIT_Z) {
-            float* wc = a.W + ((int64_t)h * a.zmax + c) * a.ldA;
-            for (int i = threadIdx.x; i < t; i += blockDim.x) wc[i] = xs[i];
-        } else {
-            for (int i = threadIdx.x; i < t; i += blockDim.x) a.X[((int64_t)off + i) * a.d + c] = xs[i];
+        __syncthreads();
+        nv = 0;
+        for (int e = tid; e < CB * CG; e += 256, ++nv) Y[k64 * CG + e] = v[nv];
+        __syncthreads();
+        const int kb = min(CB, t - k64);
+        for (int r = k64 + CB + tid; r < t; r += 256) {
+            const float* lr = L + (int64_t)r * a.ldA + k64;
+            float acc[CG];
+#pragma unroll
+            for (int cc = 0; cc < CG; ++cc) acc[cc] = 0.f;
+            for (int m = 0; m < kb; ++m) {
+                const float l = lr[m];
+#pragma unroll
+                for (int cc = 0; cc < CG; ++cc) acc[cc] = fmaf(l, Y[(k64 + m) * CG + cc], acc[cc]);
+            }
+#pragma unroll
+            for (int cc = 0; cc < CG; ++cc) Y[r * CG + cc] -= acc[cc];
         }
+    }
+    // ---- backward
+    for (int k = nb - 1; k >= 0; --k) {
+        const int k64 = k * CB;
+        __syncthreads();
+        for (int e = tid; e < CB * CB; e += 256) Ds[(e / CB) * (CB + 1) + e % CB] = Dh[(int64_t)k64 * CB + e];
+        __syncthreads();
+        float v[CG > 4 ? CG * CB / 256 + 1 : 1];
+        int nv = 0;
+        for (int e = tid; e < CB * CG; e += 256, ++nv) {
+            const int i = e / CG, cc = e % CG;
+            float s = 0.f;
+            for (int m = i; m < CB; ++m) s = fmaf(Ds[m * (CB + 1) + i], Y[(k64 + m) * CG + cc], s);
+            v[nv] = s;
+        }
+        __syncthreads();
+        nv = 0;
+        for (int e = tid; e < CB * CG; e += 256, ++nv) Y[k64 * CG + e] = v[nv];
+        __syncthreads();
+        const int kb = min(CB, t - k64);
+        for (int r = tid; r < k64; r += 256) {
+            float acc[CG];
+#pragma unroll
+            for (int cc = 0; cc < CG; ++cc) acc[cc] = 0.f;
+            for (int m = 0; m < kb; ++m) {
+                const float l = L[(int64_t)(k64 + m) * a.ldA + r];
+#pragma unroll
+                for (int cc = 0; cc < CG; ++cc) acc[cc] = fmaf(l, Y[(k64 + m) * CG + cc], acc[cc]);
+            }
+#pragma unroll
+            for (int cc = 0; cc < CG; ++cc) Y[r * CG + cc] -= acc[cc];
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < t * CG; e += 256) {
+        const int r = e / CG, cc = e % CG, c = c0 + cc;
+        if (c >= ncol) continue;
+        if (a.mode == SOLVE_VEC) a.vout[off + r] = Y[e];
+        else if (a.mode == SOLVE_UNIT_Z) a.W[((int64_t)h * a.zmax + c) * a.ldA + r] = Y[e];
+        else a.X[((int64_t)off + r) * a.d + c] = Y[e];
     }
 }
 
@@ -694,12 +754,12 @@ __global__ void k_beta_out(float* __restrict__ x, const int32_t* __restrict__ of
 }
 
 // ------------------------------------------------------------ launchers
-cudaError_t launch_chol(float* mats, const int32_t* offsets, int H, int max_t, int64_t ldA, float* dscr,
+cudaError_t launch_chol(float* mats, const int32_t* offsets, int H, int max_t, int64_t ldA, float* dinv,
                         int32_t* status, cudaStream_t st) {
     for (int k0 = 0; k0 < max_t; k0 += CB) {
         const int rows_below = max(0, max_t - k0 - CB);
         const int nrb = (rows_below + CB - 1) / CB;
-        k_chol_panel<<<dim3(1 + nrb, H), 128, 0, st>>>(mats, offsets, ldA, k0, dscr, status);
+        k_chol_panel<<<dim3(1 + nrb, H), 256, 0, st>>>(mats, offsets, ldA, k0, dinv, status);
         if (nrb > 0) {
             k_chol_update<<<dim3(nrb * (nrb + 1) / 2, H), 256, 0, st>>>(mats, offsets, ldA, k0, status);
         }
@@ -713,18 +773,25 @@ int chol_launches(int max_t) {
     return c;
 }
 
-static cudaError_t launch_trsv(const SolveArgs& a, int ncta, int H, cudaStream_t st) {
-    const size_t smem = (size_t)(a.ldA + CB * (CB + 1)) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(k_trsv_cols, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+// Solve for every column of the mode with CG columns per CTA.
+template <int CG>
+static cudaError_t launch_solve_t(const SolveArgs& a, int ncols, int H, cudaStream_t st) {
+    const size_t smem = (size_t)(a.ldA * CG + CB * (CB + 1)) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(k_solve_cols<CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_trsv_cols<<<dim3(ncta, H), 256, smem, st>>>(a);
+    k_solve_cols<CG><<<dim3((ncols + CG - 1) / CG, H), 256, smem, st>>>(a);
     return cudaGetLastError();
 }
+static cudaError_t launch_solve(const SolveArgs& a, int ncols, int H, cudaStream_t st) {
+    if (ncols <= 1) return launch_solve_t<1>(a, ncols, H, st);
+    return launch_solve_t<4>(a, ncols, H, st);
+}
 
-cudaError_t launch_cholsolve(int d, const float* L, const float* R, const int32_t* offsets, int H, int64_t ldA,
-                             float* Cv, const int32_t* status, cudaStream_t st) {
+cudaError_t launch_cholsolve(int d, const float* L, const float* dinv, const float* R, const int32_t* offsets, int H,
+                             int64_t ldA, float* Cv, const int32_t* status, cudaStream_t st) {
     SolveArgs a{};
     a.L = L;
+    a.dinv = dinv;
     a.offsets = offsets;
     a.ldA = ldA;
     a.mode = SOLVE_RHS_D;
@@ -732,7 +799,7 @@ cudaError_t launch_cholsolve(int d, const float* L, const float* R, const int32_
     a.X = Cv;
     a.d = d;
     a.status = status;
-    return launch_trsv(a, d, H, st);
+    return launch_solve(a, d, H, st);
 }
 
 static size_t bpp_smem(int64_t ldA, int zmax) {
@@ -741,7 +808,8 @@ static size_t bpp_smem(int64_t ldA, int zmax) {
 }
 
 // The whole NNLS: x0 = H^{-1} f, `max_iter` pivoting steps, refinement.
-cudaError_t launch_nnls_all(const float* L, const float* f, const int32_t* offsets, int H, int n, int max_t,
+cudaError_t launch_nnls_all(const float* L, const float* dinv, const float* f, const int32_t* offsets, int H, int n,
+                            int max_t,
                             int64_t ldA, const float* L2, float* x, float* x0, int8_t* zflag, int32_t* zlist,
                             int32_t* nz, float* W, float* S, int32_t* piv, float* u, float* r, float* d0,
                             HeadScalars* hs, int zmax, int max_iter, int refine_iters, int32_t* status,
@@ -752,13 +820,14 @@ cudaError_t launch_nnls_all(const float* L, const float* f, const int32_t* offse
     ++nl;
     SolveArgs sv{};
     sv.L = L;
+    sv.dinv = dinv;
     sv.offsets = offsets;
     sv.ldA = ldA;
     sv.status = status;
     sv.mode = SOLVE_VEC;
     sv.vin = f;
     sv.vout = x0;
-    cudaError_t e = launch_trsv(sv, 1, H, st);
+    cudaError_t e = launch_solve(sv, 1, H, st);
     if (e != cudaSuccess) return e;
     ++nl;
     const size_t smem = bpp_smem(ldA, zmax);
@@ -768,6 +837,7 @@ cudaError_t launch_nnls_all(const float* L, const float* f, const int32_t* offse
     if (e != cudaSuccess) return e;
     SolveArgs sz{};
     sz.L = L;
+    sz.dinv = dinv;
     sz.offsets = offsets;
     sz.ldA = ldA;
     sz.status = status;
@@ -781,7 +851,7 @@ cudaError_t launch_nnls_all(const float* L, const float* f, const int32_t* offse
     for (int it = 0; it < max_iter; ++it) {
         if (it > 0) {
             // columns H^{-1} e_z for the zero set chosen by the previous step
-            e = launch_trsv(sz, 32, H, st);
+            e = launch_solve(sz, zmax, H, st);
             if (e != cudaSuccess) return e;
             ++nl;
         }
@@ -796,7 +866,7 @@ cudaError_t launch_nnls_all(const float* L, const float* f, const int32_t* offse
         SolveArgs s3 = sv;
         s3.vin = r;
         s3.vout = d0;
-        e = launch_trsv(s3, 1, H, st);
+        e = launch_solve(s3, 1, H, st);
         if (e != cudaSuccess) return e;
         k_refine_apply<<<H, 512, smem, st>>>(b, d0);
         nl += 4;

@@ -141,11 +141,14 @@ __global__ void __launch_bounds__(1024) k_select(const float* __restrict__ score
 // ---------------------------------------------------------------- gather
 // grid (ceil(max_t/8), H), block 256 (one warp per kept row).
 // C_k[off+i] = K[h][idx[off+i]] (storage dtype, 16-byte vectors) and
-// Vsel[off+i] = fp32(V[h][idx[off+i]]).
+// Vsel[off+i] = fp32(V[h][idx[off+i]]).  When Ckw is given, the kept keys
+// are also copied to Ckw[h][i] (rows padded per head to ldw), the layout the
+// tensor-core mass pass reads through TMA.
 template <typename TIn, int D>
 __global__ void __launch_bounds__(256) k_gather(const TIn* __restrict__ K, const TIn* __restrict__ V, int T,
                                                 const int32_t* __restrict__ offsets, const int32_t* __restrict__ idx,
                                                 TIn* __restrict__ Ck, float* __restrict__ Vsel,
+                                                TIn* __restrict__ Ckw, int64_t ldw,
                                                 const int32_t* __restrict__ status) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
@@ -159,7 +162,12 @@ __global__ void __launch_bounds__(256) k_gather(const TIn* __restrict__ K, const
     constexpr int NV = D / VEC;
     const uint4* src = reinterpret_cast<const uint4*>(K + ((int64_t)h * T + j) * D);
     uint4* dst = reinterpret_cast<uint4*>(Ck + ((int64_t)off + i) * D);
-    for (int v = lane; v < NV; v += 32) dst[v] = src[v];
+    uint4* dw = Ckw ? reinterpret_cast<uint4*>(Ckw + ((int64_t)h * ldw + i) * D) : nullptr;
+    for (int v = lane; v < NV; v += 32) {
+        const uint4 x = src[v];
+        dst[v] = x;
+        if (dw) dw[v] = x;
+    }
     const TIn* vr = V + ((int64_t)h * T + j) * D;
     float* vo = Vsel + ((int64_t)off + i) * D;
     for (int c = lane; c < D; c += 32) vo[c] = to_f32(vr[c]);
@@ -177,19 +185,23 @@ cudaError_t launch_select(const float* score, int H, int T, const int32_t* offse
 }
 template <typename TIn, int D>
 static cudaError_t launch_gather_t(const void* K, const void* V, int H, int T, int max_t, const int32_t* offsets,
-                                   const int32_t* idx, void* Ck, float* Vsel, const int32_t* status, cudaStream_t st) {
+                                   const int32_t* idx, void* Ck, float* Vsel, void* Ckw, int64_t ldw,
+                                   const int32_t* status, cudaStream_t st) {
     dim3 grid((max_t + 7) / 8, H);
-    k_gather<TIn, D><<<grid, 256, 0, st>>>((const TIn*)K, (const TIn*)V, T, offsets, idx, (TIn*)Ck, Vsel, status);
+    k_gather<TIn, D><<<grid, 256, 0, st>>>((const TIn*)K, (const TIn*)V, T, offsets, idx, (TIn*)Ck, Vsel, (TIn*)Ckw,
+                                           ldw, status);
     return cudaGetLastError();
 }
 cudaError_t launch_gather(int dtype, int d, const void* K, const void* V, int H, int T, int max_t,
-                          const int32_t* offsets, const int32_t* idx, void* Ck, float* Vsel, const int32_t* status,
-                          cudaStream_t st) {
+                          const int32_t* offsets, const int32_t* idx, void* Ck, float* Vsel, void* Ckw, int64_t ldw,
+                          const int32_t* status, cudaStream_t st) {
     if (dtype == KVC_DTYPE_BF16)
-        return d == 128 ? launch_gather_t<__nv_bfloat16, 128>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, status, st)
-                        : launch_gather_t<__nv_bfloat16, 64>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, status, st);
-    return d == 128 ? launch_gather_t<float, 128>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, status, st)
-                    : launch_gather_t<float, 64>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, status, st);
+        return d == 128 ? launch_gather_t<__nv_bfloat16, 128>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, Ckw, ldw,
+                                                              status, st)
+                        : launch_gather_t<__nv_bfloat16, 64>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, Ckw, ldw,
+                                                             status, st);
+    return d == 128 ? launch_gather_t<float, 128>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, nullptr, 0, status, st)
+                    : launch_gather_t<float, 64>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, nullptr, 0, status, st);
 }
 
 }  // namespace kvc
