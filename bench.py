@@ -122,7 +122,7 @@ def stage_work(w, buds):
         "gather": ("bytes", 2.0 * st * d * b_in + st * d * (b_in + 4) + 4.0 * st),
         "masslogits": ("flops", 2.0 * n * d * st),
         "gram_a": ("flops", float(sum(n * ti * (ti + 1) for ti in t))),
-        "chol_h": ("flops", float(sum(ti ** 3 / 3.0 for ti in t))),
+        "inv_h": ("flops", float(sum(float(ti) ** 3 for ti in t))),
         "gram_x": ("flops", float(sum(n * ti * (ti + 1) for ti in t))),
         "xto": ("flops", 2.0 * n * d * st),
         "chol_m": ("flops", float(sum(ti ** 3 / 3.0 for ti in t))),
@@ -138,8 +138,10 @@ MUFU_PEAK_TEXP = 148 * 16 * 2.032e9 / 1e12
 def tensor_stages(w) -> set[str]:
     """Stages that run on the tensor cores (bf16 operands, fp32 accumulation)
     for this workload; the others run on the CUDA cores (fp32 FFMA) or are
-    memory-bound."""
-    return {"attn_fwd", "colscore"} if w.dtype == "bf16" else set()
+    memory-bound.  The Gram products run on the tensor cores for every input
+    dtype (their fp32 operands are split into two bf16 terms)."""
+    grams = {"gram_a", "gram_x", "xto"}
+    return grams | ({"attn_fwd", "colscore", "masslogits"} if w.dtype == "bf16" else set())
 
 
 TENSOR_STAGES: set[str] = set()

@@ -3,7 +3,7 @@
 // C_v by least squares through the normal equations; the Gram products
 // themselves are in gram_tc.cu):
 //   k_ridge_*      mu / lambda from the trace, added to the diagonal
-//   k_xsoftmax     X_qi = softmax_i(l2_qi + log2 w_i), in place over l2
+//   k_xsoftmax     X_qi = softmax_i(l2_qi + log2 w_i), as bf16 hi / lo terms
 // Matrices are per head, row-major with leading dimension ldA (a multiple
 // of 64); only the lower triangle of G / M is read.
 #include "common.cuh"
@@ -48,32 +48,53 @@ __global__ void k_ridge_g(float* __restrict__ G, const float* __restrict__ b, co
     if (threadIdx.x == 0) hs[h].mu = mu;
 }
 
-// C_v ridge: lam = eps * tr(M)/t; M += lam I; R += lam Vsel.  grid H, block 256.
+// C_v ridge: lam = eps * tr(M)/t; M += lam I; R += lam Vsel.
+// k_ridge_m: grid (chunks, H), block 256: every CTA forms the trace (t
+// entries) and updates its 4096-element slice of R; CTA 0 records lam.
+// k_ridge_m_diag then adds lam to the diagonal (a separate launch, so that
+// no CTA of the first one can read an already shifted diagonal).
+constexpr int kRidgeChunk = 4096;
+
 template <int D>
 __global__ void k_ridge_m(float* __restrict__ M, float* __restrict__ R, const float* __restrict__ Vsel,
                           const int32_t* __restrict__ offsets, int64_t ldA, float eps, HeadScalars* __restrict__ hs,
                           int32_t* __restrict__ status) {
-    const int h = blockIdx.x;
+    const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     __shared__ double sred[32];
     const int off = offsets[h];
     const int t = offsets[h + 1] - off;
+    const int64_t e0 = (int64_t)blockIdx.x * kRidgeChunk;
+    if (e0 >= (int64_t)t * D) return;
     float* Mh = M + (int64_t)h * ldA * ldA;
     const double tr = block_trace(Mh, t, ldA, sred);
     if (!isfinite(tr) || !(tr > 0.0)) {
-        if (threadIdx.x == 0) set_status(status, h, KVC_ERR_NONFINITE);
+        if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, h, KVC_ERR_NONFINITE);
         return;
     }
     const float lam = (float)(eps * tr / t);
-    for (int i = threadIdx.x; i < t; i += blockDim.x) Mh[(int64_t)i * ldA + i] += lam;
-    for (int e = threadIdx.x; e < t * D; e += blockDim.x) R[(int64_t)off * D + e] += lam * Vsel[(int64_t)off * D + e];
-    if (threadIdx.x == 0) hs[h].lam = lam;
+    const int64_t e1 = min((int64_t)t * D, e0 + kRidgeChunk);
+    for (int64_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) R[(int64_t)off * D + e] += lam * Vsel[(int64_t)off * D + e];
+    if (blockIdx.x == 0 && threadIdx.x == 0) hs[h].lam = lam;
 }
 
-// X_qi = softmax_i(l2_qi + log2 w_i) over i < t (padding columns set to 0),
-// in place.  grid (ceil(n/8), H), block 256 (one warp per row).
-__global__ void __launch_bounds__(256) k_xsoftmax(float* __restrict__ L2, const float* __restrict__ w,
+// grid H, block 256.
+__global__ void k_ridge_m_diag(float* __restrict__ M, const int32_t* __restrict__ offsets, int64_t ldA,
+                               const HeadScalars* __restrict__ hs, const int32_t* __restrict__ status) {
+    const int h = blockIdx.x;
+    if (!head_ok(status, h)) return;
+    const int t = offsets[h + 1] - offsets[h];
+    const float lam = hs[h].lam;
+    float* Mh = M + (int64_t)h * ldA * ldA;
+    for (int i = threadIdx.x; i < t; i += blockDim.x) Mh[(int64_t)i * ldA + i] += lam;
+}
+
+// X_qi = softmax_i(l2_qi + log2 w_i) over i < t, written as bf16 hi / lo
+// terms (the Gram operand format, see gram_tc.cu); padding columns up to the
+// next multiple of 64 are 0.  grid (ceil(n/8), H), block 256 (one warp per row).
+__global__ void __launch_bounds__(256) k_xsoftmax(const float* __restrict__ L2, const float* __restrict__ w,
                                                   const int32_t* __restrict__ offsets, int n, int64_t ldA,
+                                                  __nv_bfloat16* __restrict__ Xh, __nv_bfloat16* __restrict__ Xl,
                                                   const int32_t* __restrict__ status) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
@@ -82,7 +103,8 @@ __global__ void __launch_bounds__(256) k_xsoftmax(float* __restrict__ L2, const 
     const int q = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (q >= n) return;
-    float* row = L2 + ((int64_t)h * n + q) * ldA;
+    const int64_t ro = ((int64_t)h * n + q) * ldA;
+    const float* row = L2 + ro;
     float mx = -INFINITY;
     for (int i = lane; i < t; i += 32) mx = fmaxf(mx, row[i] + log2f(w[off + i]));
     mx = warp_max(mx);
@@ -94,7 +116,9 @@ __global__ void __launch_bounds__(256) k_xsoftmax(float* __restrict__ L2, const 
     for (int i = lane; i < tp; i += 32) {
         float x = 0.f;
         if (i < t && inv > 0.f) x = exp2f(row[i] + log2f(w[off + i]) - mx) * inv;
-        row[i] = x;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+        Xh[ro + i] = hi;
+        Xl[ro + i] = __float2bfloat16_rn(x - __bfloat162float(hi));
     }
 }
 
@@ -106,16 +130,19 @@ cudaError_t launch_ridge_g(float* G, const float* b, const int32_t* offsets, int
 }
 cudaError_t launch_ridge_m(int d, float* M, float* R, const float* Vsel, const int32_t* offsets, int H, int64_t ldA,
                            float eps, HeadScalars* hs, int32_t* status, cudaStream_t st) {
+    // launched before M is factored, after R is complete; the max_t bound is ldA
+    const int chunks = (int)(((int64_t)ldA * d + kRidgeChunk - 1) / kRidgeChunk);
     if (d == 128)
-        k_ridge_m<128><<<H, 256, 0, st>>>(M, R, Vsel, offsets, ldA, eps, hs, status);
+        k_ridge_m<128><<<dim3(chunks, H), 256, 0, st>>>(M, R, Vsel, offsets, ldA, eps, hs, status);
     else
-        k_ridge_m<64><<<H, 256, 0, st>>>(M, R, Vsel, offsets, ldA, eps, hs, status);
+        k_ridge_m<64><<<dim3(chunks, H), 256, 0, st>>>(M, R, Vsel, offsets, ldA, eps, hs, status);
+    k_ridge_m_diag<<<H, 256, 0, st>>>(M, offsets, ldA, hs, status);
     return cudaGetLastError();
 }
-cudaError_t launch_xsoftmax(float* L2, const float* w, const int32_t* offsets, int H, int n, int64_t ldA,
-                            const int32_t* status, cudaStream_t st) {
+cudaError_t launch_xsoftmax(const float* L2, const float* w, const int32_t* offsets, int H, int n, int64_t ldA,
+                            void* Xh, void* Xl, const int32_t* status, cudaStream_t st) {
     dim3 grid((n + 7) / 8, H);
-    k_xsoftmax<<<grid, 256, 0, st>>>(L2, w, offsets, n, ldA, status);
+    k_xsoftmax<<<grid, 256, 0, st>>>(L2, w, offsets, n, ldA, (__nv_bfloat16*)Xh, (__nv_bfloat16*)Xl, status);
     return cudaGetLastError();
 }
 

@@ -2,33 +2,26 @@
 // Compaction via Attention Matching", section 2, fitting beta by NNLS and
 // C_v by least squares through the normal equations):
 //
-//   G = A'^T A'   (mass matrix, t x t, lower tiles)
-//   M = X^T X     (biased softmax, t x t, lower tiles)
+//   G = A'^T A'   (mass matrix, t x t; lower tiles computed, mirrored)
+//   M = X^T X     (biased softmax, t x t; lower tiles computed, mirrored)
 //   R = X^T O     (t x d)
 //
-// C[i][j] = sum_q A[q][i] B[q][j] over the n reference queries, with A and B
-// fp32 row-major [n][ld].  The products run on the tcgen05 tensor cores in
-// bf16 with three terms per product: every operand is split as x = hi + lo
-// with hi = bf16(x) and lo = bf16(x - hi) (round to nearest), and C
-// accumulates A_hi B_hi + A_hi B_lo + A_lo B_hi in fp32.  The split carries
-// ~2^-17 of each value and the dropped A_lo B_lo term is ~2^-18 relative;
-// both errors have random sign, so a sum over the queries keeps close to fp32
-// accuracy.  (Both operands are MN-major here: the queries are the
-// contraction and the outer dimension of the stored matrices.)
-//
-// For G the stored operand is log2 A' (as the mass-logit pass writes it) and
-// the split stage applies exp2 first; the CTAs of the first column tile also
-// sum A' over the queries, b = A'^T 1, per column, in double, in a fixed
-// order.
+// C[i][j] = sum_q A[q][i] B[q][j] over the n reference queries.  Every fp32
+// operand value x is stored as two bf16 terms, hi = bf16(x) and
+// lo = bf16(x - hi) (round to nearest), in separate [H][n][ld] arrays
+// written once by the pass that produces the operand (k_split_hilo below for
+// A' and O, the biased softmax for X).  The products run on the tcgen05
+// tensor cores in bf16: C accumulates A_hi B_hi + A_hi B_lo + A_lo B_hi in
+// fp32.  The split carries ~2^-17 of each value and the dropped A_lo B_lo
+// term is ~2^-18 relative; both errors have random sign, so a sum over the
+// queries keeps close to fp32 accuracy.  (Both operands are MN-major: the
+// queries are the contraction and the outer dimension of the stored arrays.)
 //
 // One CTA per 128 x 128 output tile (x head).  Warp roles:
-//   warp 0       TMA producer: raw fp32 tiles [32 queries][32 columns] with
-//                128-byte swizzle, four per 128-column operand tile
+//   warp 0       TMA producer: [64 queries][64 columns] bf16 boxes with
+//                128-byte swizzle (the MN-major operand layout), 8 per stage
 //   warp 1       MMA issuer; owns the TMEM accumulator (128 columns)
-//   warps 2..5   split every landed fp32 element into bf16 (hi, lo) and write
-//                them into the MN-major 128-byte-swizzled operand layout
-//                ([32 queries][64 columns] blocks), then run the epilogue
-//                (TMEM -> global)
+//   warps 2..5   epilogue (TMEM -> global)
 #include "tc.cuh"
 
 namespace kvc {
@@ -37,18 +30,13 @@ using namespace tc;
 namespace {
 
 constexpr int GB = 128;                 // output tile
-constexpr int GK = 32;                  // queries per pipeline stage
-constexpr int kGBox = GK * 128;         // one [32][32] fp32 box, or one [32][64] bf16 block: 4 KB
-constexpr int kOpBytes = 4 * kGBox;     // one 128-column fp32 operand tile: 16 KB
+constexpr int GK = 64;                  // queries per pipeline stage
+constexpr int kGBox = GK * 128;         // one [64 queries][64 columns] bf16 box: 8 KB
 constexpr int kStages = 3;
 constexpr int kGThreads = 192;
 
 __device__ __forceinline__ uint8_t* align1024g(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
@@ -65,8 +53,7 @@ __device__ __forceinline__ void tri_tile(int p, int& I, int& J) {
 }
 
 struct GramArgs {
-    float* C;                    // [H][ldc_rows][ldc] (symmetric) or off-indexed [sum t][ldc] (rect)
-    float* colsum;               // EXP mode: b[off + i] = sum_q A'[q][i]
+    float* C;                    // [H][ldc][ldc] (symmetric) or off-indexed [sum t][ldc] (rect)
     const int32_t* offsets;
     int64_t ldc;
     int n;
@@ -74,31 +61,14 @@ struct GramArgs {
     int32_t* status;
 };
 
-// One float4 of a landed raw tile (4 consecutive columns of one query row)
-// -> bf16 (hi, lo) pairs.  EXP applies exp2 first and zeroes rows past the
-// last query (the TMA fill value 0 would become 1).  Returns the fp32 values
-// (for the column sums).
-template <bool EXP>
-__device__ __forceinline__ float4 split4(float4 x, uint2& hi, uint2& lo, bool row_valid) {
-    if (EXP) {
-        x.x = row_valid ? exp2f(x.x) : 0.f;
-        x.y = row_valid ? exp2f(x.y) : 0.f;
-        x.z = row_valid ? exp2f(x.z) : 0.f;
-        x.w = row_valid ? exp2f(x.w) : 0.f;
-    }
-    hi.x = pack_bf16(x.x, x.y);
-    hi.y = pack_bf16(x.z, x.w);
-    lo.x = pack_bf16(x.x - bf16_lo(hi.x), x.y - bf16_hi(hi.x));
-    lo.y = pack_bf16(x.z - bf16_lo(hi.y), x.w - bf16_hi(hi.y));
-    return x;
-}
-
-// grid (tiles, H), block 192.  SYM: lower tiles of the t x t product of A with
-// itself (B map = A map), written to C[h] with leading dimension ldc.  RECT:
-// tiles (I, 0) of A^T B with B [n][nb], written to C[off + i][j].
-template <bool SYM, int NB, bool EXP>
+// grid (tiles, H), block 192.  SYM: lower tiles of the t x t product of A
+// with itself (B maps = A maps), written to C[h] with leading dimension ldc
+// and mirrored into the upper triangle.  RECT: tiles (I, 0) of A^T B with B
+// [n][nb], written to C[off + i][j].  Maps: bf16 hi / lo arrays.
+template <bool SYM, int NB>
 __global__ void __launch_bounds__(kGThreads, 1)
-    k_gram_tc(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB, GramArgs g) {
+    k_gram_tc(const __grid_constant__ CUtensorMap mAh, const __grid_constant__ CUtensorMap mAl,
+              const __grid_constant__ CUtensorMap mBh, const __grid_constant__ CUtensorMap mBl, GramArgs g) {
     const int h = blockIdx.y;
     if (!head_ok(g.status, h)) return;
     const int off = g.offsets[h];
@@ -110,19 +80,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
         J = 0;
     }
     if (I * GB >= t) return;
-    constexpr int kBBytes = (NB / 32) * kGBox;               // raw fp32 B tile
-    // stage: raw A | raw B | A hi | A lo | B hi | B lo (bf16 tiles are half size)
-    constexpr int kAHi = kOpBytes + kBBytes;
-    constexpr int kALo = kAHi + kOpBytes / 2;
-    constexpr int kBHi = kALo + kOpBytes / 2;
-    constexpr int kBLo = kBHi + kBBytes / 2;
-    constexpr int kStage = kBLo + kBBytes / 2;
+    constexpr int kA = 2 * kGBox;                 // one 128-column operand term
+    constexpr int kB = (NB / 64) * kGBox;
+    constexpr int kAH = 0, kAL = kA, kBH = 2 * kA, kBL = 2 * kA + kB;
+    constexpr int kStage = 2 * kA + 2 * kB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024g(smem_raw);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kStages * kStage);
     uint64_t* full = bars;                  // [kStages] TMA landed
-    uint64_t* conv = full + kStages;        // [kStages] split done (128 arrivals)
-    uint64_t* empty = conv + kStages;       // [kStages] MMAs done reading
+    uint64_t* empty = full + kStages;       // [kStages] MMAs done reading
     uint64_t* acc_full = empty + kStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -130,7 +96,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(conv + s, 128);
             mbar_init(empty + s, 1);
         }
         mbar_init(acc_full, 1);
@@ -143,21 +108,27 @@ __global__ void __launch_bounds__(kGThreads, 1)
     fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const int nk = (g.n + GK - 1) / GK;
-    auto stage_ptr = [&](int s) { return sm + s * kStage; };
 
     if (warp == 0) {
         if (lane == 0) {
-            prefetch_tmap(&mA);
-            prefetch_tmap(&mB);
+            prefetch_tmap(&mAh);
+            prefetch_tmap(&mAl);
+            prefetch_tmap(&mBh);
+            prefetch_tmap(&mBl);
             int issued = 0;
             for (int k = 0; k < nk; ++k) {
                 const int s = k % kStages;
                 if (k >= kStages && !mbar_wait(empty + s, (uint32_t)((k / kStages) - 1) & 1u, abort_flag)) break;
-                uint8_t* st = stage_ptr(s);
-                mbar_expect_tx(full + s, (uint32_t)(kOpBytes + kBBytes));
-                for (int b = 0; b < 4; ++b) tma_load_3d(st + b * kGBox, &mA, full + s, I * GB + 32 * b, k * GK, h);
-                for (int b = 0; b < NB / 32; ++b)
-                    tma_load_3d(st + kOpBytes + b * kGBox, &mB, full + s, J * GB + 32 * b, k * GK, h);
+                uint8_t* st = sm + s * kStage;
+                mbar_expect_tx(full + s, (uint32_t)kStage);
+                for (int b = 0; b < 2; ++b) {
+                    tma_load_3d(st + kAH + b * kGBox, &mAh, full + s, I * GB + 64 * b, k * GK, h);
+                    tma_load_3d(st + kAL + b * kGBox, &mAl, full + s, I * GB + 64 * b, k * GK, h);
+                }
+                for (int b = 0; b < NB / 64; ++b) {
+                    tma_load_3d(st + kBH + b * kGBox, &mBh, full + s, J * GB + 64 * b, k * GK, h);
+                    tma_load_3d(st + kBL + b * kGBox, &mBl, full + s, J * GB + 64 * b, k * GK, h);
+                }
                 issued = k + 1;
             }
             for (int k = (issued > kStages ? issued - kStages : 0); k < issued; ++k)
@@ -169,17 +140,17 @@ __global__ void __launch_bounds__(kGThreads, 1)
             constexpr uint32_t idesc = idesc_bf16(128, NB, true, true);
             for (int k = 0; k < nk; ++k) {
                 const int s = k % kStages;
-                if (!mbar_wait(conv + s, (uint32_t)(k / kStages) & 1u, abort_flag)) break;
+                if (!mbar_wait(full + s, (uint32_t)(k / kStages) & 1u, abort_flag)) break;
                 fence_after_sync();
-                const uint32_t st = smem_addr(stage_ptr(s));
+                const uint32_t st = smem_addr(sm + s * kStage);
 #pragma unroll
                 for (int kk = 0; kk < GK / 16; ++kk) {
                     // 16 queries = two 8-row groups; 64-column blocks kGBox apart
                     const uint32_t o = (uint32_t)kk * 2048;
-                    const uint64_t dAH = sdesc_sw128(st + kAHi + o, kGBox, 1024);
-                    const uint64_t dAL = sdesc_sw128(st + kALo + o, kGBox, 1024);
-                    const uint64_t dBH = sdesc_sw128(st + kBHi + o, kGBox, 1024);
-                    const uint64_t dBL = sdesc_sw128(st + kBLo + o, kGBox, 1024);
+                    const uint64_t dAH = sdesc_sw128(st + kAH + o, kGBox, 1024);
+                    const uint64_t dAL = sdesc_sw128(st + kAL + o, kGBox, 1024);
+                    const uint64_t dBH = sdesc_sw128(st + kBH + o, kGBox, 1024);
+                    const uint64_t dBL = sdesc_sw128(st + kBL + o, kGBox, 1024);
                     mma_ss(tmem, dAH, dBH, idesc, (k > 0 || kk > 0) ? 1u : 0u);
                     mma_ss(tmem, dAH, dBL, idesc, 1u);
                     mma_ss(tmem, dAL, dBH, idesc, 1u);
@@ -191,76 +162,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         __syncwarp();
     } else {
-        const int ct = threadIdx.x - 64;            // 0..127
-        // Column sums (EXP mode, first column tile): float4 e = ct + 128 m of
-        // the A tile lies in box m/2, row (ct/8) + 16 (m%2), and its 16-byte
-        // chunk is the logical chunk (ct%8) ^ ((ct/8)%8) under the 128-byte
-        // swizzle, so each thread always sees the same 16 columns.
-        const bool do_b = EXP && J == 0;
-        double bsum[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) bsum[q] = 0.0;
-        bool ok = true;
-        for (int k = 0; k < nk; ++k) {
-            const int s = k % kStages;
-            ok = __all_sync(0xffffffffu, mbar_wait(full + s, (uint32_t)(k / kStages) & 1u, abort_flag));
-            if (!ok) break;
-            uint8_t* st = stage_ptr(s);
-            // float4 e = ct + 128 m of a raw tile: box m / 2, query row
-            // (ct / 8) + 16 (m % 2), physical 16-byte chunk ct % 8, logical
-            // chunk lc = (ct % 8) ^ (row % 8) -> columns 32 (m / 2) + 4 lc ..+3.
-            // Its bf16 image goes to 64-column block m / 4, logical chunk
-            // ((m / 2) % 2) * 4 + lc / 2, half lc % 2, swizzled by row % 8.
-            const int r0 = k * GK + (ct >> 3);
-            const int lc = (ct & 7) ^ ((ct >> 3) & 7);
-            const float4* raw = reinterpret_cast<const float4*>(st);
-#pragma unroll
-            for (int m = 0; m < kOpBytes / 16 / 128; ++m) {
-                const int q = (ct >> 3) + 16 * (m & 1);
-                uint2 hi, lo;
-                const float4 v = split4<EXP>(raw[ct + 128 * m], hi, lo, r0 + 16 * (m & 1) < g.n);
-                if (do_b) {
-                    bsum[(m >> 1) * 4 + 0] += (double)v.x;
-                    bsum[(m >> 1) * 4 + 1] += (double)v.y;
-                    bsum[(m >> 1) * 4 + 2] += (double)v.z;
-                    bsum[(m >> 1) * 4 + 3] += (double)v.w;
-                }
-                const int lc2 = ((m >> 1) & 1) * 4 + (lc >> 1);
-                const int byte = (m >> 2) * kGBox + q * 128 + ((lc2 ^ (q & 7)) << 4) + (lc & 1) * 8;
-                *reinterpret_cast<uint2*>(st + kAHi + byte) = hi;
-                *reinterpret_cast<uint2*>(st + kALo + byte) = lo;
-            }
-            const float4* rawb = reinterpret_cast<const float4*>(st + kOpBytes);
-#pragma unroll
-            for (int m = 0; m < kBBytes / 16 / 128; ++m) {
-                const int q = (ct >> 3) + 16 * (m & 1);
-                uint2 hi, lo;
-                (void)split4<EXP>(rawb[ct + 128 * m], hi, lo, r0 + 16 * (m & 1) < g.n);
-                const int lc2 = ((m >> 1) & 1) * 4 + (lc >> 1);
-                const int byte = (m >> 2) * kGBox + q * 128 + ((lc2 ^ (q & 7)) << 4) + (lc & 1) * 8;
-                *reinterpret_cast<uint2*>(st + kBHi + byte) = hi;
-                *reinterpret_cast<uint2*>(st + kBLo + byte) = lo;
-            }
-            fence_proxy_async();
-            mbar_arrive(conv + s);
-        }
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag));
-        if (do_b) {
-            // every MMA is done, so stage 0 can hold the [16][128] partial sums
-            double* red = reinterpret_cast<double*>(sm);
-            const int grp = ct >> 3, chunk = (ct & 7) ^ ((ct >> 3) & 7);
-            if (ok) {
-#pragma unroll
-                for (int q = 0; q < 16; ++q) red[grp * 128 + (q >> 2) * 32 + chunk * 4 + (q & 3)] = bsum[q];
-            }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            const int i = I * GB + ct;
-            if (ok && i < t) {
-                double v = 0.0;
-                for (int r = 0; r < 16; ++r) v += red[r * 128 + ct];
-                g.colsum[off + i] = (float)v;
-            }
-        }
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag));
         if (ok) {
             fence_after_sync();
             const int quarter = warp & 3;
@@ -288,6 +190,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
                         for (int q = 0; q < 32; ++q)
                             if (j0 + q < jmax) dst[q] = __uint_as_float(r[q]);
                     }
+                    if (SYM && I != J) {
+                        // mirror into the upper triangle (the sweep inverse reads
+                        // both); for a fixed column a warp writes 32 consecutive rows
+                        float* dT = g.C + ((int64_t)h * g.ldc + j0) * g.ldc + i;
+#pragma unroll 4
+                        for (int q = 0; q < 32; ++q)
+                            if (j0 + q < jmax) dT[(int64_t)q * g.ldc] = __uint_as_float(r[q]);
+                    }
                 }
             }
         }
@@ -301,55 +211,126 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
 template <int NB>
 constexpr int gram_smem() {
-    // per stage: raw fp32 A and B, plus bf16 hi and lo images of both (same total bytes)
-    return kStages * 2 * (kOpBytes + (NB / 32) * kGBox) + 256 + 1024;
+    return kStages * (4 * kGBox + 2 * (NB / 64) * kGBox) + 256 + 1024;
+}
+
+// fp32 [H][rows][ld] (first `cols` columns) -> bf16 hi / lo arrays of the same
+// shape; EXP: the stored values are log2 x.  Columns in [cols, cpad) are
+// written as 0.  When colsum is given, the CTA's 128-row column sums of x go
+// to colsum[rowtile][off + c] (fp32), to be added in a fixed order.
+// grid (ceil(cpad / 64), ceil(rows / 128), H), block 256 (64 columns x 4 row groups).
+template <bool EXP>
+__global__ void __launch_bounds__(256) k_split_hilo(const float* __restrict__ X, int rows, int64_t ld,
+                                                    const int32_t* __restrict__ offsets, int fixed_cols,
+                                                    __nv_bfloat16* __restrict__ Xh, __nv_bfloat16* __restrict__ Xl,
+                                                    float* __restrict__ colsum, int64_t colsum_stride,
+                                                    const int32_t* __restrict__ status) {
+    const int h = blockIdx.z;
+    if (!head_ok(status, h)) return;
+    const int off = offsets ? offsets[h] : 0;
+    const int cols = offsets ? offsets[h + 1] - off : fixed_cols;
+    const int cpad = (int)round_up(cols, 64);
+    const int c = blockIdx.x * 64 + (threadIdx.x & 63);
+    if (blockIdx.x * 64 >= cpad) return;
+    const int rg = threadIdx.x >> 6;
+    const int q0 = blockIdx.y * 128;
+    float s = 0.f;
+    for (int q = q0 + rg; q < min(rows, q0 + 128); q += 4) {
+        const int64_t e = ((int64_t)h * rows + q) * ld + c;
+        float x = 0.f;
+        if (c < cols) x = EXP ? exp2f(X[e]) : X[e];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+        Xh[e] = hi;
+        Xl[e] = __float2bfloat16_rn(x - __bfloat162float(hi));
+        s += x;
+    }
+    if (colsum) {
+        __shared__ float red[4][64];
+        red[rg][threadIdx.x & 63] = s;
+        __syncthreads();
+        if (rg == 0 && c < cols)
+            colsum[(int64_t)blockIdx.y * colsum_stride + off + c] =
+                (red[0][threadIdx.x] + red[1][threadIdx.x]) + (red[2][threadIdx.x] + red[3][threadIdx.x]);
+    }
+}
+
+// b[off + c] = sum over row tiles of colsum (double, fixed order).  grid (ceil(max_t / 256), H).
+__global__ void k_colsum_total(const float* __restrict__ colsum, int ntiles, int64_t stride,
+                               const int32_t* __restrict__ offsets, float* __restrict__ b,
+                               const int32_t* __restrict__ status) {
+    const int h = blockIdx.y;
+    if (!head_ok(status, h)) return;
+    const int off = offsets[h];
+    const int t = offsets[h + 1] - off;
+    const int c = blockIdx.x * 256 + threadIdx.x;
+    if (c >= t) return;
+    double v = 0.0;
+    for (int k = 0; k < ntiles; ++k) v += (double)colsum[(int64_t)k * stride + off + c];
+    b[off + c] = (float)v;
 }
 
 }  // namespace
 
-bool make_map_f32(CUtensorMap* m, const void* base, int cols, int64_t ld, int rows, int H);   // tmap.cu
+bool make_map_bf16(CUtensorMap* m, const void* base, int cols, int64_t ld, int rows, int H);   // tmap.cu
 
-// C = A^T A (lower tiles) for A fp32 [H][n][ld] with t_h columns per head.
-// exp_mode: the stored values are log2 A (C = exp2(.)^T exp2(.)), and the
-// column sums of exp2(A) go to colsum (off-indexed).
-cudaError_t launch_gram_sym_tc(bool exp_mode, const float* A, const int32_t* offsets, int H, int n, int max_t,
-                               int64_t ld, float* C, int64_t ldc, float* colsum, int32_t* status, cudaStream_t st) {
-    CUtensorMap mA;
-    if (!make_map_f32(&mA, A, (int)ld, ld, n, H)) return cudaErrorInvalidValue;
+// C = A^T A (lower tiles, mirrored) from the hi / lo arrays of A
+// ([H][n][ld] bf16), t_h columns per head.
+cudaError_t launch_gram_sym_tc(const void* Ah, const void* Al, const int32_t* offsets, int H, int n, int max_t,
+                               int64_t ld, float* C, int64_t ldc, int32_t* status, cudaStream_t st) {
+    CUtensorMap mh, ml;
+    if (!make_map_bf16(&mh, Ah, (int)ld, ld, n, H) || !make_map_bf16(&ml, Al, (int)ld, ld, n, H))
+        return cudaErrorInvalidValue;
     constexpr int smem = gram_smem<128>();
+    cudaError_t e = cudaFuncSetAttribute(k_gram_tc<true, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
     const int nt = (max_t + GB - 1) / GB;
-    GramArgs g{C, colsum, offsets, ldc, n, 0, status};
-    dim3 grid(nt * (nt + 1) / 2, H);
-    if (exp_mode) {
-        cudaError_t e = cudaFuncSetAttribute(k_gram_tc<true, 128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    GramArgs g{C, offsets, ldc, n, 0, status};
+    k_gram_tc<true, 128><<<dim3(nt * (nt + 1) / 2, H), kGThreads, smem, st>>>(mh, ml, mh, ml, g);
+    return cudaGetLastError();
+}
+
+// C[off + i][j] = sum_q A[q][i] B[q][j] from hi / lo arrays: A [H][n][ld], B [H][n][d].
+cudaError_t launch_gram_rect_tc(int d, const void* Ah, const void* Al, const void* Bh, const void* Bl,
+                                const int32_t* offsets, int H, int n, int max_t, int64_t ld, float* C,
+                                int32_t* status, cudaStream_t st) {
+    CUtensorMap mah, mal, mbh, mbl;
+    if (!make_map_bf16(&mah, Ah, (int)ld, ld, n, H) || !make_map_bf16(&mal, Al, (int)ld, ld, n, H) ||
+        !make_map_bf16(&mbh, Bh, d, d, n, H) || !make_map_bf16(&mbl, Bl, d, d, n, H))
+        return cudaErrorInvalidValue;
+    GramArgs g{C, offsets, d, n, d, status};
+    dim3 grid((max_t + GB - 1) / GB, H);
+    if (d == 128) {
+        constexpr int smem = gram_smem<128>();
+        cudaError_t e = cudaFuncSetAttribute(k_gram_tc<false, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        k_gram_tc<true, 128, true><<<grid, kGThreads, smem, st>>>(mA, mA, g);
+        k_gram_tc<false, 128><<<grid, kGThreads, smem, st>>>(mah, mal, mbh, mbl, g);
     } else {
-        cudaError_t e = cudaFuncSetAttribute(k_gram_tc<true, 128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        constexpr int smem = gram_smem<64>();
+        cudaError_t e = cudaFuncSetAttribute(k_gram_tc<false, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        k_gram_tc<true, 128, false><<<grid, kGThreads, smem, st>>>(mA, mA, g);
+        k_gram_tc<false, 64><<<grid, kGThreads, smem, st>>>(mah, mal, mbh, mbl, g);
     }
     return cudaGetLastError();
 }
 
-// C[off + i][j] = sum_q A[q][i] B[q][j] for A fp32 [H][n][ld], B fp32 [H][n][d].
-cudaError_t launch_gram_rect_tc(int d, const float* A, const float* B, const int32_t* offsets, int H, int n,
-                                int max_t, int64_t ld, float* C, int32_t* status, cudaStream_t st) {
-    CUtensorMap mA, mB;
-    if (!make_map_f32(&mA, A, (int)ld, ld, n, H) || !make_map_f32(&mB, B, d, d, n, H)) return cudaErrorInvalidValue;
-    GramArgs g{C, nullptr, offsets, d, n, d, status};
-    dim3 grid((max_t + GB - 1) / GB, H);
-    if (d == 128) {
-        constexpr int smem = gram_smem<128>();
-        cudaError_t e = cudaFuncSetAttribute(k_gram_tc<false, 128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        k_gram_tc<false, 128, false><<<grid, kGThreads, smem, st>>>(mA, mB, g);
-    } else {
-        constexpr int smem = gram_smem<64>();
-        cudaError_t e = cudaFuncSetAttribute(k_gram_tc<false, 64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        k_gram_tc<false, 64, false><<<grid, kGThreads, smem, st>>>(mA, mB, g);
-    }
+// fp32 [H][rows][ld] -> bf16 hi / lo.  offsets given: t_h addressed columns
+// per head (padded to 64 with zeros); else `cols` for every head.  exp_mode:
+// stored values are log2.  colsum (optional): b = column sums, through the
+// per-row-tile partials in `part` ([ceil(rows/128)][H * max_t]).
+cudaError_t launch_split_hilo(bool exp_mode, const float* X, int H, int rows, int64_t ld, const int32_t* offsets,
+                              int cols, int max_cols, void* Xh, void* Xl, float* part, float* colsum,
+                              const int32_t* status, cudaStream_t st) {
+    const int rt = (rows + 127) / 128;
+    const int64_t stride = (int64_t)H * max_cols;
+    dim3 grid((unsigned)((round_up(max_cols, 64) + 63) / 64), rt, H);
+    if (exp_mode)
+        k_split_hilo<true><<<grid, 256, 0, st>>>(X, rows, ld, offsets, cols, (__nv_bfloat16*)Xh, (__nv_bfloat16*)Xl,
+                                                 colsum ? part : nullptr, stride, status);
+    else
+        k_split_hilo<false><<<grid, 256, 0, st>>>(X, rows, ld, offsets, cols, (__nv_bfloat16*)Xh, (__nv_bfloat16*)Xl,
+                                                  colsum ? part : nullptr, stride, status);
+    if (colsum && offsets)
+        k_colsum_total<<<dim3((max_cols + 255) / 256, H), 256, 0, st>>>(part, rt, stride, offsets, colsum, status);
     return cudaGetLastError();
 }
 

@@ -23,26 +23,33 @@ cudaError_t launch_masslogits(int, int, const void*, const void*, const float*, 
                               float, float*, const int32_t*, cudaStream_t);
 cudaError_t launch_attend(int, int, const void*, int, const void*, const float*, const float*, const int32_t*, int,
                           float, float*, int32_t*, cudaStream_t);
-cudaError_t launch_gram_sym_tc(bool exp_mode, const float* A, const int32_t* offsets, int H, int n, int max_t,
-                               int64_t ld, float* C, int64_t ldc, float* colsum, int32_t* status, cudaStream_t st);
-cudaError_t launch_gram_rect_tc(int d, const float* A, const float* B, const int32_t* offsets, int H, int n,
-                                int max_t, int64_t ld, float* C, int32_t* status, cudaStream_t st);
+cudaError_t launch_gram_sym_tc(const void* Ah, const void* Al, const int32_t* offsets, int H, int n, int max_t,
+                               int64_t ld, float* C, int64_t ldc, int32_t* status, cudaStream_t st);
+cudaError_t launch_gram_rect_tc(int d, const void* Ah, const void* Al, const void* Bh, const void* Bl,
+                                const int32_t* offsets, int H, int n, int max_t, int64_t ld, float* C,
+                                int32_t* status, cudaStream_t st);
+cudaError_t launch_split_hilo(bool exp_mode, const float* X, int H, int rows, int64_t ld, const int32_t* offsets,
+                              int cols, int max_cols, void* Xh, void* Xl, float* part, float* colsum,
+                              const int32_t* status, cudaStream_t st);
 cudaError_t launch_ridge_g(float*, const float*, const int32_t*, int, int64_t, float, float*, HeadScalars*, int32_t*,
                            cudaStream_t);
 cudaError_t launch_ridge_m(int, float*, float*, const float*, const int32_t*, int, int64_t, float, HeadScalars*,
                            int32_t*, cudaStream_t);
-cudaError_t launch_xsoftmax(float*, const float*, const int32_t*, int, int, int64_t, const int32_t*, cudaStream_t);
+cudaError_t launch_xsoftmax(const float*, const float*, const int32_t*, int, int, int64_t, void*, void*,
+                            const int32_t*, cudaStream_t);
 cudaError_t launch_chol(float*, const int32_t*, int, int, int64_t, float*, int32_t*, cudaStream_t);
 int chol_launches(int max_t);
 cudaError_t launch_cholsolve(int, const float*, const float*, const float*, const int32_t*, int, int64_t, float*,
                              const int32_t*,
                              cudaStream_t);
-cudaError_t launch_nnls_all(const float* L, const float* dinv, const float* f, const int32_t* offsets, int H, int n,
-                            int max_t,
+cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* offsets, int H, int n, int max_t,
                             int64_t ldA, const float* L2, float* x, float* x0, int8_t* zflag, int32_t* zlist,
-                            int32_t* nz, float* W, float* S, int32_t* piv, float* u, float* r, float* d0,
-                            HeadScalars* hs, int zmax, int max_iter, int refine_iters, int32_t* status,
+                            int32_t* nz, float* S, int32_t* piv, float* u, float* r, float* d0, HeadScalars* hs,
+                            int zmax, int max_iter, int refine_iters, void* rpart_ws, int32_t* status,
                             cudaStream_t st, int* launches);
+cudaError_t launch_sweep_inverse(float* A, const int32_t* offsets, int H, int max_t, int64_t ldA, float* U, float* V,
+                                 float* P, int32_t* status, cudaStream_t st);
+int sweep_launches(int max_t);
 cudaError_t launch_attn_fwd_tc(int d, const void* Q, const void* K, const void* V, int H, int n, int T, float c2,
                                float* O, float* lse2, int32_t* status, cudaStream_t st);
 cudaError_t launch_colscore_tc(int d, const void* Q, const void* K, const float* lse2, int H, int n, int T,
@@ -104,7 +111,7 @@ struct StageClock {
 struct Layout {
     int64_t ldA;
     int zmax;
-    size_t O, lse2, score, L2, Vsel, Ckw, G, dinv, b, f, x, x0, d0, u, r, R, zflag, zlist, nz, piv, W, S, hs, total;
+    size_t O, lse2, score, L2, Ah, Al, Oh, Ol, bpart, Vsel, Ckw, G, dinv, swV, swP, rpart, b, f, x, x0, d0, u, r, R, zflag, zlist, nz, piv, S, hs, total;
 };
 
 static size_t carve(size_t& cur, size_t bytes) {
@@ -124,10 +131,17 @@ static Layout make_layout(const kvc_problem& p, const kvc_params& prm) {
     L.lse2 = carve(c, H * n * 4);
     L.score = carve(c, H * T * 4);
     L.L2 = carve(c, H * n * ldA * 4);
+    L.Ah = carve(c, H * n * ldA * 2);         // A' (then X) as bf16 hi / lo terms
+    L.Al = carve(c, H * n * ldA * 2);
+    L.Oh = carve(c, H * n * d * 2);           // O as bf16 hi / lo terms
+    L.Ol = carve(c, H * n * d * 2);
+    L.bpart = carve(c, ((n + 127) / 128) * H * mt * 4);   // column sums of A' per 128-query tile
     L.Vsel = carve(c, H * mt * d * 4);
     L.Ckw = carve(c, H * ldA * d * 2);
     L.G = carve(c, H * ldA * ldA * 4);
-    L.dinv = carve(c, H * ldA * 64 * 4);
+    L.dinv = carve(c, H * ldA * 64 * 4);      // Cholesky diagonal inverses; sweep U panel
+    L.swV = carve(c, H * 64 * ldA * 4);       // sweep: copy of the pivot row block
+    L.swP = carve(c, H * 64 * 64 * 4);        // sweep: pivot block inverse
     L.b = carve(c, H * mt * 4);
     L.f = carve(c, H * mt * 4);
     L.x = carve(c, H * mt * 4);
@@ -135,12 +149,12 @@ static Layout make_layout(const kvc_problem& p, const kvc_params& prm) {
     L.d0 = carve(c, H * mt * 4);
     L.u = carve(c, H * n * 4);
     L.r = carve(c, H * mt * 4);
+    L.rpart = carve(c, 8 * H * mt * 8);      // residual partial sums (8 query splits, double-float)
     L.R = carve(c, H * mt * d * 4);
     L.zflag = carve(c, H * mt);
     L.zlist = carve(c, H * zm * 4);
     L.nz = carve(c, H * 4);
     L.piv = carve(c, H * 16);
-    L.W = carve(c, H * zm * ldA * 4);
     L.S = carve(c, H * zm * zm * 4);
     L.hs = carve(c, H * sizeof(HeadScalars));
     L.total = (size_t)round_up((int64_t)c, 256);
@@ -265,7 +279,6 @@ kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* 
     int32_t* piv = (int32_t*)(ws + L.piv);
     float* x0 = (float*)(ws + L.x0);
     float* d0 = (float*)(ws + L.d0);
-    float* W = (float*)(ws + L.W);
     float* S = (float*)(ws + L.S);
     HeadScalars* hs = (HeadScalars*)(ws + L.hs);
 
@@ -298,20 +311,32 @@ kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* 
         KVC_STAGE("masslogits", 1,
                   launch_masslogits(dt, d, Q_ref, C_k, lse2, offsets, H, n, mt, L.ldA, c2, L2, head_status, st));
     }
+    KVC_STAGE("split_a", 2,
+              launch_split_hilo(true, L2, H, n, L.ldA, offsets, 0, mt, ws + L.Ah, ws + L.Al, (float*)(ws + L.bpart),
+                                b, head_status, st));
     KVC_STAGE("gram_a", 1,
-              launch_gram_sym_tc(true, L2, offsets, H, n, mt, L.ldA, G, L.ldA, b, head_status, st));
+              launch_gram_sym_tc(ws + L.Ah, ws + L.Al, offsets, H, n, mt, L.ldA, G, L.ldA, head_status, st));
     KVC_STAGE("ridge_g", 1, launch_ridge_g(G, b, offsets, H, L.ldA, q.eps_mu, f, hs, head_status, st));
-    KVC_STAGE("chol_h", chol_launches(mt), launch_chol(G, offsets, H, mt, L.ldA, dinv, head_status, st));
+    KVC_STAGE("inv_h", sweep_launches(mt),
+              launch_sweep_inverse(G, offsets, H, mt, L.ldA, dinv, (float*)(ws + L.swV), (float*)(ws + L.swP),
+                                   head_status, st));
     int nnls_launches = 0;
     KVC_STAGE("nnls", nnls_launches,
-              launch_nnls_all(G, dinv, f, offsets, H, n, mt, L.ldA, L2, x, x0, zflag, zlist, nzv, W, S, piv, u, r, d0, hs,
-                              L.zmax, q.nnls_max_iter, q.refine_iters, head_status, st, &nnls_launches));
+              launch_nnls_all(G, f, offsets, H, n, mt, L.ldA, L2, x, x0, zflag, zlist, nzv, S, piv, u, r, d0, hs,
+                              L.zmax, q.nnls_max_iter, q.refine_iters, ws + L.rpart, head_status, st,
+                              &nnls_launches));
     KVC_STAGE("beta", 1, launch_beta_out(x, offsets, H, mt, beta, head_status, st));
-    KVC_STAGE("xsoftmax", 1, launch_xsoftmax(L2, x, offsets, H, n, L.ldA, head_status, st));
+    KVC_STAGE("xsoftmax", 1,
+              launch_xsoftmax(L2, x, offsets, H, n, L.ldA, ws + L.Ah, ws + L.Al, head_status, st));
     KVC_STAGE("gram_x", 1,
-              launch_gram_sym_tc(false, L2, offsets, H, n, mt, L.ldA, G, L.ldA, nullptr, head_status, st));
-    KVC_STAGE("xto", 1, launch_gram_rect_tc(d, L2, O, offsets, H, n, mt, L.ldA, R, head_status, st));
-    KVC_STAGE("ridge_m", 1, launch_ridge_m(d, G, R, Vsel, offsets, H, L.ldA, q.eps_lambda, hs, head_status, st));
+              launch_gram_sym_tc(ws + L.Ah, ws + L.Al, offsets, H, n, mt, L.ldA, G, L.ldA, head_status, st));
+    KVC_STAGE("split_o", 1,
+              launch_split_hilo(false, O, H, n, d, nullptr, d, d, ws + L.Oh, ws + L.Ol, nullptr, nullptr,
+                                head_status, st));
+    KVC_STAGE("xto", 1,
+              launch_gram_rect_tc(d, ws + L.Ah, ws + L.Al, ws + L.Oh, ws + L.Ol, offsets, H, n, mt, L.ldA, R,
+                                  head_status, st));
+    KVC_STAGE("ridge_m", 2, launch_ridge_m(d, G, R, Vsel, offsets, H, L.ldA, q.eps_lambda, hs, head_status, st));
     KVC_STAGE("chol_m", chol_launches(mt), launch_chol(G, offsets, H, mt, L.ldA, dinv, head_status, st));
     KVC_STAGE("cholsolve", 1, launch_cholsolve(d, G, dinv, R, offsets, H, L.ldA, C_v, head_status, st));
     clk.finish();

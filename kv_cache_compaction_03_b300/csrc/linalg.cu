@@ -10,13 +10,13 @@
 //       heads still fills the GPU
 //   k_solve_cols
 //       (L L^T) x = b for many right-hand sides, one CTA per group of
-//       columns, blocked with the stored inverses of the diagonal blocks:
-//       x0 = H^{-1} f, the zero-set columns H^{-1} e_z, refinement steps and
-//       the C_v columns
+//       columns, blocked with the stored inverses of the diagonal blocks
+//       (the C_v columns)
 //   k_bpp_step
 //       one block-principal-pivoting step of min_{w>=0} 1/2 w'Hw - f'w: the
-//       free-set solution through the Schur complement (H^{-1})_ZZ, the
-//       feasibility / optimality check and the exchange of violators
+//       free-set solution through the Schur complement (H^{-1})_ZZ of the
+//       explicit inverse (sweep.cu), the feasibility / optimality check and
+//       the exchange of violators
 //   k_rowmass / k_colresid / k_refine_apply
 //       iterative refinement of w with the residual A'^T(1 - A'w) + mu(1 - w)
 //       taken from A' itself (not from the rounded Gram)
@@ -169,10 +169,14 @@ __global__ void __launch_bounds__(256) k_chol_panel(float* __restrict__ mats, co
             d = 1.f;
         }
         const float li = cb[i] / d;
+        // columns c = cq + 4m; those <= j are final.  m is static, so whole
+        // groups are skipped at compile time.  Entries above the diagonal
+        // (c > i) are never read back.
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
+            if (4 * m + 3 <= j) continue;
             const int c = cq + 4 * m;
-            if (c > j && c <= i) a[m] = fmaf(-li, cb[c], a[m]);
+            if (4 * m > j || c > j) a[m] = fmaf(-li, cb[c], a[m]);
         }
     }
 #pragma unroll
@@ -194,12 +198,16 @@ __global__ void __launch_bounds__(256) k_chol_panel(float* __restrict__ mats, co
     float x[16];
 #pragma unroll
     for (int m = 0; m < 16; ++m) x[m] = (cq + 4 * m == i) ? 1.f : 0.f;
+    // row j of X = L^{-1} has no entries right of column j, so step j only
+    // touches column groups m <= j / 4 (static after unrolling)
+#pragma unroll
     for (int j = 0; j < CB; ++j) {
         float* rbuf = colb[j & 1];
         if (i == j) {
             const float inv = 1.f / Ls[j][j];
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
+                if (4 * m > j) continue;
                 x[m] *= inv;
                 rbuf[cq + 4 * m] = x[m];
             }
@@ -208,7 +216,10 @@ __global__ void __launch_bounds__(256) k_chol_panel(float* __restrict__ mats, co
         if (i > j) {
             const float lij = Ls[i][j];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) x[m] = fmaf(-lij, rbuf[cq + 4 * m], x[m]);
+            for (int m = 0; m < 16; ++m) {
+                if (4 * m > j) continue;
+                x[m] = fmaf(-lij, rbuf[cq + 4 * m], x[m]);
+            }
         }
     }
     __syncthreads();
@@ -327,8 +338,14 @@ struct SolveArgs {
 // y_k = L_kk^{-1} (b_k - sum_{m<k} L_km y_m), then backward
 // x_k = L_kk^{-T} (y_k - sum_{m>k} L_mk^T x_m), both right-looking so every
 // block step is a dense product spread over the CTA.  The CTA keeps its
-// columns of the whole vector in shared memory.
-// grid (ceil(columns / CG), H), block 256; smem: ldA*CG + 64*65 floats.
+// columns of the whole vector in shared memory.  In the forward update the
+// L panel below the diagonal block is staged through shared memory 256 rows
+// at a time with coalesced 16-byte loads; in the backward update consecutive
+// threads read consecutive columns of L rows directly.
+// grid (ceil(columns / CG), H), block 256;
+// smem: ldA*CG + 64*65 + 256*65 floats.
+constexpr int kSolveRows = 256;
+
 template <int CG>
 __global__ void __launch_bounds__(256) k_solve_cols(SolveArgs a) {
     const int h = blockIdx.y;
@@ -344,6 +361,7 @@ __global__ void __launch_bounds__(256) k_solve_cols(SolveArgs a) {
     extern __shared__ float sm[];
     float* Y = sm;                                   // [rows][CG]
     float* Ds = sm + a.ldA * CG;                     // [64][65]
+    float* Lc = Ds + CB * (CB + 1);                  // [256][65]
     const int tid = threadIdx.x;
     const int nb = (t + CB - 1) / CB;
     const int rows = nb * CB;
@@ -359,57 +377,72 @@ __global__ void __launch_bounds__(256) k_solve_cols(SolveArgs a) {
         }
         Y[e] = v;
     }
-    // ---- forward
-    for (int k = 0; k < nb; ++k) {
-        const int k64 = k * CB;
+    // y_k <- D_k y_k (TRANS: D_k^T), D_k the stored 64 x 64 inverse
+    auto diag = [&](int k64, bool trans) {
         __syncthreads();
         for (int e = tid; e < CB * CB; e += 256) Ds[(e / CB) * (CB + 1) + e % CB] = Dh[(int64_t)k64 * CB + e];
         __syncthreads();
-        float v[CG > 4 ? CG * CB / 256 + 1 : 1];
-        int nv = 0;
-        for (int e = tid; e < CB * CG; e += 256, ++nv) {
-            const int i = e / CG, cc = e % CG;
-            float s = 0.f;
-            for (int m = 0; m <= i; ++m) s = fmaf(Ds[i * (CB + 1) + m], Y[(k64 + m) * CG + cc], s);
-            v[nv] = s;
+        constexpr int NV = (CB * CG + 255) / 256;
+        float v[NV];
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            const int e = tid + 256 * u;
+            float acc = 0.f;
+            if (e < CB * CG) {
+                const int i = e / CG, cc = e % CG;
+                if (!trans)
+                    for (int m = 0; m <= i; ++m) acc = fmaf(Ds[i * (CB + 1) + m], Y[(k64 + m) * CG + cc], acc);
+                else
+                    for (int m = i; m < CB; ++m) acc = fmaf(Ds[m * (CB + 1) + i], Y[(k64 + m) * CG + cc], acc);
+            }
+            v[u] = acc;
         }
         __syncthreads();
-        nv = 0;
-        for (int e = tid; e < CB * CG; e += 256, ++nv) Y[k64 * CG + e] = v[nv];
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            const int e = tid + 256 * u;
+            if (e < CB * CG) Y[k64 * CG + e] = v[u];
+        }
         __syncthreads();
+    };
+    // ---- forward
+    for (int k = 0; k < nb; ++k) {
+        const int k64 = k * CB;
+        diag(k64, false);
         const int kb = min(CB, t - k64);
-        for (int r = k64 + CB + tid; r < t; r += 256) {
-            const float* lr = L + (int64_t)r * a.ldA + k64;
-            float acc[CG];
-#pragma unroll
-            for (int cc = 0; cc < CG; ++cc) acc[cc] = 0.f;
-            for (int m = 0; m < kb; ++m) {
-                const float l = lr[m];
-#pragma unroll
-                for (int cc = 0; cc < CG; ++cc) acc[cc] = fmaf(l, Y[(k64 + m) * CG + cc], acc[cc]);
+        for (int r0 = k64 + CB; r0 < t; r0 += kSolveRows) {
+            const int nr = min(kSolveRows, t - r0);
+            // stage rows r0 .. r0+nr-1, columns k64 .. k64+63 of L (16 float4 per row)
+            for (int idx = tid; idx < nr * (CB / 4); idx += 256) {
+                const int rr = idx >> 4, c4 = idx & 15;
+                const float4 q = *reinterpret_cast<const float4*>(L + (int64_t)(r0 + rr) * a.ldA + k64 + 4 * c4);
+                float* dst = Lc + rr * (CB + 1) + 4 * c4;
+                dst[0] = q.x;
+                dst[1] = q.y;
+                dst[2] = q.z;
+                dst[3] = q.w;
             }
+            __syncthreads();
+            if (tid < nr) {
+                float acc[CG];
 #pragma unroll
-            for (int cc = 0; cc < CG; ++cc) Y[r * CG + cc] -= acc[cc];
+                for (int cc = 0; cc < CG; ++cc) acc[cc] = 0.f;
+                const float* lr = Lc + tid * (CB + 1);
+                for (int m = 0; m < kb; ++m) {
+                    const float l = lr[m];
+#pragma unroll
+                    for (int cc = 0; cc < CG; ++cc) acc[cc] = fmaf(l, Y[(k64 + m) * CG + cc], acc[cc]);
+                }
+#pragma unroll
+                for (int cc = 0; cc < CG; ++cc) Y[(r0 + tid) * CG + cc] -= acc[cc];
+            }
+            __syncthreads();
         }
     }
     // ---- backward
     for (int k = nb - 1; k >= 0; --k) {
         const int k64 = k * CB;
-        __syncthreads();
-        for (int e = tid; e < CB * CB; e += 256) Ds[(e / CB) * (CB + 1) + e % CB] = Dh[(int64_t)k64 * CB + e];
-        __syncthreads();
-        float v[CG > 4 ? CG * CB / 256 + 1 : 1];
-        int nv = 0;
-        for (int e = tid; e < CB * CG; e += 256, ++nv) {
-            const int i = e / CG, cc = e % CG;
-            float s = 0.f;
-            for (int m = i; m < CB; ++m) s = fmaf(Ds[m * (CB + 1) + i], Y[(k64 + m) * CG + cc], s);
-            v[nv] = s;
-        }
-        __syncthreads();
-        nv = 0;
-        for (int e = tid; e < CB * CG; e += 256, ++nv) Y[k64 * CG + e] = v[nv];
-        __syncthreads();
+        diag(k64, true);
         const int kb = min(CB, t - k64);
         for (int r = tid; r < k64; r += 256) {
             float acc[CG];
@@ -438,7 +471,7 @@ __global__ void __launch_bounds__(256) k_solve_cols(SolveArgs a) {
 // Per-head pivoting state lives in the workspace:
 //   zflag[off+i]  1 if w_i is held at zero
 //   zlist[h][k]   ascending indices of the zero set, nz[h] = |Z|
-//   W[h][k][:]    H^{-1} e_{zlist[k]} (computed by k_trsv_cols before each step)
+//   Hinv[h]       H^{-1} in full (k_sweep_*): row z is H^{-1} e_z
 //   S[h]          Cholesky factor of (H^{-1})_ZZ
 //   x0            H^{-1} f;  x  current iterate
 //   piv[h]        {done, best, budget, iterations}
@@ -448,7 +481,7 @@ struct BppArgs {
     int8_t* zflag;
     int32_t* zlist;
     int32_t* nz;
-    const float* W;
+    const float* Hinv;         // [H][ldA][ldA]
     float* S;
     int32_t* piv;              // [H][4]
     const int32_t* offsets;
@@ -498,13 +531,13 @@ __device__ int build_zlist(const int8_t* zf, int t, int* zl, int zmax, int* sbuf
 // `factor` is set.  Returns false if (H^{-1})_ZZ is not numerically SPD.
 __device__ bool schur_solution(const BppArgs& a, int h, int off, int t, int nz, const int* zl, bool factor,
                                const float* src, float* sx, float* snu, float* sm_chol, int* sflag) {
-    const float* W = a.W + (int64_t)h * a.zmax * a.ldA;
+    const float* Hi = a.Hinv + (int64_t)h * a.ldA * a.ldA;    // row z = H^{-1} e_z (symmetric)
     float* S = a.S + (int64_t)h * a.zmax * a.zmax;
     if (nz > 0) {
         if (factor) {
             for (int e = threadIdx.x; e < nz * nz; e += blockDim.x) {
                 const int r = e / nz, c = e % nz;
-                S[(int64_t)r * a.zmax + c] = W[(int64_t)c * a.ldA + zl[r]];
+                S[(int64_t)r * a.zmax + c] = Hi[(int64_t)zl[c] * a.ldA + zl[r]];
             }
             __syncthreads();
             if (!cta_chol_small(S, nz, a.zmax, sm_chol, sflag)) return false;
@@ -533,7 +566,7 @@ __device__ bool schur_solution(const BppArgs& a, int h, int off, int t, int nz, 
     }
     for (int i = threadIdx.x; i < t; i += blockDim.x) {
         float v = src[i];
-        for (int k = 0; k < nz; ++k) v = fmaf(W[(int64_t)k * a.ldA + i], snu[k], v);
+        for (int k = 0; k < nz; ++k) v = fmaf(Hi[(int64_t)zl[k] * a.ldA + i], snu[k], v);
         sx[i] = v;
     }
     __syncthreads();
@@ -688,33 +721,56 @@ __global__ void __launch_bounds__(256) k_rowmass(const float* __restrict__ L2, c
 }
 
 // r_i = sum_q A'_qi u_q + mu (1 - x_i) on the free set, 0 on the zero set.
-// grid (ceil(max_t/64), H), block 256 (4 row groups x 64 columns).
+// Pass 1 (k_colresid): grid (ceil(max_t/64), kResidSplit, H), block 256 (4 row
+// groups x 64 columns); split s sums the rows q = s, s + kResidSplit, ... in
+// double-float and writes its partial to part[s][off + c].  Pass 2
+// (k_colresid_sum) adds the partials in a fixed order, so the result does
+// not depend on scheduling.
+constexpr int kResidSplit = 8;
+
 __global__ void __launch_bounds__(256) k_colresid(const float* __restrict__ L2, const float* __restrict__ u,
-                                                  const float* __restrict__ x, const int8_t* __restrict__ zflag,
                                                   const int32_t* __restrict__ offsets, int n, int64_t ldA,
-                                                  const HeadScalars* __restrict__ hs, float* __restrict__ r,
+                                                  int64_t part_stride, dfloat* __restrict__ part,
                                                   const int32_t* __restrict__ status) {
-    const int h = blockIdx.y;
+    const int h = blockIdx.z;
     if (!head_ok(status, h)) return;
     const int off = offsets[h];
     const int t = offsets[h + 1] - off;
     const int c = blockIdx.x * 64 + (threadIdx.x & 63);
     const int rg = threadIdx.x >> 6;
+    const int sp = blockIdx.y;
     __shared__ dfloat red[4][64];
     dfloat acc{0.f, 0.f};
     if (c < t) {
         const float* col = L2 + (int64_t)h * n * ldA + c;
         const float* uh = u + (int64_t)h * n;
-        for (int q = rg; q < n; q += 4) df_fma(acc, exp2f(col[(int64_t)q * ldA]), uh[q]);
+        for (int q = sp + kResidSplit * rg; q < n; q += 4 * kResidSplit)
+            df_fma(acc, exp2f(col[(int64_t)q * ldA]), uh[q]);
     }
     red[rg][threadIdx.x & 63] = acc;
     __syncthreads();
     if (rg == 0 && c < t) {
         for (int g = 1; g < 4; ++g) df_add_df(acc, red[g][threadIdx.x]);
-        const float mu = hs[h].mu;
-        df_fma(acc, mu, 1.f - x[off + c]);
-        r[off + c] = zflag[off + c] ? 0.f : acc.hi + acc.lo;
+        part[(int64_t)sp * part_stride + off + c] = acc;
     }
+}
+
+// grid (ceil(max_t/256), H), block 256.
+__global__ void __launch_bounds__(256) k_colresid_sum(const dfloat* __restrict__ part, int64_t part_stride,
+                                                      const float* __restrict__ x, const int8_t* __restrict__ zflag,
+                                                      const int32_t* __restrict__ offsets,
+                                                      const HeadScalars* __restrict__ hs, float* __restrict__ r,
+                                                      const int32_t* __restrict__ status) {
+    const int h = blockIdx.y;
+    if (!head_ok(status, h)) return;
+    const int off = offsets[h];
+    const int t = offsets[h + 1] - off;
+    const int c = blockIdx.x * 256 + threadIdx.x;
+    if (c >= t) return;
+    dfloat acc = part[off + c];
+    for (int sp = 1; sp < kResidSplit; ++sp) df_add_df(acc, part[(int64_t)sp * part_stride + off + c]);
+    df_fma(acc, hs[h].mu, 1.f - x[off + c]);
+    r[off + c] = zflag[off + c] ? 0.f : acc.hi + acc.lo;
 }
 
 // x += H_FF^{-1} r_F: d0 = H^{-1} r is in `d0`; apply the Schur correction
@@ -776,14 +832,21 @@ int chol_launches(int max_t) {
 // Solve for every column of the mode with CG columns per CTA.
 template <int CG>
 static cudaError_t launch_solve_t(const SolveArgs& a, int ncols, int H, cudaStream_t st) {
-    const size_t smem = (size_t)(a.ldA * CG + CB * (CB + 1)) * sizeof(float);
+    const size_t smem = (size_t)(a.ldA * CG + CB * (CB + 1) + kSolveRows * (CB + 1)) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(k_solve_cols<CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     k_solve_cols<CG><<<dim3((ncols + CG - 1) / CG, H), 256, smem, st>>>(a);
     return cudaGetLastError();
 }
+// Columns per CTA: one for a single right-hand side; otherwise as many as
+// keep about two CTAs per SM busy (more columns per CTA = fewer reads of L),
+// within the shared-memory budget.
 static cudaError_t launch_solve(const SolveArgs& a, int ncols, int H, cudaStream_t st) {
     if (ncols <= 1) return launch_solve_t<1>(a, ncols, H, st);
+    const int64_t work = (int64_t)ncols * H;
+    const bool fits16 = (a.ldA * 16 + CB * (CB + 1) + kSolveRows * (CB + 1)) * 4 <= 200 * 1024;
+    if (fits16 && work >= 16 * 2 * 148) return launch_solve_t<16>(a, ncols, H, st);
+    if (work >= 8 * 2 * 148) return launch_solve_t<8>(a, ncols, H, st);
     return launch_solve_t<4>(a, ncols, H, st);
 }
 
@@ -807,54 +870,30 @@ static size_t bpp_smem(int64_t ldA, int zmax) {
            (size_t)(CB * (CB + 1) + (size_t)zmax * (CB + 1)) * sizeof(float);
 }
 
-// The whole NNLS: x0 = H^{-1} f, `max_iter` pivoting steps, refinement.
-cudaError_t launch_nnls_all(const float* L, const float* dinv, const float* f, const int32_t* offsets, int H, int n,
-                            int max_t,
+cudaError_t launch_symv(const float* Hinv, const float* v, const int32_t* offsets, int H, int max_t, int64_t ldA,
+                        float* y, const int32_t* done, int done_stride, const int32_t* status, cudaStream_t st);
+
+// The whole NNLS from the explicit inverse: x0 = H^{-1} f, `max_iter`
+// pivoting steps (each reads the zero-set rows of H^{-1}), refinement.
+cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* offsets, int H, int n, int max_t,
                             int64_t ldA, const float* L2, float* x, float* x0, int8_t* zflag, int32_t* zlist,
-                            int32_t* nz, float* W, float* S, int32_t* piv, float* u, float* r, float* d0,
-                            HeadScalars* hs, int zmax, int max_iter, int refine_iters, int32_t* status,
+                            int32_t* nz, float* S, int32_t* piv, float* u, float* r, float* d0, HeadScalars* hs,
+                            int zmax, int max_iter, int refine_iters, void* rpart_ws, int32_t* status,
                             cudaStream_t st, int* launches) {
-    BppArgs b{x0, x, zflag, zlist, nz, W, S, piv, offsets, f, ldA, zmax, hs, status};
+    dfloat* rpart = static_cast<dfloat*>(rpart_ws);
+    const int64_t part_stride = (int64_t)H * max_t;
+    BppArgs b{x0, x, zflag, zlist, nz, Hinv, S, piv, offsets, f, ldA, zmax, hs, status};
     int nl = 0;
     k_bpp_init<<<dim3((max_t + 255) / 256, H), 256, 0, st>>>(b);
-    ++nl;
-    SolveArgs sv{};
-    sv.L = L;
-    sv.dinv = dinv;
-    sv.offsets = offsets;
-    sv.ldA = ldA;
-    sv.status = status;
-    sv.mode = SOLVE_VEC;
-    sv.vin = f;
-    sv.vout = x0;
-    cudaError_t e = launch_solve(sv, 1, H, st);
+    cudaError_t e = launch_symv(Hinv, f, offsets, H, max_t, ldA, x0, nullptr, 0, status, st);
     if (e != cudaSuccess) return e;
-    ++nl;
+    nl += 2;
     const size_t smem = bpp_smem(ldA, zmax);
     e = cudaFuncSetAttribute(k_bpp_step, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_refine_apply, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    SolveArgs sz{};
-    sz.L = L;
-    sz.dinv = dinv;
-    sz.offsets = offsets;
-    sz.ldA = ldA;
-    sz.status = status;
-    sz.mode = SOLVE_UNIT_Z;
-    sz.zlist = zlist;
-    sz.nz = nz;
-    sz.W = W;
-    sz.zmax = zmax;
-    sz.done = piv;          // piv[4h] is the done flag
-    sz.done_stride = 4;
     for (int it = 0; it < max_iter; ++it) {
-        if (it > 0) {
-            // columns H^{-1} e_z for the zero set chosen by the previous step
-            e = launch_solve(sz, zmax, H, st);
-            if (e != cudaSuccess) return e;
-            ++nl;
-        }
         k_bpp_step<<<H, 512, smem, st>>>(b);
         ++nl;
     }
@@ -862,14 +901,14 @@ cudaError_t launch_nnls_all(const float* L, const float* dinv, const float* f, c
     ++nl;
     for (int it = 0; it < refine_iters; ++it) {
         k_rowmass<<<dim3((n + 7) / 8, H), 256, 0, st>>>(L2, x, offsets, n, ldA, u, status);
-        k_colresid<<<dim3((max_t + 63) / 64, H), 256, 0, st>>>(L2, u, x, zflag, offsets, n, ldA, hs, r, status);
-        SolveArgs s3 = sv;
-        s3.vin = r;
-        s3.vout = d0;
-        e = launch_solve(s3, 1, H, st);
+        k_colresid<<<dim3((max_t + 63) / 64, kResidSplit, H), 256, 0, st>>>(L2, u, offsets, n, ldA, part_stride,
+                                                                           rpart, status);
+        k_colresid_sum<<<dim3((max_t + 255) / 256, H), 256, 0, st>>>(rpart, part_stride, x, zflag, offsets, hs, r,
+                                                                    status);
+        e = launch_symv(Hinv, r, offsets, H, max_t, ldA, d0, nullptr, 0, status, st);
         if (e != cudaSuccess) return e;
         k_refine_apply<<<H, 512, smem, st>>>(b, d0);
-        nl += 4;
+        nl += 5;
     }
     if (launches) *launches = nl;
     return cudaGetLastError();

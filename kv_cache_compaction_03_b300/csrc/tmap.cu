@@ -53,4 +53,12 @@ bool make_map_f32(CUtensorMap* m, const void* base, int cols, int64_t ld, int ro
     return encode3d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, cols, ld, rows, H, 32, 32);
 }
 
+// [H][rows][ld] bf16 (first `cols` columns addressed) as a 3-D tensor: boxes
+// of [64 rows][64 columns] (128 bytes) with 128-byte swizzle, the MN-major
+// operand layout of the Gram products; reads past the addressed columns or
+// rows return 0.
+bool make_map_bf16(CUtensorMap* m, const void* base, int cols, int64_t ld, int rows, int H) {
+    return encode3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, ld, rows, H, 64, 64);
+}
+
 }  // namespace kvc
