@@ -127,6 +127,8 @@ def stage_work(w, buds):
         "xto": ("flops", 2.0 * n * d * st),
         "chol_m": ("flops", float(sum(ti ** 3 / 3.0 for ti in t))),
         "cholsolve": ("flops", float(sum(2.0 * ti * ti * d for ti in t))),
+        "inv_m": ("flops", float(sum(float(ti) ** 3 for ti in t))),
+        "apply_minv": ("flops", float(sum(2.0 * ti * ti * d for ti in t))),
     }
 
 

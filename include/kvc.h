@@ -92,6 +92,11 @@ typedef struct kvc_params {
  * kvc_compact, readable with kvc_stage_times (the events are created once per
  * host thread on first use and kept until exit). */
 #define KVC_FLAG_STAGE_TIMING 1u
+/* kvc_params.flags: solve the C_v normal equations with a blocked Cholesky
+ * factorisation and two triangular solves instead of the default explicit
+ * inverse by symmetric block sweeps (same results to rounding; the default is
+ * faster because its block steps are shorter). */
+#define KVC_FLAG_CHOLESKY_CV 2u
 
 /* Fill *prm with the defaults listed above.  Returns KVC_ERR_INVALID_ARG for a
  * null pointer. */

@@ -64,6 +64,7 @@ _lib = None
 EXPORTS = ("kvc_default_params", "kvc_workspace_size", "kvc_workspace_offset", "kvc_compact",
            "kvc_compact_noalloc", "kvc_attend", "kvc_stage_times", "kvc_status_string", "kvc_version")
 FLAG_STAGE_TIMING = 1
+FLAG_CHOLESKY_CV = 2
 
 
 def lib() -> ctypes.CDLL:

@@ -91,34 +91,41 @@ __global__ void k_ridge_m_diag(float* __restrict__ M, const int32_t* __restrict_
 
 // X_qi = softmax_i(l2_qi + log2 w_i) over i < t, written as bf16 hi / lo
 // terms (the Gram operand format, see gram_tc.cu); padding columns up to the
-// next multiple of 64 are 0.  grid (ceil(n/8), H), block 256 (one warp per row).
-__global__ void __launch_bounds__(256) k_xsoftmax(const float* __restrict__ L2, const float* __restrict__ w,
+// next multiple of 64 are 0.  log2 w_i = beta_i log2 e (beta = ln w, -inf
+// where w = 0).  grid (ceil(n/32), H), block 256: a warp per row, four rows
+// per warp; the CTA's 32 rows share one staged copy of log2 w.
+__global__ void __launch_bounds__(256) k_xsoftmax(const float* __restrict__ L2, const float* __restrict__ beta,
                                                   const int32_t* __restrict__ offsets, int n, int64_t ldA,
                                                   __nv_bfloat16* __restrict__ Xh, __nv_bfloat16* __restrict__ Xl,
                                                   const int32_t* __restrict__ status) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
+    extern __shared__ float lw[];
     const int off = offsets[h];
     const int t = offsets[h + 1] - off;
-    const int q = blockIdx.x * 8 + (threadIdx.x >> 5);
+    for (int i = threadIdx.x; i < t; i += blockDim.x) lw[i] = beta[off + i] * kLog2e;
+    __syncthreads();
     const int lane = threadIdx.x & 31;
-    if (q >= n) return;
-    const int64_t ro = ((int64_t)h * n + q) * ldA;
-    const float* row = L2 + ro;
-    float mx = -INFINITY;
-    for (int i = lane; i < t; i += 32) mx = fmaxf(mx, row[i] + log2f(w[off + i]));
-    mx = warp_max(mx);
-    float s = 0.f;
-    for (int i = lane; i < t; i += 32) s += exp2f(row[i] + log2f(w[off + i]) - mx);
-    s = warp_sum(s);
-    const float inv = (s > 0.f && mx > -INFINITY) ? 1.f / s : 0.f;
     const int tp = (int)round_up(t, GT);
-    for (int i = lane; i < tp; i += 32) {
-        float x = 0.f;
-        if (i < t && inv > 0.f) x = exp2f(row[i] + log2f(w[off + i]) - mx) * inv;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-        Xh[ro + i] = hi;
-        Xl[ro + i] = __float2bfloat16_rn(x - __bfloat162float(hi));
+    for (int rr = 0; rr < 4; ++rr) {
+        const int q = blockIdx.x * 32 + (threadIdx.x >> 5) * 4 + rr;
+        if (q >= n) break;
+        const int64_t ro = ((int64_t)h * n + q) * ldA;
+        const float* row = L2 + ro;
+        float mx = -INFINITY;
+        for (int i = lane; i < t; i += 32) mx = fmaxf(mx, row[i] + lw[i]);
+        mx = warp_max(mx);
+        float s = 0.f;
+        for (int i = lane; i < t; i += 32) s += exp2f(row[i] + lw[i] - mx);
+        s = warp_sum(s);
+        const float inv = (s > 0.f && mx > -INFINITY) ? 1.f / s : 0.f;
+        for (int i = lane; i < tp; i += 32) {
+            float x = 0.f;
+            if (i < t && inv > 0.f) x = exp2f(row[i] + lw[i] - mx) * inv;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+            Xh[ro + i] = hi;
+            Xl[ro + i] = __float2bfloat16_rn(x - __bfloat162float(hi));
+        }
     }
 }
 
@@ -139,10 +146,13 @@ cudaError_t launch_ridge_m(int d, float* M, float* R, const float* Vsel, const i
     k_ridge_m_diag<<<H, 256, 0, st>>>(M, offsets, ldA, hs, status);
     return cudaGetLastError();
 }
-cudaError_t launch_xsoftmax(const float* L2, const float* w, const int32_t* offsets, int H, int n, int64_t ldA,
+cudaError_t launch_xsoftmax(const float* L2, const float* beta, const int32_t* offsets, int H, int n, int64_t ldA,
                             void* Xh, void* Xl, const int32_t* status, cudaStream_t st) {
-    dim3 grid((n + 7) / 8, H);
-    k_xsoftmax<<<grid, 256, 0, st>>>(L2, w, offsets, n, ldA, (__nv_bfloat16*)Xh, (__nv_bfloat16*)Xl, status);
+    dim3 grid((n + 31) / 32, H);
+    const size_t smem = (size_t)ldA * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(k_xsoftmax, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_xsoftmax<<<grid, 256, smem, st>>>(L2, beta, offsets, n, ldA, (__nv_bfloat16*)Xh, (__nv_bfloat16*)Xl, status);
     return cudaGetLastError();
 }
 

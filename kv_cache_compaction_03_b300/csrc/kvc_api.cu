@@ -50,6 +50,8 @@ cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* of
 cudaError_t launch_sweep_inverse(float* A, const int32_t* offsets, int H, int max_t, int64_t ldA, float* U, float* V,
                                  float* P, int32_t* status, cudaStream_t st);
 int sweep_launches(int max_t);
+cudaError_t launch_apply_inverse(int d, const float* Minv, const float* R, const int32_t* offsets, int H, int max_t,
+                                 int64_t ldA, float* C, const int32_t* status, cudaStream_t st);
 cudaError_t launch_attn_fwd_tc(int d, const void* Q, const void* K, const void* V, int H, int n, int T, float c2,
                                float* O, float* lse2, int32_t* status, cudaStream_t st);
 cudaError_t launch_colscore_tc(int d, const void* Q, const void* K, const float* lse2, int H, int n, int T,
@@ -177,7 +179,8 @@ static kvc_status check_params(const kvc_params& q, const kvc_problem& p) {
     if (!(q.eps_mu > 0.f) || !(q.eps_lambda > 0.f) || !std::isfinite(q.eps_mu) || !std::isfinite(q.eps_lambda))
         return KVC_ERR_INVALID_ARG;
     if (q.nnls_max_iter < 1 || q.nnls_max_zero < 1 || q.refine_iters < 0) return KVC_ERR_INVALID_ARG;
-    if (q.keep_first < 0 || q.keep_last < 0 || (q.flags & ~KVC_FLAG_STAGE_TIMING) != 0) return KVC_ERR_INVALID_ARG;
+    if (q.keep_first < 0 || q.keep_last < 0 || (q.flags & ~(KVC_FLAG_STAGE_TIMING | KVC_FLAG_CHOLESKY_CV)) != 0)
+        return KVC_ERR_INVALID_ARG;
     if ((int64_t)q.keep_first + q.keep_last > p.T) return KVC_ERR_INVALID_ARG;
     return KVC_OK;
 }
@@ -327,7 +330,7 @@ kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* 
                               &nnls_launches));
     KVC_STAGE("beta", 1, launch_beta_out(x, offsets, H, mt, beta, head_status, st));
     KVC_STAGE("xsoftmax", 1,
-              launch_xsoftmax(L2, x, offsets, H, n, L.ldA, ws + L.Ah, ws + L.Al, head_status, st));
+              launch_xsoftmax(L2, beta, offsets, H, n, L.ldA, ws + L.Ah, ws + L.Al, head_status, st));
     KVC_STAGE("gram_x", 1,
               launch_gram_sym_tc(ws + L.Ah, ws + L.Al, offsets, H, n, mt, L.ldA, G, L.ldA, head_status, st));
     KVC_STAGE("split_o", 1,
@@ -337,8 +340,15 @@ kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* 
               launch_gram_rect_tc(d, ws + L.Ah, ws + L.Al, ws + L.Oh, ws + L.Ol, offsets, H, n, mt, L.ldA, R,
                                   head_status, st));
     KVC_STAGE("ridge_m", 2, launch_ridge_m(d, G, R, Vsel, offsets, H, L.ldA, q.eps_lambda, hs, head_status, st));
-    KVC_STAGE("chol_m", chol_launches(mt), launch_chol(G, offsets, H, mt, L.ldA, dinv, head_status, st));
-    KVC_STAGE("cholsolve", 1, launch_cholsolve(d, G, dinv, R, offsets, H, L.ldA, C_v, head_status, st));
+    if (q.flags & KVC_FLAG_CHOLESKY_CV) {
+        KVC_STAGE("chol_m", chol_launches(mt), launch_chol(G, offsets, H, mt, L.ldA, dinv, head_status, st));
+        KVC_STAGE("cholsolve", 1, launch_cholsolve(d, G, dinv, R, offsets, H, L.ldA, C_v, head_status, st));
+    } else {
+        KVC_STAGE("inv_m", sweep_launches(mt),
+                  launch_sweep_inverse(G, offsets, H, mt, L.ldA, dinv, (float*)(ws + L.swV), (float*)(ws + L.swP),
+                                       head_status, st));
+        KVC_STAGE("apply_minv", 1, launch_apply_inverse(d, G, R, offsets, H, mt, L.ldA, C_v, head_status, st));
+    }
     clk.finish();
     return KVC_OK;
 }

@@ -12,8 +12,9 @@
 //       (L L^T) x = b for many right-hand sides, one CTA per group of
 //       columns, blocked with the stored inverses of the diagonal blocks
 //       (the C_v columns)
-//   k_bpp_step
-//       one block-principal-pivoting step of min_{w>=0} 1/2 w'Hw - f'w: the
+//   k_bpp_solve
+//       block principal pivoting for min_{w>=0} 1/2 w'Hw - f'w, all steps of
+//       a head in one CTA; each step forms the
 //       free-set solution through the Schur complement (H^{-1})_ZZ of the
 //       explicit inverse (sweep.cu), the feasibility / optimality check and
 //       the exchange of violators
@@ -576,11 +577,11 @@ __device__ bool schur_solution(const BppArgs& a, int h, int off, int t, int nz, 
 }
 
 // grid H, block 512.  smem: 2*ldA floats + zmax floats + zmax ints + chol scratch.
-__global__ void __launch_bounds__(512) k_bpp_step(BppArgs a) {
+__device__ bool bpp_step_body(const BppArgs& a) {
     const int h = blockIdx.x;
-    if (!head_ok(a.status, h)) return;
+    if (!head_ok(a.status, h)) return true;
     int32_t* piv = a.piv + 4 * h;
-    if (piv[0]) return;                               // converged
+    if (piv[0]) return true;                          // converged
     extern __shared__ float sm[];
     const int off = a.offsets[h];
     const int t = a.offsets[h + 1] - off;
@@ -598,7 +599,7 @@ __global__ void __launch_bounds__(512) k_bpp_step(BppArgs a) {
     __syncthreads();
     if (!schur_solution(a, h, off, t, nz, zl, true, ssrc, sx, snu, sm_chol, &sflag)) {
         if (threadIdx.x == 0) set_status(a.status, h, KVC_ERR_NOT_SPD);
-        return;
+        return true;
     }
     int8_t* zf = a.zflag + off;
     // gradient on Z: y_{z_k} = nu_k
@@ -635,7 +636,7 @@ __global__ void __launch_bounds__(512) k_bpp_step(BppArgs a) {
             a.hs[h].nzero = nz;
             a.hs[h].iters = piv[3] + 1;
         }
-        return;
+        return true;
     }
     if (threadIdx.x == 0) {
         int best = piv[1], budget = piv[2];
@@ -670,11 +671,22 @@ __global__ void __launch_bounds__(512) k_bpp_step(BppArgs a) {
             set_status(a.status, h, KVC_ERR_NNLS_MAXITER);
             piv[0] = 1;
         }
-        return;
+        return true;
     }
     for (int k = threadIdx.x; k < nz2; k += blockDim.x) a.zlist[(int64_t)h * a.zmax + k] = zl[k];
     for (int i = threadIdx.x; i < t; i += blockDim.x) a.x[off + i] = zf[i] ? 0.f : fmaxf(sx[i], 0.f);
     if (threadIdx.x == 0) a.nz[h] = nz2;
+    return false;
+}
+
+// All pivoting steps of a head in one CTA: the state (zero set, iterate,
+// counters) lives in global memory between steps and is re-read after a
+// block barrier.  grid H, block 512.
+__global__ void __launch_bounds__(512) k_bpp_solve(BppArgs a, int max_iter) {
+    for (int it = 0; it < max_iter; ++it) {
+        if (bpp_step_body(a)) break;
+        __syncthreads();
+    }
 }
 
 // Reset the pivoting state (grid ceil(sum/256) x H); also zero the zero set.
@@ -889,14 +901,12 @@ cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* of
     if (e != cudaSuccess) return e;
     nl += 2;
     const size_t smem = bpp_smem(ldA, zmax);
-    e = cudaFuncSetAttribute(k_bpp_step, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(k_bpp_solve, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_refine_apply, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    for (int it = 0; it < max_iter; ++it) {
-        k_bpp_step<<<H, 512, smem, st>>>(b);
-        ++nl;
-    }
+    k_bpp_solve<<<H, 512, smem, st>>>(b, max_iter);
+    ++nl;
     k_bpp_finish<<<(H + 127) / 128, 128, 0, st>>>(b, H);
     ++nl;
     for (int it = 0; it < refine_iters; ++it) {

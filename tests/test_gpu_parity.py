@@ -64,6 +64,18 @@ def test_small_bf16_ragged(d):
     _check(w)
 
 
+def test_small_cholesky_cv_path():
+    """C_v through the blocked Cholesky and triangular solves (the
+    KVC_FLAG_CHOLESKY_CV alternative to the explicit inverse)."""
+    import kv_cache_compaction_03_b300 as kvc
+    w = small_variant(WORKLOADS[2], H=2, n=320, T=1000, t=150)
+    g, inputs = run_gpu(w, params=kvc.default_params(flags=kvc.FLAG_CHOLESKY_CV))
+    assert np.all(g["status"] == 0)
+    for h in range(w.H):
+        r, Ohat = run_oracle_head(w, inputs, h, w.t)
+        compare_head(g, h, r, Ohat, {"head": h})
+
+
 def test_config1_fp32_full():
     _check(WORKLOADS[1])
 
