@@ -115,7 +115,10 @@ __global__ void __launch_bounds__(256) k_sweep_pivot(SweepArgs s) {
                 if (tid == 0) bad = 1;
                 d = 1.f;
             }
-            const float inv = 1.f / d;
+            // reciprocal: hardware approximation plus one Newton step (~1 ulp)
+            float inv;
+            asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(d));
+            inv = inv * fmaf(-d, inv, 2.f);
             if (ii != p) {
                 // a_ic -= a_ip a_pc / d; column p itself becomes a_ip / d
                 const float f = rb[ii] * inv;
