@@ -17,3 +17,4 @@ from .am import (  # noqa: F401
     fit_values, key_scores, mass_matrix, nnls_bpp, nnls_kkt_violation,
     select_top_t,
 )
+from .chunked import compact_chunked  # noqa: F401
