@@ -62,9 +62,10 @@ typedef enum kvc_status {
 
 typedef enum kvc_dtype { KVC_DTYPE_BF16 = 0, KVC_DTYPE_F32 = 1 } kvc_dtype;
 
-/* Shape of one call.  H independent KV heads, each with n reference queries
- * (for GQA, the group's query heads stacked), T cached tokens, head dim d
- * (64 or 128).  max_t bounds every per-head budget. */
+/* Shape of one call.  H independent KV heads (1 <= H <= 65535), each with n
+ * reference queries (for GQA, the group's query heads stacked), T cached
+ * tokens, head dim d (64 or 128).  max_t bounds every per-head budget
+ * (max_t <= min(T, 4096)). */
 typedef struct kvc_problem {
     int32_t H;
     int32_t n;
@@ -115,6 +116,8 @@ kvc_status kvc_workspace_size(const kvc_problem* p, const kvc_params* prm, size_
  *   3 W      fp32 [sum t]     NNLS weights w = exp(beta), offsets-indexed
  *   4 HEAD   32-byte records per head (ridges mu, lambda; NNLS zero-set
  *            size and iterations)
+ * prm->keep_first / keep_last are not checked against p->T here (the layout
+ * does not depend on them).
  * Host-only.  Errors: INVALID_ARG (bad problem/params or unknown item). */
 kvc_status kvc_workspace_offset(const kvc_problem* p, const kvc_params* prm, int32_t item, size_t* offset);
 
@@ -183,6 +186,51 @@ kvc_status kvc_compact_noalloc(const kvc_problem* p, const kvc_params* prm,
                                const int32_t* budgets, const int32_t* offsets,
                                int32_t* idx_out, void* C_k, float* beta, float* C_v,
                                int32_t* head_status, kvc_stream_t stream);
+
+/* Chunked compaction (page section 2, "Compaction par blocs": the full
+ * context is prefilled, its KV cache is cut into contiguous chunks, each
+ * chunk is compacted on its own, and the compacted chunks are concatenated).
+ *
+ * *p describes the whole cache: H KV heads of T positions, n reference
+ * queries per head, max_t bounding every per-chunk budget.  Each head's cache
+ * is split into `chunks` equal chunks of Tc = T / chunks positions (T must be
+ * a multiple of chunks; max_t <= Tc).  Chunk c of head h is compacted exactly
+ * as kvc_compact compacts one head of Tc positions, against all n reference
+ * queries of head h.  Chunks are indexed g = h * chunks + c throughout.
+ *
+ * Arguments (device unless stated):
+ *   p, prm     host; whole-cache shape, parameters (prm NULL -> defaults);
+ *              H * chunks <= 65535
+ *   chunks     host; number of chunks per head, >= 1 (1 = kvc_compact)
+ *   Q_ref      [H][n][d] dtype       K, V  [H][T][d] dtype   (16B aligned)
+ *   budgets    int32 [H*chunks]: t_g, 1 <= t_g <= min(Tc, max_t)
+ *   offsets    int32 [H*chunks+1]: exclusive prefix sum of budgets.  The rows
+ *              of head h's merged compact cache are [offsets[h*chunks],
+ *              offsets[(h+1)*chunks]), chunk by chunk; that range is what
+ *              kvc_attend reads with per-head offsets offsets[h*chunks].
+ *   idx_out    int32 [sum t]: kept positions in the WHOLE cache (c*Tc plus
+ *              the position inside chunk c), ascending within a chunk and so
+ *              within a head
+ *   C_k, beta, C_v   as in kvc_compact, per chunk
+ *   head_status int32 [H*chunks]: per-chunk outcomes as in kvc_compact
+ *   workspace  at least kvc_workspace_size_chunked bytes, 256B aligned
+ * prm->keep_first / keep_last count positions of the whole cache: chunk c
+ * keeps the part of [0, keep_first) and of [T - keep_last, T) inside it.
+ * Errors: INVALID_ARG (also T not a multiple of chunks, max_t > Tc, too many
+ * chunks), ALIGN, WORKSPACE, CUDA (nothing enqueued on the first three).
+ * Workspace offsets (kvc_workspace_offset) are those of the per-chunk problem
+ * {H*chunks, n, Tc, d, dtype, max_t}, whose intermediates are per chunk. */
+kvc_status kvc_compact_chunked(const kvc_problem* p, const kvc_params* prm, int32_t chunks,
+                               const void* Q_ref, const void* K, const void* V,
+                               const int32_t* budgets, const int32_t* offsets,
+                               int32_t* idx_out, void* C_k, float* beta, float* C_v,
+                               int32_t* head_status,
+                               void* workspace, size_t workspace_bytes, kvc_stream_t stream);
+
+/* Bytes of workspace kvc_compact_chunked needs for *p cut into `chunks`
+ * chunks per head (that of the per-chunk problem).  Host-only.
+ * Errors: INVALID_ARG. */
+kvc_status kvc_workspace_size_chunked(const kvc_problem* p, const kvc_params* prm, int32_t chunks, size_t* bytes);
 
 /* Read a compacted cache with a per-key bias (page section 2 objective, and
  * section 5 on use with standard attention kernels):

@@ -62,7 +62,8 @@ class KvcError(RuntimeError):
 
 _lib = None
 EXPORTS = ("kvc_default_params", "kvc_workspace_size", "kvc_workspace_offset", "kvc_compact",
-           "kvc_compact_noalloc", "kvc_attend", "kvc_stage_times", "kvc_status_string", "kvc_version")
+           "kvc_compact_noalloc", "kvc_compact_chunked", "kvc_workspace_size_chunked", "kvc_attend",
+           "kvc_stage_times", "kvc_status_string", "kvc_version")
 FLAG_STAGE_TIMING = 1
 FLAG_CHOLESKY_CV = 2
 
@@ -82,6 +83,8 @@ def lib() -> ctypes.CDLL:
     L.kvc_workspace_offset.argtypes = [P, PP, i32, ctypes.POINTER(sz)]
     L.kvc_compact.argtypes = [P, PP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.kvc_compact_noalloc.argtypes = [P, PP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.kvc_compact_chunked.argtypes = [P, PP, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.kvc_workspace_size_chunked.argtypes = [P, PP, i32, ctypes.POINTER(sz)]
     L.kvc_attend.argtypes = [P, vp, i32, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp]
     L.kvc_stage_times.argtypes = [ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_float),
                                   ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i32), ctypes.POINTER(i32), i32]
@@ -90,7 +93,7 @@ def lib() -> ctypes.CDLL:
     L.kvc_status_string.restype = ctypes.c_char_p
     L.kvc_version.restype = ctypes.c_char_p
     for f in ("kvc_default_params", "kvc_workspace_size", "kvc_workspace_offset", "kvc_compact",
-              "kvc_compact_noalloc", "kvc_attend"):
+              "kvc_compact_noalloc", "kvc_compact_chunked", "kvc_workspace_size_chunked", "kvc_attend"):
         getattr(L, f).restype = ctypes.c_int
     _lib = L
     return L
@@ -123,6 +126,15 @@ def workspace_size(problem: Problem, params: Params | None = None) -> int:
     rc = lib().kvc_workspace_size(ctypes.byref(problem), ctypes.byref(params) if params else None, ctypes.byref(out))
     if rc:
         raise KvcError(rc, "kvc_workspace_size")
+    return out.value
+
+
+def workspace_size_chunked(problem: Problem, params: Params | None, chunks: int) -> int:
+    out = ctypes.c_size_t()
+    rc = lib().kvc_workspace_size_chunked(ctypes.byref(problem), ctypes.byref(params) if params else None,
+                                          int(chunks), ctypes.byref(out))
+    if rc:
+        raise KvcError(rc, "kvc_workspace_size_chunked")
     return out.value
 
 
@@ -172,6 +184,17 @@ def compact_noalloc(problem: Problem, params: Params | None, Q_ref, K, V, budget
                                      _ptr(C_k), _ptr(beta), _ptr(C_v), _ptr(head_status), _stream(stream))
 
 
+def compact_chunked(problem: Problem, params: Params | None, chunks: int, Q_ref, K, V, budgets, offsets, idx_out,
+                    C_k, beta, C_v, head_status, workspace, workspace_bytes: int, stream=None) -> int:
+    """kvc_compact_chunked: every head's cache cut into `chunks` contiguous
+    chunks, each compacted against the head's reference queries.  Returns the
+    call-level status (0 = enqueued)."""
+    return lib().kvc_compact_chunked(ctypes.byref(problem), ctypes.byref(params) if params else None, int(chunks),
+                                     _ptr(Q_ref), _ptr(K), _ptr(V), _ptr(budgets), _ptr(offsets), _ptr(idx_out),
+                                     _ptr(C_k), _ptr(beta), _ptr(C_v), _ptr(head_status), _ptr(workspace),
+                                     int(workspace_bytes), _stream(stream))
+
+
 def attend(problem: Problem, Q, n_q: int, C_k, beta, C_v, offsets, O_out, head_status, scale: float = 0.0,
            stream=None) -> int:
     """kvc_attend on caller-owned buffers.  Returns the call-level status."""
@@ -196,7 +219,10 @@ def stage_times(cap: int = 32):
 # ------------------------------------------------------------------ helpers
 @dataclass
 class Compacted:
-    """Outputs of one kvc_compact call (device tensors)."""
+    """Outputs of one kvc_compact or kvc_compact_chunked call (device
+    tensors).  For a chunked call, offsets / head_status are per chunk,
+    `problem` is the per-chunk problem (its workspace layout) and head h's
+    merged cache is rows [offsets[h*chunks], offsets[(h+1)*chunks])."""
     idx: object
     C_k: object
     beta: object
@@ -206,6 +232,11 @@ class Compacted:
     workspace: object
     problem: Problem
     params: Params
+    chunks: int = 1
+
+    def head_offsets(self):
+        """int32 [H+1]: each head's row range in the (merged) compact cache."""
+        return self.offsets if self.chunks == 1 else self.offsets[::self.chunks].contiguous()
 
 
 def torch_dtype_code(dt) -> int:
@@ -247,6 +278,39 @@ def compact_tensors(Q_ref, K, V, budgets, params: Params | None = None, stream=N
     return Compacted(idx, Ck, beta, Cv, offsets, status, ws, prob, prm)
 
 
+def compact_chunked_tensors(Q_ref, K, V, budgets, params: Params | None = None, stream=None) -> Compacted:
+    """Allocate outputs and workspace with torch, then call kvc_compact_chunked.
+
+    Q_ref [H][n][d], K/V [H][T][d]; budgets int32 [H][chunks] on the device
+    (the chunk count is its second dimension; T must be a multiple of it).
+    """
+    import torch
+    H, n, d = Q_ref.shape
+    T = K.shape[1]
+    C = budgets.shape[1]
+    dev = Q_ref.device
+    flat = budgets.reshape(-1).contiguous()
+    b64 = flat.to(torch.int64)
+    offsets = torch.zeros(H * C + 1, dtype=torch.int32, device=dev)
+    offsets[1:] = torch.cumsum(b64, 0).to(torch.int32)
+    total = int(offsets[-1].item())
+    max_t = int(b64.max().item())
+    prob = make_problem(H, n, T, d, torch_dtype_code(Q_ref.dtype), max_t)
+    prm = params if params is not None else default_params()
+    ws_bytes = workspace_size_chunked(prob, prm, C)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    idx = torch.empty(total, dtype=torch.int32, device=dev)
+    Ck = torch.empty(total, d, dtype=Q_ref.dtype, device=dev)
+    beta = torch.empty(total, dtype=torch.float32, device=dev)
+    Cv = torch.empty(total, d, dtype=torch.float32, device=dev)
+    status = torch.empty(H * C, dtype=torch.int32, device=dev)
+    rc = compact_chunked(prob, prm, C, Q_ref, K, V, flat, offsets, idx, Ck, beta, Cv, status, ws, ws_bytes, stream)
+    if rc:
+        raise KvcError(rc, "kvc_compact_chunked")
+    chunk_prob = make_problem(H * C, n, T // C, d, prob.dtype, max_t)
+    return Compacted(idx, Ck, beta, Cv, offsets, status, ws, chunk_prob, prm, C)
+
+
 def workspace_view(c: Compacted, item: int, count: int, dtype):
     """A typed view of an intermediate inside a finished call's workspace."""
     import torch
@@ -256,13 +320,14 @@ def workspace_view(c: Compacted, item: int, count: int, dtype):
 
 
 def attend_tensors(Q, c: Compacted, scale: float = 0.0, stream=None):
-    """softmax(Q C_k^T * scale + beta) C_v per head; returns (O [H][n_q][d] fp32, status)."""
+    """softmax(Q C_k^T * scale + beta) C_v per head (over the merged cache of a
+    chunked call); returns (O [H][n_q][d] fp32, status)."""
     import torch
     H, nq, d = Q.shape
     O = torch.empty(H, nq, d, dtype=torch.float32, device=Q.device)
     st = torch.empty(H, dtype=torch.int32, device=Q.device)
     prob = make_problem(H, nq, 1, d, torch_dtype_code(Q.dtype), 1)
-    rc = attend(prob, Q, nq, c.C_k, c.beta, c.C_v, c.offsets, O, st, scale, stream)
+    rc = attend(prob, Q, nq, c.C_k, c.beta, c.C_v, c.head_offsets(), O, st, scale, stream)
     if rc:
         raise KvcError(rc, "kvc_attend")
     return O, st

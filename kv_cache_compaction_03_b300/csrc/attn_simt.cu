@@ -69,7 +69,7 @@ template <typename TIn, int D>
 __global__ void __launch_bounds__(NT) k_attn_fwd(const TIn* __restrict__ Q, const TIn* __restrict__ K,
                                                  const TIn* __restrict__ V, int n, int T, float c2,
                                                  float* __restrict__ O, float* __restrict__ lse2,
-                                                 const int32_t* __restrict__ status) {
+                                                 const int32_t* __restrict__ status, int qdiv) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     extern __shared__ float sm[];
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(NT) k_attn_fwd(const TIn* __restrict__ Q, cons
     float* Ps = Vs + BN * D;          // [BM][BN+1]
     const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
     const int q0 = blockIdx.x * BM;
-    const TIn* Qh = Q + ((int64_t)h * n + q0) * D;
+    const TIn* Qh = Q + ((int64_t)(h / qdiv) * n + q0) * D;
     const TIn* Kh = K + (int64_t)h * T * D;
     const TIn* Vh = V + (int64_t)h * T * D;
     load_tile<TIn, D>(Qs, Qh, min(BM, n - q0), D);
@@ -160,7 +160,8 @@ __global__ void __launch_bounds__(NT) k_attn_fwd(const TIn* __restrict__ Q, cons
 template <typename TIn, int D>
 __global__ void __launch_bounds__(NT) k_colscore(const TIn* __restrict__ Q, const TIn* __restrict__ K,
                                                  const float* __restrict__ lse2, int n, int T, float c2,
-                                                 float* __restrict__ score, const int32_t* __restrict__ status) {
+                                                 float* __restrict__ score, const int32_t* __restrict__ status,
+                                                 int qdiv) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     extern __shared__ float sm[];
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(NT) k_colscore(const TIn* __restrict__ Q, cons
     for (int q0 = 0; q0 < n; q0 += BM) {
         const int qv = min(BM, n - q0);
         __syncthreads();
-        load_tile<TIn, D>(Qs, Q + ((int64_t)h * n + q0) * D, qv, D);
+        load_tile<TIn, D>(Qs, Q + ((int64_t)(h / qdiv) * n + q0) * D, qv, D);
         for (int e = threadIdx.x; e < BM; e += NT) Ls[e] = (e < qv) ? lse2[(int64_t)h * n + q0 + e] : INFINITY;
         __syncthreads();
         float s[4][4];
@@ -214,7 +215,7 @@ template <typename TIn, int D>
 __global__ void __launch_bounds__(NT) k_masslogits(const TIn* __restrict__ Q, const TIn* __restrict__ Ck,
                                                    const float* __restrict__ lse2, const int32_t* __restrict__ offsets,
                                                    int n, int64_t ldA, float c2, float* __restrict__ L2,
-                                                   const int32_t* __restrict__ status) {
+                                                   const int32_t* __restrict__ status, int qdiv) {
     const int h = blockIdx.z;
     if (!head_ok(status, h)) return;
     const int off = offsets[h];
@@ -228,7 +229,7 @@ __global__ void __launch_bounds__(NT) k_masslogits(const TIn* __restrict__ Q, co
     const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
     const int q0 = blockIdx.y * BM;
     const int qv = min(BM, n - q0);
-    load_tile<TIn, D>(Qs, Q + ((int64_t)h * n + q0) * D, qv, D);
+    load_tile<TIn, D>(Qs, Q + ((int64_t)(h / qdiv) * n + q0) * D, qv, D);
     load_tile<TIn, D>(Cs, Ck + ((int64_t)off + i0) * D, min(BN, th - i0), D);
     __syncthreads();
     float s[4][4];
@@ -350,39 +351,39 @@ __global__ void __launch_bounds__(NT) k_attend(const TIn* __restrict__ Q, int nq
 // ---------------------------------------------------------------- launchers
 template <typename TIn, int D>
 static cudaError_t launch_attn_simt_t(const void* Q, const void* K, const void* V, int H, int n, int T, float c2,
-                                      float* O, float* lse2, const int32_t* status, cudaStream_t st) {
+                                      float* O, float* lse2, const int32_t* status, int qdiv, cudaStream_t st) {
     constexpr int P = D + 1;
     size_t smem = (size_t)(BM * P + BN * P + BN * D + BM * (BN + 1)) * sizeof(float);
     auto kern = k_attn_fwd<TIn, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((n + BM - 1) / BM, H);
-    kern<<<grid, NT, smem, st>>>((const TIn*)Q, (const TIn*)K, (const TIn*)V, n, T, c2, O, lse2, status);
+    kern<<<grid, NT, smem, st>>>((const TIn*)Q, (const TIn*)K, (const TIn*)V, n, T, c2, O, lse2, status, qdiv);
     return cudaGetLastError();
 }
 template <typename TIn, int D>
 static cudaError_t launch_colscore_simt_t(const void* Q, const void* K, const float* lse2, int H, int n, int T,
-                                          float c2, float* score, const int32_t* status, cudaStream_t st) {
+                                          float c2, float* score, const int32_t* status, int qdiv, cudaStream_t st) {
     constexpr int P = D + 1;
     size_t smem = (size_t)(BN * P + BM * P + BM) * sizeof(float) + 16 * BN * sizeof(double) + 8;
     auto kern = k_colscore<TIn, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((T + BN - 1) / BN, H);
-    kern<<<grid, NT, smem, st>>>((const TIn*)Q, (const TIn*)K, lse2, n, T, c2, score, status);
+    kern<<<grid, NT, smem, st>>>((const TIn*)Q, (const TIn*)K, lse2, n, T, c2, score, status, qdiv);
     return cudaGetLastError();
 }
 template <typename TIn, int D>
 static cudaError_t launch_masslogits_t(const void* Q, const void* Ck, const float* lse2, const int32_t* offsets,
                                        int H, int n, int max_t, int64_t ldA, float c2, float* L2,
-                                       const int32_t* status, cudaStream_t st) {
+                                       const int32_t* status, int qdiv, cudaStream_t st) {
     constexpr int P = D + 1;
     size_t smem = (size_t)(BM * P + BN * P) * sizeof(float);
     auto kern = k_masslogits<TIn, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((max_t + BN - 1) / BN, (n + BM - 1) / BM, H);
-    kern<<<grid, NT, smem, st>>>((const TIn*)Q, (const TIn*)Ck, lse2, offsets, n, ldA, c2, L2, status);
+    kern<<<grid, NT, smem, st>>>((const TIn*)Q, (const TIn*)Ck, lse2, offsets, n, ldA, c2, L2, status, qdiv);
     return cudaGetLastError();
 }
 template <typename TIn, int D>
@@ -405,17 +406,18 @@ static cudaError_t launch_attend_t(const void* Q, int nq, const void* Ck, const 
          : ((d) == 128 ? FN<float, 128>(__VA_ARGS__) : FN<float, 64>(__VA_ARGS__)))
 
 cudaError_t launch_attn_fwd_simt(int dtype, int d, const void* Q, const void* K, const void* V, int H, int n, int T,
-                                 float c2, float* O, float* lse2, const int32_t* status, cudaStream_t st) {
-    return KVC_DISPATCH(dtype, d, launch_attn_simt_t, Q, K, V, H, n, T, c2, O, lse2, status, st);
+                                 float c2, float* O, float* lse2, const int32_t* status, int qdiv, cudaStream_t st) {
+    return KVC_DISPATCH(dtype, d, launch_attn_simt_t, Q, K, V, H, n, T, c2, O, lse2, status, qdiv, st);
 }
 cudaError_t launch_colscore_simt(int dtype, int d, const void* Q, const void* K, const float* lse2, int H, int n,
-                                 int T, float c2, float* score, const int32_t* status, cudaStream_t st) {
-    return KVC_DISPATCH(dtype, d, launch_colscore_simt_t, Q, K, lse2, H, n, T, c2, score, status, st);
+                                 int T, float c2, float* score, const int32_t* status, int qdiv, cudaStream_t st) {
+    return KVC_DISPATCH(dtype, d, launch_colscore_simt_t, Q, K, lse2, H, n, T, c2, score, status, qdiv, st);
 }
 cudaError_t launch_masslogits(int dtype, int d, const void* Q, const void* Ck, const float* lse2,
                               const int32_t* offsets, int H, int n, int max_t, int64_t ldA, float c2, float* L2,
-                              const int32_t* status, cudaStream_t st) {
-    return KVC_DISPATCH(dtype, d, launch_masslogits_t, Q, Ck, lse2, offsets, H, n, max_t, ldA, c2, L2, status, st);
+                              const int32_t* status, int qdiv, cudaStream_t st) {
+    return KVC_DISPATCH(dtype, d, launch_masslogits_t, Q, Ck, lse2, offsets, H, n, max_t, ldA, c2, L2, status, qdiv,
+                        st);
 }
 cudaError_t launch_attend(int dtype, int d, const void* Q, int nq, const void* Ck, const float* beta,
                           const float* Cv, const int32_t* offsets, int H, float c2, float* O, int32_t* status,

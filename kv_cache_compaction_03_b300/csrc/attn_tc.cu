@@ -16,6 +16,9 @@
 //                   attention score of each key (key selection aggregated
 //                   by RMS).
 //
+// Q heads: head h reads reference queries of head h / qdiv (qdiv > 1 when
+// several chunks of one cache share its queries).
+//
 // bf16 inputs, fp32 accumulation.  One CTA = 10 warps and two 128-row
 // tiles (query tiles for the forward pass, key tiles for the scores):
 //   warp 0       TMA producer (one elected thread)
@@ -82,7 +85,7 @@ template <int D, int NS>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     k_attn_fwd_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                   const __grid_constant__ CUtensorMap mV, int n, int T, float c2, float* __restrict__ O,
-                  float* __restrict__ lse2, int32_t* __restrict__ status) {
+                  float* __restrict__ lse2, int32_t* __restrict__ status, int qdiv) {
     using L = FwdLayout<D, NS>;
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_expect_tx(q_full, 2 * kTileBytes);
             for (int g = 0; g < 2; ++g)
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_3d(sm + L::kQ + g * L::kTile + c * kBox, &mQ, q_full, c * 64, q0 + g * TB, h);
+                    tma_load_3d(sm + L::kQ + g * L::kTile + c * kBox, &mQ, q_full, c * 64, q0 + g * TB, h / qdiv);
             int issued = 0;
             for (int j = 0; j < nt; ++j) {
                 const int s = j % NS;
@@ -347,7 +350,7 @@ template <int D, int NS>
 __global__ void __launch_bounds__(kColThreads, 1)
     k_colscore_tc(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
                   const float* __restrict__ lse2, int n, int T, float c2, float* __restrict__ score,
-                  int32_t* __restrict__ status) {
+                  int32_t* __restrict__ status, int qdiv) {
     using L = ColLayout<D, NS>;
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
@@ -402,7 +405,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
                 if (i >= NS && !mbar_wait(q_empty + s, (uint32_t)((i / NS) - 1) & 1u, abort_flag)) break;
                 mbar_expect_tx(q_full + s, kTileBytes);
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_3d(sm + L::kQ + s * L::kTile + c * kBox, &mQ, q_full + s, c * 64, i * TB, h);
+                    tma_load_3d(sm + L::kQ + s * L::kTile + c * kBox, &mQ, q_full + s, c * 64, i * TB, h / qdiv);
                 issued = i + 1;
             }
             drain_wait(k_full, 0);
@@ -524,7 +527,7 @@ template <int D>
 __global__ void __launch_bounds__(kMassThreads, 1)
     k_masslogits_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mC,
                     const float* __restrict__ lse2, const int32_t* __restrict__ offsets, int n, int64_t ldA,
-                    float c2, float* __restrict__ L2, int32_t* __restrict__ status) {
+                    float c2, float* __restrict__ L2, int32_t* __restrict__ status, int qdiv) {
     using L = MassLayout<D>;
     const int h = blockIdx.z;
     if (!head_ok(status, h)) return;
@@ -557,7 +560,7 @@ __global__ void __launch_bounds__(kMassThreads, 1)
         if (lane == 0) {
             mbar_expect_tx(full, 2u * L::kTile);
             for (int c = 0; c < D / 64; ++c) {
-                tma_load_3d(sm + L::kQ + c * kBox, &mQ, full, c * 64, q0, h);
+                tma_load_3d(sm + L::kQ + c * kBox, &mQ, full, c * 64, q0, h / qdiv);
                 tma_load_3d(sm + L::kC + c * kBox, &mC, full, c * 64, i0, h);
             }
             drain_wait(full, 0);
@@ -616,67 +619,66 @@ __global__ void __launch_bounds__(kMassThreads, 1)
 // ------------------------------------------------------------ host side
 template <int D, int NS>
 cudaError_t launch_fwd_t(const void* Q, const void* K, const void* V, int H, int n, int T, float c2, float* O,
-                         float* lse2, int32_t* status, cudaStream_t st) {
+                         float* lse2, int32_t* status, int qdiv, cudaStream_t st) {
     CUtensorMap mQ, mK, mV;
-    if (!make_map(&mQ, Q, D, n, H) || !make_map(&mK, K, D, T, H) || !make_map(&mV, V, D, T, H))
+    if (!make_map(&mQ, Q, D, n, H / qdiv) || !make_map(&mK, K, D, T, H) || !make_map(&mV, V, D, T, H))
         return cudaErrorInvalidValue;
     constexpr int smem = FwdLayout<D, NS>::kBytes;
     auto kern = k_attn_fwd_tc<D, NS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((n + 2 * TB - 1) / (2 * TB), H);
-    kern<<<grid, kFwdThreads, smem, st>>>(mQ, mK, mV, n, T, c2, O, lse2, status);
+    kern<<<grid, kFwdThreads, smem, st>>>(mQ, mK, mV, n, T, c2, O, lse2, status, qdiv);
     return cudaGetLastError();
 }
 
 template <int D, int NS>
 cudaError_t launch_col_t(const void* Q, const void* K, const float* lse2, int H, int n, int T, float c2,
-                         float* score, int32_t* status, cudaStream_t st) {
+                         float* score, int32_t* status, int qdiv, cudaStream_t st) {
     CUtensorMap mK, mQ;
-    if (!make_map(&mK, K, D, T, H) || !make_map(&mQ, Q, D, n, H)) return cudaErrorInvalidValue;
+    if (!make_map(&mK, K, D, T, H) || !make_map(&mQ, Q, D, n, H / qdiv)) return cudaErrorInvalidValue;
     constexpr int smem = ColLayout<D, NS>::kBytes;
     auto kern = k_colscore_tc<D, NS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((T + 2 * TB - 1) / (2 * TB), H);
-    kern<<<grid, kColThreads, smem, st>>>(mK, mQ, lse2, n, T, c2, score, status);
+    kern<<<grid, kColThreads, smem, st>>>(mK, mQ, lse2, n, T, c2, score, status, qdiv);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_mass_t(const void* Q, const void* Ck, const float* lse2, const int32_t* offsets, int H, int n,
-                          int max_t, int64_t ldA, float c2, float* L2, int32_t* status, cudaStream_t st) {
+                          int max_t, int64_t ldA, float c2, float* L2, int32_t* status, int qdiv, cudaStream_t st) {
     CUtensorMap mQ, mC;
-    if (!make_map(&mQ, Q, D, n, H) || !make_map(&mC, Ck, D, (int)ldA, H)) return cudaErrorInvalidValue;
+    if (!make_map(&mQ, Q, D, n, H / qdiv) || !make_map(&mC, Ck, D, (int)ldA, H)) return cudaErrorInvalidValue;
     constexpr int smem = MassLayout<D>::kBytes;
     auto kern = k_masslogits_tc<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((max_t + TB - 1) / TB, (n + TB - 1) / TB, H);
-    kern<<<grid, kMassThreads, smem, st>>>(mQ, mC, lse2, offsets, n, ldA, c2, L2, status);
+    kern<<<grid, kMassThreads, smem, st>>>(mQ, mC, lse2, offsets, n, ldA, c2, L2, status, qdiv);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_masslogits_tc(int d, const void* Q, const void* Ck, const float* lse2, const int32_t* offsets,
-                                 int H, int n, int max_t, int sum_t, int64_t ldA, float c2, float* L2,
-                                 int32_t* status, cudaStream_t st) {
-    (void)sum_t;
-    return d == 128 ? launch_mass_t<128>(Q, Ck, lse2, offsets, H, n, max_t, ldA, c2, L2, status, st)
-                    : launch_mass_t<64>(Q, Ck, lse2, offsets, H, n, max_t, ldA, c2, L2, status, st);
+                                 int H, int n, int max_t, int64_t ldA, float c2, float* L2, int32_t* status,
+                                 int qdiv, cudaStream_t st) {
+    return d == 128 ? launch_mass_t<128>(Q, Ck, lse2, offsets, H, n, max_t, ldA, c2, L2, status, qdiv, st)
+                    : launch_mass_t<64>(Q, Ck, lse2, offsets, H, n, max_t, ldA, c2, L2, status, qdiv, st);
 }
 
 cudaError_t launch_attn_fwd_tc(int d, const void* Q, const void* K, const void* V, int H, int n, int T, float c2,
-                               float* O, float* lse2, int32_t* status, cudaStream_t st) {
-    return d == 128 ? launch_fwd_t<128, 2>(Q, K, V, H, n, T, c2, O, lse2, status, st)
-                    : launch_fwd_t<64, 3>(Q, K, V, H, n, T, c2, O, lse2, status, st);
+                               float* O, float* lse2, int32_t* status, int qdiv, cudaStream_t st) {
+    return d == 128 ? launch_fwd_t<128, 2>(Q, K, V, H, n, T, c2, O, lse2, status, qdiv, st)
+                    : launch_fwd_t<64, 3>(Q, K, V, H, n, T, c2, O, lse2, status, qdiv, st);
 }
 
 cudaError_t launch_colscore_tc(int d, const void* Q, const void* K, const float* lse2, int H, int n, int T,
-                               float c2, float* score, int32_t* status, cudaStream_t st) {
-    return d == 128 ? launch_col_t<128, 3>(Q, K, lse2, H, n, T, c2, score, status, st)
-                    : launch_col_t<64, 6>(Q, K, lse2, H, n, T, c2, score, status, st);
+                               float c2, float* score, int32_t* status, int qdiv, cudaStream_t st) {
+    return d == 128 ? launch_col_t<128, 3>(Q, K, lse2, H, n, T, c2, score, status, qdiv, st)
+                    : launch_col_t<64, 6>(Q, K, lse2, H, n, T, c2, score, status, qdiv, st);
 }
 
 }  // namespace kvc

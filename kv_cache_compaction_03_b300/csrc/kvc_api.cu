@@ -8,19 +8,21 @@
 #include "common.cuh"
 
 namespace kvc {
-cudaError_t launch_validate(const int32_t*, const int32_t*, int, int, int, int, int32_t*, HeadScalars*, cudaStream_t);
+cudaError_t launch_validate(const int32_t*, const int32_t*, int, int, int, int, int, int, int32_t*, HeadScalars*,
+                            cudaStream_t);
 cudaError_t launch_attn_fwd_simt(int, int, const void*, const void*, const void*, int, int, int, float, float*, float*,
-                                 const int32_t*, cudaStream_t);
+                                 const int32_t*, int, cudaStream_t);
 cudaError_t launch_colscore_simt(int, int, const void*, const void*, const float*, int, int, int, float, float*,
-                                 const int32_t*, cudaStream_t);
-cudaError_t launch_select(const float*, int, int, const int32_t*, int, int, int32_t*, int32_t*, cudaStream_t);
+                                 const int32_t*, int, cudaStream_t);
+cudaError_t launch_select(const float*, int, int, const int32_t*, int, int, int, int32_t*, int32_t*, cudaStream_t);
+cudaError_t launch_shift_idx(int32_t*, const int32_t*, int, int, int, int, const int32_t*, cudaStream_t);
 cudaError_t launch_gather(int, int, const void*, const void*, int, int, int, const int32_t*, const int32_t*, void*,
                           float*, void*, int64_t, const int32_t*, cudaStream_t);
 cudaError_t launch_masslogits_tc(int d, const void* Q, const void* Ck, const float* lse2, const int32_t* offsets,
-                                 int H, int n, int max_t, int sum_t, int64_t ldA, float c2, float* L2,
-                                 int32_t* status, cudaStream_t st);
+                                 int H, int n, int max_t, int64_t ldA, float c2, float* L2, int32_t* status,
+                                 int qdiv, cudaStream_t st);
 cudaError_t launch_masslogits(int, int, const void*, const void*, const float*, const int32_t*, int, int, int, int64_t,
-                              float, float*, const int32_t*, cudaStream_t);
+                              float, float*, const int32_t*, int, cudaStream_t);
 cudaError_t launch_attend(int, int, const void*, int, const void*, const float*, const float*, const int32_t*, int,
                           float, float*, int32_t*, cudaStream_t);
 cudaError_t launch_gram_sym_tc(const void* Ah, const void* Al, const int32_t* offsets, int H, int n, int max_t,
@@ -53,13 +55,14 @@ int sweep_launches(int max_t);
 cudaError_t launch_apply_inverse(int d, const float* Minv, const float* R, const int32_t* offsets, int H, int max_t,
                                  int64_t ldA, float* C, const int32_t* status, cudaStream_t st);
 cudaError_t launch_attn_fwd_tc(int d, const void* Q, const void* K, const void* V, int H, int n, int T, float c2,
-                               float* O, float* lse2, int32_t* status, cudaStream_t st);
+                               float* O, float* lse2, int32_t* status, int qdiv, cudaStream_t st);
 cudaError_t launch_colscore_tc(int d, const void* Q, const void* K, const float* lse2, int H, int n, int T,
-                               float c2, float* score, int32_t* status, cudaStream_t st);
+                               float c2, float* score, int32_t* status, int qdiv, cudaStream_t st);
 bool tc_maps_available();
 cudaError_t launch_beta_out(float*, const int32_t*, int, int, float*, const int32_t*, cudaStream_t);
 
 constexpr int kMaxT = 4096;     // largest budget the per-head solvers support
+constexpr int kMaxHeads = 65535;  // heads index grid.y
 constexpr int kMaxStages = 32;
 
 // Optional per-stage CUDA events (KVC_FLAG_STAGE_TIMING), recorded on the
@@ -167,21 +170,22 @@ static bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 
 
 static kvc_status check_problem(const kvc_problem* p) {
     if (!p) return KVC_ERR_INVALID_ARG;
-    if (p->H < 1 || p->n < 1 || p->T < 1) return KVC_ERR_INVALID_ARG;
+    if (p->H < 1 || p->H > kMaxHeads || p->n < 1 || p->T < 1) return KVC_ERR_INVALID_ARG;
     if (p->d != 64 && p->d != 128) return KVC_ERR_INVALID_ARG;
     if (p->dtype != KVC_DTYPE_BF16 && p->dtype != KVC_DTYPE_F32) return KVC_ERR_INVALID_ARG;
     if (p->max_t < 1 || p->max_t > p->T || p->max_t > kMaxT) return KVC_ERR_INVALID_ARG;
     return KVC_OK;
 }
 
-static kvc_status check_params(const kvc_params& q, const kvc_problem& p) {
+// T_total: the length of the whole cache the forced ranges count positions of.
+static kvc_status check_params(const kvc_params& q, int64_t T_total) {
     if (!(q.scale >= 0.f) || !std::isfinite(q.scale)) return KVC_ERR_INVALID_ARG;
     if (!(q.eps_mu > 0.f) || !(q.eps_lambda > 0.f) || !std::isfinite(q.eps_mu) || !std::isfinite(q.eps_lambda))
         return KVC_ERR_INVALID_ARG;
     if (q.nnls_max_iter < 1 || q.nnls_max_zero < 1 || q.refine_iters < 0) return KVC_ERR_INVALID_ARG;
     if (q.keep_first < 0 || q.keep_last < 0 || (q.flags & ~(KVC_FLAG_STAGE_TIMING | KVC_FLAG_CHOLESKY_CV)) != 0)
         return KVC_ERR_INVALID_ARG;
-    if ((int64_t)q.keep_first + q.keep_last > p.T) return KVC_ERR_INVALID_ARG;
+    if ((int64_t)q.keep_first + q.keep_last > T_total) return KVC_ERR_INVALID_ARG;
     return KVC_OK;
 }
 
@@ -219,7 +223,7 @@ kvc_status kvc_workspace_size(const kvc_problem* p, const kvc_params* prm, size_
     if (s != KVC_OK || !bytes) return KVC_ERR_INVALID_ARG;
     kvc_params q;
     if (prm) q = *prm; else kvc_default_params(&q);
-    if ((s = check_params(q, *p)) != KVC_OK) return s;
+    if ((s = check_params(q, p->T)) != KVC_OK) return s;
     *bytes = make_layout(*p, q).total;
     return KVC_OK;
 }
@@ -229,7 +233,9 @@ kvc_status kvc_workspace_offset(const kvc_problem* p, const kvc_params* prm, int
     if (s != KVC_OK || !offset) return KVC_ERR_INVALID_ARG;
     kvc_params q;
     if (prm) q = *prm; else kvc_default_params(&q);
-    if ((s = check_params(q, *p)) != KVC_OK) return s;
+    // the layout does not depend on the forced ranges, which may count the
+    // positions of a longer cache (the per-chunk problem of a chunked call)
+    if ((s = check_params(q, INT64_MAX)) != KVC_OK) return s;
     const Layout L = make_layout(*p, q);
     switch (item) {
         case 0: *offset = L.O; break;
@@ -242,26 +248,22 @@ kvc_status kvc_workspace_offset(const kvc_problem* p, const kvc_params* prm, int
     return KVC_OK;
 }
 
-kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* Q_ref, const void* K, const void* V,
-                       const int32_t* budgets, const int32_t* offsets, int32_t* idx_out, void* C_k, float* beta,
-                       float* C_v, int32_t* head_status, void* workspace, size_t workspace_bytes,
-                       kvc_stream_t stream) {
-    kvc_status s = check_problem(p);
-    if (s != KVC_OK) return s;
-    kvc_params q;
-    if (prm) q = *prm; else kvc_default_params(&q);
-    if ((s = check_params(q, *p)) != KVC_OK) return s;
-    if (!Q_ref || !K || !V || !budgets || !offsets || !idx_out || !C_k || !beta || !C_v || !head_status)
-        return KVC_ERR_INVALID_ARG;
-    if (!aligned(Q_ref, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(C_k, 16) || !aligned(C_v, 16) ||
-        !aligned(beta, 4) || !aligned(idx_out, 4) || !aligned(budgets, 4) || !aligned(offsets, 4) ||
-        !aligned(head_status, 4))
-        return KVC_ERR_ALIGN;
+}  // extern "C"
+
+namespace kvc {
+
+// The launch sequence of one compaction over the heads of *p.  `chunks` > 1
+// when each head of *p is one of `chunks` contiguous chunks of a longer cache
+// (heads head * chunks + c share the reference queries of `head`); the
+// arguments have been checked by the caller.
+static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int chunks, const void* Q_ref,
+                                  const void* K, const void* V, const int32_t* budgets, const int32_t* offsets,
+                                  int32_t* idx_out, void* C_k, float* beta, float* C_v, int32_t* head_status,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t st) {
     const Layout L = make_layout(*p, q);
     if (!workspace || workspace_bytes < L.total) return KVC_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return KVC_ERR_ALIGN;
 
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(workspace);
     float* O = (float*)(ws + L.O);
     float* lse2 = (float*)(ws + L.lse2);
@@ -286,33 +288,41 @@ kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* 
     HeadScalars* hs = (HeadScalars*)(ws + L.hs);
 
     const int H = p->H, n = p->n, T = p->T, d = p->d, dt = p->dtype, mt = p->max_t;
-    const int forced = std::min(T, q.keep_first + q.keep_last);
+    const int qdiv = chunks;
     const float c2 = log2_scale(*p, q.scale);
 
     StageClock clk(q.flags & KVC_FLAG_STAGE_TIMING, st);
-    KVC_STAGE("validate", 1, launch_validate(budgets, offsets, H, T, mt, forced, head_status, hs, st));
+    KVC_STAGE("validate", 1,
+              launch_validate(budgets, offsets, H, T, mt, chunks, q.keep_first, q.keep_last, head_status, hs, st));
     // bf16 inputs take the tensor-core passes (tcgen05/TMEM/TMA); fp32 inputs
     // the FFMA passes (a tf32 contraction would not keep fp32 accuracy).
     if (dt == KVC_DTYPE_BF16) {
-        KVC_STAGE("attn_fwd", 1, launch_attn_fwd_tc(d, Q_ref, K, V, H, n, T, c2, O, lse2, head_status, st));
-        KVC_STAGE("colscore", 1, launch_colscore_tc(d, Q_ref, K, lse2, H, n, T, c2, score, head_status, st));
+        KVC_STAGE("attn_fwd", 1, launch_attn_fwd_tc(d, Q_ref, K, V, H, n, T, c2, O, lse2, head_status, qdiv, st));
+        KVC_STAGE("colscore", 1, launch_colscore_tc(d, Q_ref, K, lse2, H, n, T, c2, score, head_status, qdiv, st));
     } else {
-        KVC_STAGE("attn_fwd", 1, launch_attn_fwd_simt(dt, d, Q_ref, K, V, H, n, T, c2, O, lse2, head_status, st));
-        KVC_STAGE("colscore", 1, launch_colscore_simt(dt, d, Q_ref, K, lse2, H, n, T, c2, score, head_status, st));
+        KVC_STAGE("attn_fwd", 1,
+                  launch_attn_fwd_simt(dt, d, Q_ref, K, V, H, n, T, c2, O, lse2, head_status, qdiv, st));
+        KVC_STAGE("colscore", 1,
+                  launch_colscore_simt(dt, d, Q_ref, K, lse2, H, n, T, c2, score, head_status, qdiv, st));
     }
-    KVC_STAGE("select", 1, launch_select(score, H, T, offsets, q.keep_first, q.keep_last, idx_out, head_status, st));
+    KVC_STAGE("select", 1,
+              launch_select(score, H, T, offsets, chunks, q.keep_first, q.keep_last, idx_out, head_status, st));
     void* Ckw = ws + L.Ckw;
     const bool tc = dt == KVC_DTYPE_BF16;
     KVC_STAGE("gather", 1,
               launch_gather(dt, d, K, V, H, T, mt, offsets, idx_out, C_k, Vsel, tc ? Ckw : nullptr, L.ldA,
                             head_status, st));
+    if (chunks > 1)
+        KVC_STAGE("shift_idx", 1, launch_shift_idx(idx_out, offsets, H, T, mt, chunks, head_status, st));
     if (tc) {
         // the kept keys' per-head copy has ldA rows per head; the map sees H * ldA rows
         KVC_STAGE("masslogits", 1,
-                  launch_masslogits_tc(d, Q_ref, Ckw, lse2, offsets, H, n, mt, 0, L.ldA, c2, L2, head_status, st));
+                  launch_masslogits_tc(d, Q_ref, Ckw, lse2, offsets, H, n, mt, L.ldA, c2, L2, head_status, qdiv,
+                                       st));
     } else {
         KVC_STAGE("masslogits", 1,
-                  launch_masslogits(dt, d, Q_ref, C_k, lse2, offsets, H, n, mt, L.ldA, c2, L2, head_status, st));
+                  launch_masslogits(dt, d, Q_ref, C_k, lse2, offsets, H, n, mt, L.ldA, c2, L2, head_status, qdiv,
+                                    st));
     }
     KVC_STAGE("split_a", 2,
               launch_split_hilo(true, L2, H, n, L.ldA, offsets, 0, mt, ws + L.Ah, ws + L.Al, (float*)(ws + L.bpart),
@@ -351,6 +361,73 @@ kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* 
     }
     clk.finish();
     return KVC_OK;
+}
+
+// Whole-cache problem *p split into `chunks` chunks: the per-chunk problem.
+static kvc_status chunk_problem(const kvc_problem* p, int32_t chunks, kvc_problem* pc) {
+    if (!p || chunks < 1 || p->T < 1 || p->T % chunks != 0) return KVC_ERR_INVALID_ARG;
+    if ((int64_t)p->H * chunks > kMaxHeads) return KVC_ERR_INVALID_ARG;
+    *pc = *p;
+    pc->H = p->H * chunks;
+    pc->T = p->T / chunks;
+    return check_problem(pc);
+}
+
+static kvc_status check_buffers(const void* Q_ref, const void* K, const void* V, const int32_t* budgets,
+                                const int32_t* offsets, const int32_t* idx_out, const void* C_k, const float* beta,
+                                const float* C_v, const int32_t* head_status) {
+    if (!Q_ref || !K || !V || !budgets || !offsets || !idx_out || !C_k || !beta || !C_v || !head_status)
+        return KVC_ERR_INVALID_ARG;
+    if (!aligned(Q_ref, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(C_k, 16) || !aligned(C_v, 16) ||
+        !aligned(beta, 4) || !aligned(idx_out, 4) || !aligned(budgets, 4) || !aligned(offsets, 4) ||
+        !aligned(head_status, 4))
+        return KVC_ERR_ALIGN;
+    return KVC_OK;
+}
+
+}  // namespace kvc
+
+extern "C" {
+
+kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* Q_ref, const void* K, const void* V,
+                       const int32_t* budgets, const int32_t* offsets, int32_t* idx_out, void* C_k, float* beta,
+                       float* C_v, int32_t* head_status, void* workspace, size_t workspace_bytes,
+                       kvc_stream_t stream) {
+    kvc_status s = check_problem(p);
+    if (s != KVC_OK) return s;
+    kvc_params q;
+    if (prm) q = *prm; else kvc_default_params(&q);
+    if ((s = check_params(q, p->T)) != KVC_OK) return s;
+    if ((s = check_buffers(Q_ref, K, V, budgets, offsets, idx_out, C_k, beta, C_v, head_status)) != KVC_OK) return s;
+    return enqueue_compact(p, q, 1, Q_ref, K, V, budgets, offsets, idx_out, C_k, beta, C_v, head_status, workspace,
+                           workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kvc_status kvc_workspace_size_chunked(const kvc_problem* p, const kvc_params* prm, int32_t chunks, size_t* bytes) {
+    kvc_problem pc;
+    const kvc_status s = chunk_problem(p, chunks, &pc);
+    if (s != KVC_OK || !bytes) return KVC_ERR_INVALID_ARG;
+    kvc_params q;
+    if (prm) q = *prm; else kvc_default_params(&q);
+    if (check_params(q, p->T) != KVC_OK) return KVC_ERR_INVALID_ARG;
+    *bytes = make_layout(pc, q).total;
+    return KVC_OK;
+}
+
+kvc_status kvc_compact_chunked(const kvc_problem* p, const kvc_params* prm, int32_t chunks, const void* Q_ref,
+                               const void* K, const void* V, const int32_t* budgets, const int32_t* offsets,
+                               int32_t* idx_out, void* C_k, float* beta, float* C_v, int32_t* head_status,
+                               void* workspace, size_t workspace_bytes, kvc_stream_t stream) {
+    kvc_status s = check_problem(p);
+    if (s != KVC_OK) return s;
+    kvc_problem pc;
+    if ((s = chunk_problem(p, chunks, &pc)) != KVC_OK) return s;
+    kvc_params q;
+    if (prm) q = *prm; else kvc_default_params(&q);
+    if ((s = check_params(q, p->T)) != KVC_OK) return s;
+    if ((s = check_buffers(Q_ref, K, V, budgets, offsets, idx_out, C_k, beta, C_v, head_status)) != KVC_OK) return s;
+    return enqueue_compact(&pc, q, chunks, Q_ref, K, V, budgets, offsets, idx_out, C_k, beta, C_v, head_status,
+                           workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 kvc_status kvc_attend(const kvc_problem* p, const void* Q, int32_t n_q, const void* C_k, const float* beta,

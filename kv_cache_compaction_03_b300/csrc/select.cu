@@ -7,12 +7,30 @@
 
 namespace kvc {
 
+// Forced positions of head h.  When a KV head's cache is split into `chunks`
+// contiguous chunks of T positions each (heads h = head * chunks + c), the
+// caller's keep_first / keep_last count positions of the whole cache: chunk c
+// keeps [0, kf) and [T - kl, T) with kf, kl the parts of those ranges that
+// fall inside it.  chunks = 1 is the unchunked cache.
+struct ForcedRange {
+    int kf, kl;
+};
+__device__ __forceinline__ ForcedRange forced_range(int h, int T, int chunks, int keep_first, int keep_last) {
+    const int c = h % chunks;
+    const int64_t kf = (int64_t)keep_first - (int64_t)c * T;
+    const int64_t kl = (int64_t)keep_last - (int64_t)(chunks - 1 - c) * T;
+    return ForcedRange{(int)max((int64_t)0, min((int64_t)T, kf)), (int)max((int64_t)0, min((int64_t)T, kl))};
+}
+
 // ---------------------------------------------------------------- validate
 // grid ceil(H/256), block 256.  head_status[h] = OK or BAD_BUDGET.
 __global__ void k_validate(const int32_t* __restrict__ budgets, const int32_t* __restrict__ offsets, int H, int T,
-                           int max_t, int forced, int32_t* __restrict__ status, HeadScalars* __restrict__ hs) {
+                           int max_t, int chunks, int keep_first, int keep_last, int32_t* __restrict__ status,
+                           HeadScalars* __restrict__ hs) {
     const int h = blockIdx.x * blockDim.x + threadIdx.x;
     if (h >= H) return;
+    const ForcedRange fr = forced_range(h, T, chunks, keep_first, keep_last);
+    const int forced = min(T, fr.kf + fr.kl);
     const int t = budgets[h];
     bool ok = t >= 1 && t <= T && t <= max_t && t >= forced;
     ok = ok && offsets[h + 1] - offsets[h] == t;
@@ -65,10 +83,11 @@ __device__ __forceinline__ uint32_t score_key(const float* sc, int j, int T, int
 // bit patterns (monotone for non-negative floats); ties at the threshold go
 // to the lowest positions.
 __global__ void __launch_bounds__(1024) k_select(const float* __restrict__ score, int T, const int32_t* __restrict__ offsets,
-                                                 int keep_first, int keep_last, int32_t* __restrict__ idx_out,
-                                                 int32_t* __restrict__ status) {
+                                                 int chunks, int keep_first, int keep_last,
+                                                 int32_t* __restrict__ idx_out, int32_t* __restrict__ status) {
     const int h = blockIdx.x;
     if (!head_ok(status, h)) return;
+    const ForcedRange fr = forced_range(h, T, chunks, keep_first, keep_last);
     __shared__ int hist[256];
     __shared__ int sbuf[33];
     __shared__ uint32_t s_digit;
@@ -85,7 +104,7 @@ __global__ void __launch_bounds__(1024) k_select(const float* __restrict__ score
         for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
         __syncthreads();
         for (int j = threadIdx.x; j < T; j += blockDim.x) {
-            const uint32_t k = score_key(sc, j, T, keep_first, keep_last);
+            const uint32_t k = score_key(sc, j, T, fr.kf, fr.kl);
             if (shift == 24 && k > 0x7f800000u) s_nan = 1;
             if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
         }
@@ -118,7 +137,7 @@ __global__ void __launch_bounds__(1024) k_select(const float* __restrict__ score
     const int j0 = min(T, (int)threadIdx.x * chunk), j1 = min(T, j0 + chunk);
     int gt = 0, eq = 0;
     for (int j = j0; j < j1; ++j) {
-        const uint32_t k = score_key(sc, j, T, keep_first, keep_last);
+        const uint32_t k = score_key(sc, j, T, fr.kf, fr.kl);
         gt += k > tau;
         eq += k == tau;
     }
@@ -128,7 +147,7 @@ __global__ void __launch_bounds__(1024) k_select(const float* __restrict__ score
     const int pos0 = block_exclusive_scan(gt + take_eq, sbuf, &tot);
     int pos = pos0, er = eq_before;
     for (int j = j0; j < j1; ++j) {
-        const uint32_t k = score_key(sc, j, T, keep_first, keep_last);
+        const uint32_t k = score_key(sc, j, T, fr.kf, fr.kl);
         bool take = k > tau;
         if (k == tau) {
             take = er < krem;
@@ -173,14 +192,34 @@ __global__ void __launch_bounds__(256) k_gather(const TIn* __restrict__ K, const
     for (int c = lane; c < D; c += 32) vo[c] = to_f32(vr[c]);
 }
 
-cudaError_t launch_validate(const int32_t* budgets, const int32_t* offsets, int H, int T, int max_t, int forced,
-                            int32_t* status, HeadScalars* hs, cudaStream_t st) {
-    k_validate<<<(H + 255) / 256, 256, 0, st>>>(budgets, offsets, H, T, max_t, forced, status, hs);
+// ---------------------------------------------------------------- chunk shift
+// grid (ceil(max_t/256), H), block 256.  Chunk c = h % chunks of a cache
+// split into chunks of T positions: idx[off .. off+t) += c * T, turning
+// positions inside the chunk into positions in the whole cache.
+__global__ void k_shift_idx(int32_t* __restrict__ idx, const int32_t* __restrict__ offsets, int T, int chunks,
+                            const int32_t* __restrict__ status) {
+    const int h = blockIdx.y;
+    if (!head_ok(status, h)) return;
+    const int off = offsets[h];
+    const int t = offsets[h + 1] - off;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < t) idx[off + i] += (h % chunks) * T;
+}
+
+cudaError_t launch_validate(const int32_t* budgets, const int32_t* offsets, int H, int T, int max_t, int chunks,
+                            int keep_first, int keep_last, int32_t* status, HeadScalars* hs, cudaStream_t st) {
+    k_validate<<<(H + 255) / 256, 256, 0, st>>>(budgets, offsets, H, T, max_t, chunks, keep_first, keep_last, status,
+                                                hs);
     return cudaGetLastError();
 }
-cudaError_t launch_select(const float* score, int H, int T, const int32_t* offsets, int keep_first, int keep_last,
-                          int32_t* idx_out, int32_t* status, cudaStream_t st) {
-    k_select<<<H, 1024, 0, st>>>(score, T, offsets, keep_first, keep_last, idx_out, status);
+cudaError_t launch_select(const float* score, int H, int T, const int32_t* offsets, int chunks, int keep_first,
+                          int keep_last, int32_t* idx_out, int32_t* status, cudaStream_t st) {
+    k_select<<<H, 1024, 0, st>>>(score, T, offsets, chunks, keep_first, keep_last, idx_out, status);
+    return cudaGetLastError();
+}
+cudaError_t launch_shift_idx(int32_t* idx, const int32_t* offsets, int H, int T, int max_t, int chunks,
+                             const int32_t* status, cudaStream_t st) {
+    k_shift_idx<<<dim3((max_t + 255) / 256, H), 256, 0, st>>>(idx, offsets, T, chunks, status);
     return cudaGetLastError();
 }
 template <typename TIn, int D>

@@ -93,6 +93,36 @@ def test_rejects_bad_problems_on_host():
     assert _call(good, prm=kvc.default_params(keep_first=200, keep_last=100)) == kvc.ERR_INVALID_ARG
 
 
+def test_chunked_rejects_bad_shapes_on_host():
+    ok = kvc.make_problem(2, 64, 1000, 64, kvc.DTYPE_BF16, 250)
+    # the workspace of 4 chunks is that of the per-chunk problem
+    assert kvc.workspace_size_chunked(ok, None, 4) == kvc.workspace_size(
+        kvc.make_problem(8, 64, 250, 64, kvc.DTYPE_BF16, 250))
+    assert kvc.workspace_size_chunked(ok, None, 1) == kvc.workspace_size(
+        kvc.make_problem(2, 64, 1000, 64, kvc.DTYPE_BF16, 250))
+    bad = [
+        (kvc.make_problem(2, 64, 1000, 64, 0, 100), 3),      # 1000 % 3 != 0
+        (kvc.make_problem(2, 64, 1000, 64, 0, 300), 4),      # max_t > T / chunks
+        (kvc.make_problem(2, 64, 1000, 64, 0, 100), 0),      # no chunks
+        (kvc.make_problem(40000, 64, 1000, 64, 0, 100), 2),  # H * chunks above the grid limit
+    ]
+    for p, c in bad:
+        with pytest.raises(kvc.KvcError):
+            kvc.workspace_size_chunked(p, None, c)
+        ptr = 0x100000
+        assert kvc.compact_chunked(p, None, c, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1 << 30,
+                                   stream=0) == kvc.ERR_INVALID_ARG
+    # forced keeps count positions of the whole cache, not of one chunk
+    prm = kvc.default_params(keep_first=4, keep_last=400)
+    assert kvc.workspace_size_chunked(ok, prm, 4) > 0
+    ptr = 0x100000
+    assert kvc.compact_chunked(ok, None, 4, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 16,
+                               stream=0) == kvc.ERR_WORKSPACE
+    assert kvc.compact_chunked(ok, None, 4, 0x100004, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1 << 30,
+                               stream=0) == kvc.ERR_ALIGN
+    assert _call(kvc.make_problem(70000, 64, 256, 64, 0, 32)) == kvc.ERR_INVALID_ARG   # H above the grid limit
+
+
 def test_attend_rejects_bad_args_on_host():
     p = kvc.make_problem(2, 1, 1, 128, kvc.DTYPE_BF16, 1)
     assert kvc.attend(p, 0x1000, 0, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0.0, 0) == kvc.ERR_INVALID_ARG
