@@ -49,8 +49,8 @@ cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* of
                             int32_t* nz, float* S, int32_t* piv, float* u, float* r, float* d0, HeadScalars* hs,
                             int zmax, int max_iter, int refine_iters, void* rpart_ws, int32_t* status,
                             cudaStream_t st, int* launches);
-cudaError_t launch_sweep_inverse(float* A, const int32_t* offsets, int H, int max_t, int64_t ldA, float* U, float* V,
-                                 float* P, int32_t* status, cudaStream_t st);
+cudaError_t launch_sweep_inverse(float* A, const int32_t* offsets, int H, int max_t, int64_t ldA, float* U,
+                                 void* split, float* P, int32_t* status, cudaStream_t st);
 int sweep_launches(int max_t);
 cudaError_t launch_apply_inverse(int d, const float* Minv, const float* R, const int32_t* offsets, int H, int max_t,
                                  int64_t ldA, float* C, const int32_t* status, cudaStream_t st);
@@ -145,7 +145,7 @@ static Layout make_layout(const kvc_problem& p, const kvc_params& prm) {
     L.Ckw = carve(c, H * ldA * d * 2);
     L.G = carve(c, H * ldA * ldA * 4);
     L.dinv = carve(c, H * ldA * 64 * 4);      // Cholesky diagonal inverses; sweep U panel
-    L.swV = carve(c, H * 64 * ldA * 4);       // sweep: copy of the pivot row block
+    L.swV = carve(c, 6 * H * 64 * ldA * 2);   // sweep: U^T and V as three bf16 terms each
     L.swP = carve(c, H * 64 * 64 * 4);        // sweep: pivot block inverse
     L.b = carve(c, H * mt * 4);
     L.f = carve(c, H * mt * 4);
@@ -331,7 +331,7 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
               launch_gram_sym_tc(ws + L.Ah, ws + L.Al, offsets, H, n, mt, L.ldA, G, L.ldA, head_status, st));
     KVC_STAGE("ridge_g", 1, launch_ridge_g(G, b, offsets, H, L.ldA, q.eps_mu, f, hs, head_status, st));
     KVC_STAGE("inv_h", sweep_launches(mt),
-              launch_sweep_inverse(G, offsets, H, mt, L.ldA, dinv, (float*)(ws + L.swV), (float*)(ws + L.swP),
+              launch_sweep_inverse(G, offsets, H, mt, L.ldA, dinv, ws + L.swV, (float*)(ws + L.swP),
                                    head_status, st));
     int nnls_launches = 0;
     KVC_STAGE("nnls", nnls_launches,
@@ -355,7 +355,7 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
         KVC_STAGE("cholsolve", 1, launch_cholsolve(d, G, dinv, R, offsets, H, L.ldA, C_v, head_status, st));
     } else {
         KVC_STAGE("inv_m", sweep_launches(mt),
-                  launch_sweep_inverse(G, offsets, H, mt, L.ldA, dinv, (float*)(ws + L.swV), (float*)(ws + L.swP),
+                  launch_sweep_inverse(G, offsets, H, mt, L.ldA, dinv, ws + L.swV, (float*)(ws + L.swP),
                                        head_status, st));
         KVC_STAGE("apply_minv", 1, launch_apply_inverse(d, G, R, offsets, H, mt, L.ldA, C_v, head_status, st));
     }

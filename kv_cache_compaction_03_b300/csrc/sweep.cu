@@ -14,14 +14,14 @@
 // and columns past t act as an identity block.
 //
 //   k_sweep_pivot   grid (blocks, H): every CTA sweeps the 64 x 64 pivot
-//                   block in registers (64 scalar sweeps, giving -P), then
-//                   computes U_i = A_ik P for its row block i (stored
-//                   transposed) and copies V_i = A_ki (row block k)
-//   k_sweep_update  grid (lower tiles, H): every 64 x 64 tile on or below
-//                   the diagonal is updated from U, V and P (128 threads, an
-//                   8 x 4 register tile each; both operand tiles are 64
-//                   contiguous 256-byte rows); on a head's last block the
-//                   stored result is negated, so the matrix ends as +H^{-1}
+//                   block in registers (64 scalar sweeps over 4 x 8 thread
+//                   tiles, giving -P), then computes U_i = A_ik P for its row
+//                   block i (stored transposed) and copies V_i = A_ki
+//   k_sweep_update_tc  grid (lower 128 x 128 tiles, H): A_ij -= U_i V_j on
+//                   the tcgen05 tensor cores (operands as three exact bf16
+//                   terms, six products), with the pivot row / column copies
+//                   in the epilogue; on a head's last block the stored result
+//                   is negated, so the matrix ends as +H^{-1}
 //   k_sweep_mirror  copies the lower triangle into the upper one
 //   k_symv          y = H^{-1} v for every head (one warp per row)
 //   k_apply_inverse C_v = M^{-1} R (the least-squares fit of C_v when M is
@@ -29,9 +29,10 @@
 // The sweep keeps the symmetric matrix in its lower triangle (row-major,
 // leading dimension ldA); an entry above the diagonal is read from its
 // mirror image.  The finished inverse is stored in full.
-#include "common.cuh"
+#include "tc.cuh"
 
 namespace kvc {
+using namespace tc;
 
 namespace {
 constexpr int SB = 64;     // sweep block
@@ -39,22 +40,44 @@ constexpr int SB = 64;     // sweep block
 struct SweepArgs {
     float* A;                 // [H][ldA][ldA]
     float* U;                 // [H][64][ldA]  U^T: U[p][r] = (A_ik P)[r][p]
-    float* V;                 // [H][64][ldA]
+    __nv_bfloat16* Us;        // [3][H][64][ldA]  U^T as three bf16 terms
+    __nv_bfloat16* Vs;        // [3][H][64][ldA]  V[p][r] = A_kr[p][r], three bf16 terms
     float* P;                 // [H][64][64]
     const int32_t* offsets;
     int64_t ldA;
+    int64_t ts;               // elements between the terms of Us / Vs (H * 64 * ldA)
     int k0;                   // first row of the pivot block
     int32_t* status;
 };
 
+// x = hi + mid + lo exactly (three bf16 terms of 8 significant bits each;
+// the subtractions are exact), for fp32 x away from the underflow range.
+__device__ __forceinline__ void split3(float x, __nv_bfloat16& hi, __nv_bfloat16& mid, __nv_bfloat16& lo) {
+    hi = __float2bfloat16_rn(x);
+    const float r1 = x - __bfloat162float(hi);
+    mid = __float2bfloat16_rn(r1);
+    lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+}
 
-// grid (blocks, H), block 256.  Thread (ii, cq) holds row ii, columns
-// 16 cq .. 16 cq + 15 of the pivot block in registers; the 64 scalar sweeps
-// run as 4 x 16 with the inner 16 unrolled, so the column the sweep pivots on
-// has a static register index (and the loop body stays small).
+
+// grid (blocks, H), block 128.  Every CTA first inverts the 64 x 64 pivot
+// block by 64 scalar sweeps, then (row blocks i != k) forms U_i = A_ik P.
+//
+// The scalar sweeps are a dependent chain, so their cost is the latency of
+// one step: the owner threads publish the pivot row through shared memory,
+// one barrier, every thread reads what it needs and updates its entries.
+// Each thread holds a 4 x 8 register tile (rows 4 ty .., columns 8 tx ..),
+// so a step reads only 8 + 4 pivot-row values per thread (by symmetry the
+// pivot row also provides the pivot column): the shared-memory return
+// traffic of those broadcast reads, not the barrier, sets the step time.
+// The chain loop runs as 8 x 8 with the inner 8 unrolled, so the row and
+// column a step pivots on have static register indices.
 constexpr int kPS = SB + 4;      // padded smem row, 16-byte aligned
+constexpr int kPivThreads = 128;
+constexpr int kCR = 4;           // chain tile rows per thread (columns: 8)
 
-__global__ void __launch_bounds__(256) k_sweep_pivot(SweepArgs s) {
+__global__ void __launch_bounds__(kPivThreads) k_sweep_pivot(SweepArgs s) {
+    constexpr int NT = kPivThreads, R = kCR;
     const int h = blockIdx.y;
     if (!head_ok(s.status, h)) return;
     const int t = s.offsets[h + 1] - s.offsets[h];
@@ -62,80 +85,99 @@ __global__ void __launch_bounds__(256) k_sweep_pivot(SweepArgs s) {
     if (k0 >= t) return;
     const int r0 = blockIdx.x * SB;
     if (r0 >= t) return;
+    __shared__ __align__(16) float Dn[SB][kPS];     // pivot block, then P
+    __shared__ __align__(16) float At[SB][kPS];     // At[p][r] = A_ik[r][p]
     __shared__ __align__(16) float rowb[2][SB];
-    __shared__ __align__(16) float Ps[SB][kPS];     // A_ik (rows r0.., columns k0..)
-    __shared__ __align__(16) float Pn[SB][kPS];     // P
     __shared__ int bad;
     const float* A = s.A + (int64_t)h * s.ldA * s.ldA;
     const int tid = threadIdx.x;
-    const int ii = tid >> 2, cq = tid & 3;          // row ii, columns 16 cq + m
-    // the pivot block: its stored lower triangle, staged through Pn
-    for (int e = tid; e < SB * SB; e += 256) {
-        const int r = e / SB, c = e % SB;
-        if (c <= r) Pn[r][c] = (k0 + r < t && k0 + c < t) ? A[(int64_t)(k0 + r) * s.ldA + k0 + c] : (r == c ? 1.f : 0.f);
-    }
-    __syncthreads();
-    float a[16];
+    const bool diag = (r0 == k0);
+    // stage the pivot block (its stored lower triangle is what gets used) and
+    // A_ik (rows below the pivot: stored directly; above: the transpose of
+    // the stored tile (k, i)); every load is issued before the first store
+    {
+        float4 dv[8], av[8];
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        const int c = 16 * cq + m;
-        a[m] = (c <= ii) ? Pn[ii][c] : Pn[c][ii];
-    }
-    if (r0 > k0) {
-        for (int e = tid; e < SB * SB; e += 256) {
-            const int rr = e / SB, c = e % SB;
-            const int r = r0 + rr, col = k0 + c;
-            Ps[rr][c] = (r < t && col < t) ? A[(int64_t)r * s.ldA + col] : 0.f;
+        for (int q = 0; q < 8; ++q) {
+            const int e = tid + NT * q, r = e >> 4, c4 = (e & 15) * 4;
+            dv[q] = *reinterpret_cast<const float4*>(A + (int64_t)(k0 + r) * s.ldA + k0 + c4);
+            if (!diag) {
+                if (r0 > k0) av[q] = *reinterpret_cast<const float4*>(A + (int64_t)(r0 + r) * s.ldA + k0 + c4);
+                else av[q] = *reinterpret_cast<const float4*>(A + (int64_t)(k0 + r) * s.ldA + r0 + c4);
+            }
         }
-    } else if (r0 < k0) {
-        // A_ik above the diagonal: the transpose of the stored tile (k, i)
-        for (int e = tid; e < SB * SB; e += 256) {
-            const int c = e / SB, rr = e % SB;
-            const int r = r0 + rr, col = k0 + c;
-            Ps[rr][c] = (r < t && col < t) ? A[(int64_t)col * s.ldA + r] : 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = tid + NT * q, r = e >> 4, c4 = (e & 15) * 4;
+            *reinterpret_cast<float4*>(&Dn[r][c4]) = dv[q];
+            if (!diag) {
+                const float x[4] = {av[q].x, av[q].y, av[q].z, av[q].w};
+                if (r0 > k0) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) At[c4 + j][r] = (r0 + r < t && k0 + c4 + j < t) ? x[j] : 0.f;
+                } else {
+                    // stored row k0 + r, columns r0 + c4 + j: A_ik[c4 + j][r]
+                    *reinterpret_cast<float4*>(&At[r][c4]) = make_float4(
+                        (k0 + r < t && r0 + c4 < t) ? x[0] : 0.f, (k0 + r < t && r0 + c4 + 1 < t) ? x[1] : 0.f,
+                        (k0 + r < t && r0 + c4 + 2 < t) ? x[2] : 0.f, (k0 + r < t && r0 + c4 + 3 < t) ? x[3] : 0.f);
+                }
+            }
         }
     }
     if (tid == 0) bad = 0;
-    __syncthreads();     // Pn is rewritten below
-    // 64 scalar sweeps of the pivot block; the block stays symmetric, so row
-    // p also provides column p
-    for (int pb = 0; pb < 4; ++pb) {
+    __syncthreads();
+    const int tx = tid & 7, ty = tid >> 3;
+    float a[R][8];
 #pragma unroll
-        for (int m0 = 0; m0 < 16; ++m0) {
-            const int p = 16 * pb + m0;
-            float* rb = rowb[p & 1];
-            if (ii == p) {
+    for (int i = 0; i < R; ++i)
 #pragma unroll
-                for (int m = 0; m < 16; m += 4)
-                    *reinterpret_cast<float4*>(rb + 16 * cq + m) = make_float4(a[m], a[m + 1], a[m + 2], a[m + 3]);
+        for (int j = 0; j < 8; ++j) {
+            const int r = R * ty + i, c = 8 * tx + j;
+            const bool in = (k0 + r < t) && (k0 + c < t);    // rows / columns past t: identity
+            a[i][j] = in ? ((c <= r) ? Dn[r][c] : Dn[c][r]) : (r == c ? 1.f : 0.f);
+        }
+    for (int pb = 0; pb < 8; ++pb) {
+#pragma unroll
+        for (int m0 = 0; m0 < 8; ++m0) {
+            const int p = 8 * pb + m0;
+            float* rb = rowb[m0 & 1];
+            if (ty == p / R) {
+#pragma unroll
+                for (int i = 0; i < R; ++i)
+                    if (i == p % R) {
+                        *reinterpret_cast<float4*>(rb + 8 * tx) = make_float4(a[i][0], a[i][1], a[i][2], a[i][3]);
+                        *reinterpret_cast<float4*>(rb + 8 * tx + 4) = make_float4(a[i][4], a[i][5], a[i][6], a[i][7]);
+                    }
             }
             __syncthreads();
+            const float4 x0 = *reinterpret_cast<const float4*>(rb + 8 * tx);
+            const float4 x1 = *reinterpret_cast<const float4*>(rb + 8 * tx + 4);
+            const float4 c4 = *reinterpret_cast<const float4*>(rb + R * ty);
+            const float row[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const float col[R] = {c4.x, c4.y, c4.z, c4.w};
             float d = rb[p];
             if (!(d > 0.f) || !isfinite(d)) {
-                if (tid == 0) bad = 1;
+                bad = 1;
                 d = 1.f;
             }
             // reciprocal: hardware approximation plus one Newton step (~1 ulp)
             float inv;
             asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(d));
             inv = inv * fmaf(-d, inv, 2.f);
-            if (ii != p) {
-                // a_ic -= a_ip a_pc / d; column p itself becomes a_ip / d
-                const float f = rb[ii] * inv;
 #pragma unroll
-                for (int m = 0; m < 16; m += 4) {
-                    const float4 r4 = *reinterpret_cast<const float4*>(rb + 16 * cq + m);
-                    a[m] = fmaf(-f, r4.x, a[m]);
-                    a[m + 1] = fmaf(-f, r4.y, a[m + 1]);
-                    a[m + 2] = fmaf(-f, r4.z, a[m + 2]);
-                    a[m + 3] = fmaf(-f, r4.w, a[m + 3]);
+            for (int i = 0; i < R; ++i) {
+                if (R * ty + i == p) {
+                    // row p becomes a_pc / d, the pivot -1 / d
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) a[i][j] *= inv;
+                    if (tx == pb) a[i][m0] = -inv;
+                } else {
+                    // a_ic -= a_ip a_pc / d; column p itself becomes a_ip / d
+                    const float f = col[i] * inv;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) a[i][j] = fmaf(-f, row[j], a[i][j]);
+                    if (tx == pb) a[i][m0] = f;
                 }
-                if (cq == pb) a[m0] = f;
-            } else {
-                // row p becomes a_pc / d, the pivot -1 / d
-#pragma unroll
-                for (int m = 0; m < 16; ++m) a[m] *= inv;
-                if (cq == pb) a[m0] = -inv;
             }
         }
     }
@@ -144,38 +186,70 @@ __global__ void __launch_bounds__(256) k_sweep_pivot(SweepArgs s) {
         if (blockIdx.x == 0 && tid == 0) set_status(s.status, h, KVC_ERR_NOT_SPD);
         return;
     }
+    // the block now holds -P
 #pragma unroll
-    for (int m = 0; m < 16; m += 4)
-        *reinterpret_cast<float4*>(&Pn[ii][16 * cq + m]) = make_float4(-a[m], -a[m + 1], -a[m + 2], -a[m + 3]);
+    for (int i = 0; i < R; ++i) {
+        *reinterpret_cast<float4*>(&Dn[R * ty + i][8 * tx]) = make_float4(-a[i][0], -a[i][1], -a[i][2], -a[i][3]);
+        *reinterpret_cast<float4*>(&Dn[R * ty + i][8 * tx + 4]) = make_float4(-a[i][4], -a[i][5], -a[i][6], -a[i][7]);
+    }
     __syncthreads();
-    if (r0 == k0) {
+    if (diag) {
         float* Ph = s.P + (int64_t)h * SB * SB;
-        for (int e = tid; e < SB * SB; e += 256) Ph[e] = Pn[e / SB][e % SB];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = tid + NT * q, r = e >> 4, c4 = (e & 15) * 4;
+            *reinterpret_cast<float4*>(Ph + r * SB + c4) = *reinterpret_cast<const float4*>(&Dn[r][c4]);
+        }
         return;
     }
-    // U_i = A_ik P  (rows r0 .. r0+63), V_i = A_ki = A_ik^T
-    float acc[16];
+    // U_i = A_ik P: thread (uy, ux) forms rows 8 uy .. 8 uy + 7, columns 4 ux .. 4 ux + 3
+    const int ux = tid & 15, uy = tid >> 4;
+    float acc[8][4];
 #pragma unroll
-    for (int m = 0; m < 16; ++m) acc[m] = 0.f;
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 #pragma unroll 4
     for (int p = 0; p < SB; ++p) {
-        const float x = Ps[ii][p];
+        const float4 a0 = *reinterpret_cast<const float4*>(&At[p][8 * uy]);
+        const float4 a1 = *reinterpret_cast<const float4*>(&At[p][8 * uy + 4]);
+        const float4 pv = *reinterpret_cast<const float4*>(&Dn[p][4 * ux]);
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float bv[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
-        for (int m = 0; m < 16; m += 4) {
-            const float4 q = *reinterpret_cast<const float4*>(&Pn[p][16 * cq + m]);
-            acc[m] = fmaf(x, q.x, acc[m]);
-            acc[m + 1] = fmaf(x, q.y, acc[m + 1]);
-            acc[m + 2] = fmaf(x, q.z, acc[m + 2]);
-            acc[m + 3] = fmaf(x, q.w, acc[m + 3]);
-        }
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
-    float* Uh = s.U + (int64_t)h * SB * s.ldA + r0;
+    // U^T[c][r0 + r] = U[r][c]: for each column c, 8 consecutive rows, in
+    // fp32 (the pivot row / column copies) and as three bf16 terms (the
+    // tensor-core update's operand)
+    const int64_t hb = (int64_t)h * SB * s.ldA + r0;
 #pragma unroll
-    for (int m = 0; m < 16; ++m) Uh[(int64_t)(16 * cq + m) * s.ldA + ii] = acc[m];
-    float* Vh = s.V + (int64_t)h * SB * s.ldA + r0;
-    for (int e = tid; e < SB * SB; e += 256) {
-        const int c = e / SB, rr = e % SB;
-        Vh[(int64_t)c * s.ldA + rr] = Ps[rr][c];
+    for (int j = 0; j < 4; ++j) {
+        const int64_t o = hb + (int64_t)(4 * ux + j) * s.ldA + 8 * uy;
+        *reinterpret_cast<float4*>(s.U + o) = make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
+        *reinterpret_cast<float4*>(s.U + o + 4) = make_float4(acc[4][j], acc[5][j], acc[6][j], acc[7][j]);
+        __align__(16) __nv_bfloat16 th[8], tm[8], tl[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) split3(acc[i][j], th[i], tm[i], tl[i]);
+        *reinterpret_cast<uint4*>(s.Us + o) = *reinterpret_cast<const uint4*>(th);
+        *reinterpret_cast<uint4*>(s.Us + s.ts + o) = *reinterpret_cast<const uint4*>(tm);
+        *reinterpret_cast<uint4*>(s.Us + 2 * s.ts + o) = *reinterpret_cast<const uint4*>(tl);
+    }
+    // V_i = A_ki = A_ik^T: V[c][r0 + r] = A_ik[r][c] = At[c][r], as three bf16 terms
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int e = tid + NT * q, c = e >> 4, r4 = (e & 15) * 4;
+        const float4 v = *reinterpret_cast<const float4*>(&At[c][r4]);
+        const float x[4] = {v.x, v.y, v.z, v.w};
+        __align__(8) __nv_bfloat16 th[4], tm[4], tl[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split3(x[i], th[i], tm[i], tl[i]);
+        const int64_t o = hb + (int64_t)c * s.ldA + r4;
+        *reinterpret_cast<uint2*>(s.Vs + o) = *reinterpret_cast<const uint2*>(th);
+        *reinterpret_cast<uint2*>(s.Vs + s.ts + o) = *reinterpret_cast<const uint2*>(tm);
+        *reinterpret_cast<uint2*>(s.Vs + 2 * s.ts + o) = *reinterpret_cast<const uint2*>(tl);
     }
 }
 
@@ -187,97 +261,200 @@ __device__ __forceinline__ void tri_tile(int p, int& I, int& J) {
     J = p - i * (i + 1) / 2;
 }
 
-constexpr int kUpdThreads = 128;
-constexpr int kUS = SB + 4;      // padded smem row: 16-byte aligned
+// ---------------------------------------------------------------- update
+// A_ij -= U_i V_j for every 128 x 128 tile (I >= J) of the lower triangle,
+// on the tcgen05 tensor cores: C[i][j] = sum_p U^T[p][i] V[p][j] with K = 64
+// (one pivot block).  Both operands are stored [64][ldA] (p rows, the tile
+// dimension contiguous): the MN-major layout, loaded by TMA as [64][64]
+// bf16 boxes with 128-byte swizzle.  Each fp32 operand is three exact bf16
+// terms; the six products hi.hi, hi.mid, mid.hi, hi.lo, lo.hi, mid.mid are
+// accumulated in fp32 in tensor memory (smallest first).  The three dropped
+// products are below 2^-25 of |u||v|, under fp32 rounding, so the update
+// keeps the accuracy of an fp32 FMA product.
+// Rows / columns of the pivot block take the sweep's copies instead:
+// A_ik <- U_i, A_kj <- U_j^T, A_kk <- -P.  On a head's last pivot block the
+// stored result is negated, so the matrix ends as +H^{-1}.
+// The fp32 tile of A comes in by TMA too ([32][32] boxes, 128-byte
+// swizzle), into the operand space once the products are done (so that two
+// CTAs fit on an SM); the epilogue subtracts in shared memory and writes the
+// boxes back with TMA stores.  Entries past t inside a box are
+// rewritten with sg times their old value minus a zero product (rows and
+// columns past t of U and V are zero); nothing reads them.
+// Warp roles: warp 0 TMA, warp 1 MMA issuer and TMEM owner (128 columns),
+// warps 2..5 epilogue (32 tile rows each).
+constexpr int UB = 128;                    // update tile
+constexpr int kUBox = 64 * 128;            // [64 p][64 columns] bf16 box: 8 KB
+constexpr int kABox = 32 * 128;            // [32 rows][32 columns] fp32 box: 4 KB
+constexpr int kUOps = 12 * kUBox;          // operand boxes
+constexpr int kUThreads = 192;
+constexpr int kUSmem = kUOps + 1024 + 64;
+static_assert(16 * kABox <= kUOps, "the A tile reuses the operand space");
 
-// grid (blocks * (blocks + 1) / 2, H), block 128: tile (bi >= bj) of the lower triangle.
-__global__ void __launch_bounds__(kUpdThreads) k_sweep_update(SweepArgs s) {
+__global__ void __launch_bounds__(kUThreads, 2)
+    k_sweep_update_tc(const __grid_constant__ CUtensorMap mU0, const __grid_constant__ CUtensorMap mU1,
+                      const __grid_constant__ CUtensorMap mU2, const __grid_constant__ CUtensorMap mV0,
+                      const __grid_constant__ CUtensorMap mV1, const __grid_constant__ CUtensorMap mV2,
+                      const __grid_constant__ CUtensorMap mA, SweepArgs s) {
     const int h = blockIdx.y;
     if (!head_ok(s.status, h)) return;
     const int t = s.offsets[h + 1] - s.offsets[h];
     const int k0 = s.k0;
     if (k0 >= t) return;
-    int bi, bj;
-    tri_tile(blockIdx.x, bi, bj);
-    const int ri = bi * SB, rj = bj * SB;
-    if (ri >= t) return;
-    const bool last = k0 + SB >= t;        // this head's last pivot block: store +H^{-1}
-    const float sg = last ? -1.f : 1.f;
-    float* A = s.A + (int64_t)h * s.ldA * s.ldA;
-    const float* Uh = s.U + (int64_t)h * SB * s.ldA;     // U^T [64][ldA]
-    const float* Vh = s.V + (int64_t)h * SB * s.ldA;
-    const float* Ph = s.P + (int64_t)h * SB * SB;
-    const int tid = threadIdx.x;
-    const bool pi = (ri == k0), pj = (rj == k0);
-    if (pi || pj) {
-        // pivot row / column / block: copies, no products
-        for (int e = tid; e < SB * SB; e += kUpdThreads) {
-            const int r = e / SB, c = e % SB;
-            if (ri + r >= t || rj + c >= t) continue;
-            float v;
-            if (pi && pj) v = -Ph[e];
-            else if (pj) v = Uh[(int64_t)c * s.ldA + ri + r];        // A_ik = U_i
-            else v = Uh[(int64_t)r * s.ldA + rj + c];               // A_kj = U_j^T
-            A[(int64_t)(ri + r) * s.ldA + rj + c] = sg * v;
-        }
-        return;
+    int I, J;
+    tri_tile(blockIdx.x, I, J);
+    if (I * UB >= t) return;
+    const float sg = (k0 + SB >= t) ? -1.f : 1.f;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smA = sm;                       // A boxes (after the MMAs): (row quarter q, chunk c) at (4 q + c) * kABox
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + kUOps);
+    uint64_t* fullA = full + 1;
+    uint64_t* acc_full = full + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 3);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(full, 1);
+        mbar_init(fullA, 1);
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
     }
-    __shared__ __align__(16) float Ut[SB][kUS];     // Ut[p][r] = U_i[r][p]
-    __shared__ __align__(16) float Vs[SB][kUS];     // Vs[p][c] = V[p][rj + c]
-    {
-        float4 ru[8], rv[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int e = tid + kUpdThreads * q;           // float4 index: row e / 16, column 4 (e % 16)
-            const int p = e >> 4, c4 = (e & 15) * 4;
-            ru[q] = *reinterpret_cast<const float4*>(Uh + (int64_t)p * s.ldA + ri + c4);
-            rv[q] = *reinterpret_cast<const float4*>(Vh + (int64_t)p * s.ldA + rj + c4);
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int e = tid + kUpdThreads * q;
-            const int p = e >> 4, c4 = (e & 15) * 4;
-            *reinterpret_cast<float4*>(&Ut[p][c4]) = ru[q];
-            *reinterpret_cast<float4*>(&Vs[p][c4]) = rv[q];
-        }
-    }
+    if (warp == 1) tmem_alloc(tmem_slot, 128);
+    fence_before_sync();
     __syncthreads();
-    const int ty = tid >> 4, tx = tid & 15;          // rows 8 ty .., columns 4 tx ..
-    float acc[8][4];
+    fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    if (warp == 0) {
+        if (lane == 0) {
+            const CUtensorMap* mu[3] = {&mU0, &mU1, &mU2};
+            const CUtensorMap* mv[3] = {&mV0, &mV1, &mV2};
+            prefetch_tmap(&mA);
+            mbar_expect_tx(full, (uint32_t)kUOps);
 #pragma unroll
-    for (int a = 0; a < 8; ++a)
+            for (int q = 0; q < 3; ++q)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
-#pragma unroll 4
-    for (int p = 0; p < SB; ++p) {
-        const float4 u0 = *reinterpret_cast<const float4*>(&Ut[p][ty * 8]);
-        const float4 u1 = *reinterpret_cast<const float4*>(&Ut[p][ty * 8 + 4]);
-        const float4 v0 = *reinterpret_cast<const float4*>(&Vs[p][tx * 4]);
-        const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-        const float v[4] = {v0.x, v0.y, v0.z, v0.w};
+                for (int b = 0; b < 2; ++b) {
+                    tma_load_3d(sm + (2 * q + b) * kUBox, mu[q], full, I * UB + 64 * b, 0, h);
+                    tma_load_3d(sm + (6 + 2 * q + b) * kUBox, mv[q], full, J * UB + 64 * b, 0, h);
+                }
+            // the A tile goes where the operands were, once the MMAs have read them
+            if (mbar_wait(acc_full, 0, abort_flag)) {
+                mbar_expect_tx(fullA, 16u * kABox);
 #pragma unroll
-        for (int a = 0; a < 8; ++a)
+                for (int q = 0; q < 4; ++q)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) acc[a][c] = fmaf(u[a], v[c], acc[a][c]);
-    }
+                    for (int c = 0; c < 4; ++c)
+                        tma_load_3d(smA + (4 * q + c) * kABox, &mA, fullA, J * UB + 32 * c, I * UB + 32 * q, h);
+                int never = 0;
+                (void)mbar_wait(fullA, 0, &never);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            if (mbar_wait(full, 0, abort_flag)) {
+                fence_after_sync();
+                constexpr uint32_t idesc = idesc_bf16(128, 128, true, true);
+                const uint32_t base = smem_addr(sm);
+                // (U term, V term) pairs, smallest products first
+                constexpr int pu[6] = {2, 0, 1, 1, 0, 0};
+                constexpr int pv[6] = {0, 2, 1, 0, 1, 0};
 #pragma unroll
-    for (int a = 0; a < 8; ++a) {
-        const int r = ri + ty * 8 + a;
-        if (r >= t) continue;
-        float* row = A + (int64_t)r * s.ldA + rj + tx * 4;
-        if (rj + tx * 4 + 4 <= t) {
-            float4 o = *reinterpret_cast<float4*>(row);
-            o.x = sg * (o.x - acc[a][0]);
-            o.y = sg * (o.y - acc[a][1]);
-            o.z = sg * (o.z - acc[a][2]);
-            o.w = sg * (o.w - acc[a][3]);
-            *reinterpret_cast<float4*>(row) = o;
-        } else {
+                for (int kk = 0; kk < SB / 16; ++kk) {
+                    const uint32_t o = (uint32_t)kk * 2048;     // 16 rows of p: two 8-row groups
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                if (rj + tx * 4 + c < t) row[c] = sg * (row[c] - acc[a][c]);
+                    for (int m = 0; m < 6; ++m) {
+                        const uint64_t da = sdesc_sw128(base + 2 * pu[m] * kUBox + o, kUBox, 1024);
+                        const uint64_t db = sdesc_sw128(base + (6 + 2 * pv[m]) * kUBox + o, kUBox, 1024);
+                        mma_ss(tmem, da, db, idesc, (kk > 0 || m > 0) ? 1u : 0u);
+                    }
+                }
+            }
+            mma_commit(acc_full);
+            int never = 0;
+            (void)mbar_wait(acc_full, 0, &never);
+        }
+        __syncwarp();
+    } else {
+        // lane = tile row i (TMEM lane quarter); the 32 rows lie all inside or
+        // all outside the pivot block, and so do a chunk's 32 columns
+        const int quarter = warp & 3;
+        const int i0 = I * UB + quarter * 32;
+        const int i = i0 + lane;
+        const int64_t ld = s.ldA;
+        const bool rowK = i0 >= k0 && i0 < k0 + SB;
+        const float* Uh = s.U + (int64_t)h * SB * ld;
+        const float* Ph = s.P + (int64_t)h * SB * SB;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag) && mbar_wait(fullA, 0, abort_flag));
+        if (ok) {
+            fence_after_sync();
+            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+#pragma unroll 1
+            for (int c = 0; c < UB / 32; ++c) {
+                const int j0 = J * UB + c * 32;
+                const bool colK = j0 >= k0 && j0 < k0 + SB;
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + c * 32, r);
+                tmem_ld_wait();
+                // row `lane` of the swizzled box: 16-byte chunk x sits at x ^ (lane & 7)
+                uint8_t* rowp = smA + (4 * quarter + c) * kABox + lane * 128;
+                if (!rowK && !colK) {
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        float4* p4 = reinterpret_cast<float4*>(rowp + ((x ^ (lane & 7)) << 4));
+                        float4 v = *p4;
+                        v.x = sg * (v.x - __uint_as_float(r[4 * x]));
+                        v.y = sg * (v.y - __uint_as_float(r[4 * x + 1]));
+                        v.z = sg * (v.z - __uint_as_float(r[4 * x + 2]));
+                        v.w = sg * (v.w - __uint_as_float(r[4 * x + 3]));
+                        *p4 = v;
+                    }
+                } else if (i < t) {
+                    // copies: A_kk <- -P, A_ik <- U_i, A_kj <- U_j^T (the chunk
+                    // ends inside the row: j0 < t <= ldA, both multiples of 32)
+                    float v[32];
+                    if (colK && !rowK) {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) v[q] = Uh[(int64_t)(j0 - k0 + q) * ld + i];
+                    } else {
+                        const float* src = colK ? Ph + (i - k0) * SB + (j0 - k0) : Uh + (int64_t)(i - k0) * ld + j0;
+#pragma unroll
+                        for (int q = 0; q < 32; q += 4) {
+                            const float4 x = *reinterpret_cast<const float4*>(src + q);
+                            v[q] = colK ? -x.x : x.x;
+                            v[q + 1] = colK ? -x.y : x.y;
+                            v[q + 2] = colK ? -x.z : x.z;
+                            v[q + 3] = colK ? -x.w : x.w;
+                        }
+                    }
+#pragma unroll
+                    for (int x = 0; x < 8; ++x)
+                        *reinterpret_cast<float4*>(rowp + ((x ^ (lane & 7)) << 4)) =
+                            make_float4(sg * v[4 * x], sg * v[4 * x + 1], sg * v[4 * x + 2], sg * v[4 * x + 3]);
+                }
+            }
+            // this warp's four boxes back to A (boxes starting past t hold nothing needed)
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (i0 < t) {
+#pragma unroll 1
+                    for (int c = 0; c < UB / 32; ++c)
+                        if (J * UB + 32 * c < t)
+                            tma_store_3d(&mA, smA + (4 * quarter + c) * kABox, J * UB + 32 * c, i0, h);
+                }
+                bulk_commit();
+                bulk_wait_read_all();
+            }
+            __syncwarp();
         }
     }
+    if (threadIdx.x == 0 && *abort_flag) set_status(s.status, h, KVC_ERR_TIMEOUT);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (warp == 1) tmem_dealloc(tmem, 128);
 }
 
 // Upper triangle <- lower triangle.  grid (blocks * (blocks - 1) / 2 + blocks, H), block 256.
@@ -389,16 +566,32 @@ __global__ void __launch_bounds__(256) k_apply_inverse(const float* __restrict__
 
 int sweep_launches(int max_t) { return 2 * ((max_t + SB - 1) / SB) + 1; }
 
-// H^{-1} in place for every head (max_t bounds t_h).  U, V: [H][64][ldA],
-// P: [H][64][64] scratch.
-cudaError_t launch_sweep_inverse(float* A, const int32_t* offsets, int H, int max_t, int64_t ldA, float* U, float* V,
-                                 float* P, int32_t* status, cudaStream_t st) {
+bool make_map_bf16(CUtensorMap* m, const void* base, int cols, int64_t ld, int rows, int H);   // tmap.cu
+bool make_map_f32(CUtensorMap* m, const void* base, int cols, int64_t ld, int rows, int H);    // tmap.cu
+
+// H^{-1} in place for every head (max_t bounds t_h).  U: fp32 [H][64][ldA];
+// split: bf16 [6][H][64][ldA] (U^T and V as three terms each); P: [H][64][64].
+cudaError_t launch_sweep_inverse(float* A, const int32_t* offsets, int H, int max_t, int64_t ldA, float* U,
+                                 void* split, float* P, int32_t* status, cudaStream_t st) {
     const int nb = (max_t + SB - 1) / SB;
     const int ntri = nb * (nb + 1) / 2;
+    const int nu = (max_t + UB - 1) / UB;
+    const int64_t ts = (int64_t)H * SB * ldA;
+    __nv_bfloat16* Us = static_cast<__nv_bfloat16*>(split);
+    __nv_bfloat16* Vs = Us + 3 * ts;
+    CUtensorMap mu[3], mv[3], ma;
+    for (int q = 0; q < 3; ++q)
+        if (!make_map_bf16(&mu[q], Us + q * ts, (int)ldA, ldA, SB, H) ||
+            !make_map_bf16(&mv[q], Vs + q * ts, (int)ldA, ldA, SB, H))
+            return cudaErrorInvalidValue;
+    if (!make_map_f32(&ma, A, (int)ldA, ldA, (int)ldA, H)) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k_sweep_update_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
+    if (e != cudaSuccess) return e;
     for (int k = 0; k < nb; ++k) {
-        SweepArgs s{A, U, V, P, offsets, ldA, k * SB, status};
-        k_sweep_pivot<<<dim3(nb, H), 256, 0, st>>>(s);
-        k_sweep_update<<<dim3(ntri, H), kUpdThreads, 0, st>>>(s);
+        SweepArgs s{A, U, Us, Vs, P, offsets, ldA, ts, k * SB, status};
+        k_sweep_pivot<<<dim3(nb, H), kPivThreads, 0, st>>>(s);
+        k_sweep_update_tc<<<dim3(nu * (nu + 1) / 2, H), kUThreads, kUSmem, st>>>(mu[0], mu[1], mu[2], mv[0], mv[1],
+                                                                                  mv[2], ma, s);
     }
     k_sweep_mirror<<<dim3(ntri, H), 256, 0, st>>>(A, offsets, ldA, status);
     return cudaGetLastError();
