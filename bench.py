@@ -247,6 +247,68 @@ def max_over_ranks(x: float, dist, device) -> float:
     return float(t.item())
 
 
+# --------------------------------------------------------------- decode leg
+def measure_decode(kvc, w, inputs, K, V, Ck, beta, Cv, offsets, total, flush, stream, dev, dist, reps=20):
+    """One decoded token per query head (n_q = the GQA group) read through
+    kvc_attend: over the compacted cache (t_h keys with bias) and over the
+    full cache (T keys, bias 0, values in fp32 like C_v), L2 flushed before
+    every call.  Both are HBM streams; returns times, speedup and the
+    fraction of the measured HBM bandwidth each reaches."""
+    import numpy as np
+    import torch
+
+    nq = max(1, w.gqa)
+    qt = inputs["Qt"][:, :nq]
+    qt = np.ascontiguousarray(qt)
+    Qd = torch.from_numpy(qt.view(np.int16) if w.dtype == "bf16" else qt)
+    if w.dtype == "bf16":
+        Qd = Qd.view(torch.bfloat16)
+    Qd = Qd.to(dev)
+    H, T, d = w.H, w.T, w.d
+    Kf = K.view(H * T, d)
+    Vf = V.view(H * T, d).float()
+    bf = torch.zeros(H * T, dtype=torch.float32, device=dev)
+    of = torch.arange(H + 1, dtype=torch.int32, device=dev) * T
+    O = torch.empty(H, nq, d, dtype=torch.float32, device=dev)
+    st = torch.empty(H, dtype=torch.int32, device=dev)
+    prob = kvc.make_problem(H, nq, 1, d, kvc.DTYPE_BF16 if w.dtype == "bf16" else kvc.DTYPE_F32, 1)
+
+    def timed(ck, b, cv, off):
+        for _ in range(3):
+            if kvc.attend(prob, Qd, nq, ck, b, cv, off, O, st, 0.0, stream):
+                raise RuntimeError("kvc_attend refused the call")
+        ms = 0.0
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            kvc.attend(prob, Qd, nq, ck, b, cv, off, O, st, 0.0, stream)
+            e1.record(stream)
+            e1.synchronize()
+            ms += e0.elapsed_time(e1)
+        if not bool((st == 0).all()):
+            raise RuntimeError("kvc_attend head status not OK")
+        return ms / reps
+
+    comp_ms = max_over_ranks(timed(Ck, beta, Cv, offsets), dist, dev)
+    full_ms = max_over_ranks(timed(Kf, bf, Vf, of), dist, dev)
+    b_in = 2 if w.dtype == "bf16" else 4
+    per_key = d * (b_in + 4) + 4
+    io = H * nq * d * (b_in + 4)
+    comp_bytes = total * per_key + io
+    full_bytes = H * T * per_key + io
+    peaks, src = _peaks()
+    return {
+        "n_q": nq, "keys_compacted": int(total), "keys_full": H * T,
+        "compacted_us": round(comp_ms * 1e3, 2), "full_us": round(full_ms * 1e3, 2),
+        "speedup": round(full_ms / comp_ms, 2),
+        "compacted_hbm_frac": round(comp_bytes / (comp_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+        "full_hbm_frac": round(full_bytes / (full_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+        "peak_source": f"{src} hbm_gbs",
+        "what": "kvc_attend, one decoded token per query head, compacted cache vs full cache (bias 0, fp32 values)",
+    }
+
+
 # --------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     import numpy as np
@@ -374,6 +436,9 @@ def run_ours(args, rank, world, local_rank):
     if not np.all(o_st.numpy() == 0):
         raise RuntimeError("head status not OK in the end-to-end loop")
 
+    # ---- decode: kvc_attend over the compacted cache vs over the full cache
+    decode = measure_decode(kvc, w, inputs, K, V, Ck, beta, Cv, offsets, total, flush, stream, dev, dist)
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -419,6 +484,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roof,
         "stages": per_stage,
         "cpu_baseline": cpu,
+        "decode": decode,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

@@ -243,6 +243,11 @@ kvc_status kvc_workspace_size_chunked(const kvc_problem* p, const kvc_params* pr
  *   head_status int32 [H]: KVC_OK, BAD_BUDGET (empty or inconsistent range),
  *              NONFINITE (every bias -inf for some query)
  *   scale      logit scale; 0 -> 1/sqrt(d)
+ * With n_q <= 16 (decode: one new token per query head of a group) each head
+ * is split over a cluster of 8 CTAs that stream its keys and merge their
+ * partial softmax states on chip; with more queries each CTA takes a tile of
+ * 64 queries of one head.  Both give the same result up to fp32 rounding.
+ * 1 <= H <= 65535.
  * Errors: INVALID_ARG, ALIGN, CUDA. */
 kvc_status kvc_attend(const kvc_problem* p, const void* Q, int32_t n_q,
                       const void* C_k, const float* beta, const float* C_v,

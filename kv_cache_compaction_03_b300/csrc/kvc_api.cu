@@ -25,6 +25,9 @@ cudaError_t launch_masslogits(int, int, const void*, const void*, const float*, 
                               float, float*, const int32_t*, int, cudaStream_t);
 cudaError_t launch_attend(int, int, const void*, int, const void*, const float*, const float*, const int32_t*, int,
                           float, float*, int32_t*, cudaStream_t);
+cudaError_t launch_attend_decode(int, int, const void*, int, const void*, const float*, const float*, const int32_t*,
+                                 int, float, float*, int32_t*, cudaStream_t);
+int attend_decode_max_queries();
 cudaError_t launch_gram_sym_tc(const void* Ah, const void* Al, const int32_t* offsets, int H, int n, int max_t,
                                int64_t ld, float* C, int64_t ldc, int32_t* status, cudaStream_t st);
 cudaError_t launch_gram_rect_tc(int d, const void* Ah, const void* Al, const void* Bh, const void* Bl,
@@ -433,7 +436,7 @@ kvc_status kvc_compact_chunked(const kvc_problem* p, const kvc_params* prm, int3
 kvc_status kvc_attend(const kvc_problem* p, const void* Q, int32_t n_q, const void* C_k, const float* beta,
                       const float* C_v, const int32_t* offsets, float* O_out, int32_t* head_status, float scale,
                       kvc_stream_t stream) {
-    if (!p || p->H < 1 || (p->d != 64 && p->d != 128) || n_q < 1 ||
+    if (!p || p->H < 1 || p->H > kMaxHeads || (p->d != 64 && p->d != 128) || n_q < 1 ||
         (p->dtype != KVC_DTYPE_BF16 && p->dtype != KVC_DTYPE_F32) || !(scale >= 0.f) || !std::isfinite(scale))
         return KVC_ERR_INVALID_ARG;
     if (!Q || !C_k || !beta || !C_v || !offsets || !O_out || !head_status) return KVC_ERR_INVALID_ARG;
@@ -442,8 +445,14 @@ kvc_status kvc_attend(const kvc_problem* p, const void* Q, int32_t n_q, const vo
         return KVC_ERR_ALIGN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     KVC_TRY(cudaMemsetAsync(head_status, 0, sizeof(int32_t) * p->H, st));
-    KVC_TRY(launch_attend(p->dtype, p->d, Q, n_q, C_k, beta, C_v, offsets, p->H, log2_scale(*p, scale), O_out,
-                          head_status, st));
+    // few queries per head (decode): a cluster of CTAs splits each head's keys;
+    // many queries: query tiles per head
+    if (n_q <= attend_decode_max_queries())
+        KVC_TRY(launch_attend_decode(p->dtype, p->d, Q, n_q, C_k, beta, C_v, offsets, p->H, log2_scale(*p, scale),
+                                     O_out, head_status, st));
+    else
+        KVC_TRY(launch_attend(p->dtype, p->d, Q, n_q, C_k, beta, C_v, offsets, p->H, log2_scale(*p, scale), O_out,
+                              head_status, st));
     return KVC_OK;
 }
 
