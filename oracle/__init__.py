@@ -18,3 +18,4 @@ from .am import (  # noqa: F401
     select_top_t,
 )
 from .chunked import compact_chunked  # noqa: F401
+from .omp import compact_head_omp, omp_residual, omp_select  # noqa: F401
