@@ -191,8 +191,8 @@ def time_oracle(w, heads, buds):
     return times, cores
 
 
-def config_dict(w, buds, world):
-    return {"workload": w.name, "heads_per_gpu": w.H, "n": w.n, "T": w.T, "d": w.d,
+def config_dict(w, buds, world, select="rms"):
+    return {"workload": w.name, "heads_per_gpu": w.H, "n": w.n, "T": w.T, "d": w.d, "key_selection": select,
             "t": (w.t if w.t is not None else f"nonuniform mean {float(sum(buds)) / len(buds):.1f}"),
             "input_dtype": w.dtype, "keep_first": w.keep_first, "keep_last": w.keep_last,
             "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"}
@@ -343,7 +343,8 @@ def run_ours(args, rank, world, local_rank):
     total = int(buds.sum())
     max_t = int(buds.max())
     prob = kvc.make_problem(w.H, w.n, w.T, w.d, kvc.DTYPE_BF16 if w.dtype == "bf16" else kvc.DTYPE_F32, max_t)
-    prm = kvc.default_params(keep_first=w.keep_first, keep_last=w.keep_last, flags=kvc.FLAG_STAGE_TIMING)
+    flags = kvc.FLAG_STAGE_TIMING | (kvc.FLAG_SELECT_OMP if args.select == "omp" else 0)
+    prm = kvc.default_params(keep_first=w.keep_first, keep_last=w.keep_last, flags=flags)
     ws_bytes = kvc.workspace_size(prob, prm)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -477,7 +478,7 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "bf16" if TENSOR_STAGES else "f32",
         "solver_dtype": "f32",
         "data": "synthetic (seeded generator, workload shapes of the pages)",
-        "config": config_dict(w, buds, world),
+        "config": config_dict(w, buds, world, args.select),
         "e2e": {"value": round(e2e_value, 1), "unit": "head-tokens/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": int(launches),
@@ -512,6 +513,8 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--select", default="rms", choices=["rms", "omp"],
+                    help="key selection: highest RMS attention (default) or orthogonal matching pursuit")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

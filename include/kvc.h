@@ -98,6 +98,20 @@ typedef struct kvc_params {
  * inverse by symmetric block sweeps (same results to rounding; the default is
  * faster because its block steps are shorter). */
 #define KVC_FLAG_CHOLESKY_CV 2u
+/* kvc_params.flags: choose the kept keys by orthogonal matching pursuit
+ * instead of the highest RMS attention (page section 2, "Pipeline
+ * algorithmique", key selection: keys picked greedily to best meet the
+ * attention-mass objective, the weights then fitted by NNLS).  Atoms are the
+ * columns p_j of the relative mass P_qj = exp(S_qj - lse_q) of all T keys,
+ * the target is 1 per query; a step adds the key with the largest
+ * <p_j, r> / ||p_j|| (ties to the lower position) where r is the residual of
+ * the least-squares fit of 1 on the keys chosen so far; forced positions come
+ * first.  beta and C_v are then fitted as usual.  The workspace grows by the
+ * fp32 P of every head (H * T * n * 4 bytes) and an orthonormal basis
+ * (H * max_t * n * 4 bytes); the selection order is readable at
+ * kvc_workspace_offset item 5.  The pursuit is sequential over t: expect it
+ * to cost far more than the default selection.  Not for kvc_compact_chunked. */
+#define KVC_FLAG_SELECT_OMP 4u
 
 /* Fill *prm with the defaults listed above.  Returns KVC_ERR_INVALID_ARG for a
  * null pointer. */
@@ -116,6 +130,8 @@ kvc_status kvc_workspace_size(const kvc_problem* p, const kvc_params* prm, size_
  *   3 W      fp32 [sum t]     NNLS weights w = exp(beta), offsets-indexed
  *   4 HEAD   32-byte records per head (ridges mu, lambda; NNLS zero-set
  *            size and iterations)
+ *   5 ORDER  int32 [H][max_t]: keys in the order the pursuit chose them
+ *            (KVC_FLAG_SELECT_OMP only; INVALID_ARG otherwise)
  * prm->keep_first / keep_last are not checked against p->T here (the layout
  * does not depend on them).
  * Host-only.  Errors: INVALID_ARG (bad problem/params or unknown item). */

@@ -34,7 +34,7 @@ ERR_TIMEOUT = 20
 DTYPE_BF16 = 0
 DTYPE_F32 = 1
 
-WS_O, WS_LSE2, WS_SCORE, WS_W, WS_HEAD = 0, 1, 2, 3, 4
+WS_O, WS_LSE2, WS_SCORE, WS_W, WS_HEAD, WS_ORDER = 0, 1, 2, 3, 4, 5
 
 
 class Problem(ctypes.Structure):
@@ -66,6 +66,7 @@ EXPORTS = ("kvc_default_params", "kvc_workspace_size", "kvc_workspace_offset", "
            "kvc_stage_times", "kvc_status_string", "kvc_version")
 FLAG_STAGE_TIMING = 1
 FLAG_CHOLESKY_CV = 2
+FLAG_SELECT_OMP = 4
 
 
 def lib() -> ctypes.CDLL:

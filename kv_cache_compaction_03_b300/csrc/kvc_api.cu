@@ -28,6 +28,12 @@ cudaError_t launch_attend(int, int, const void*, int, const void*, const float*,
 cudaError_t launch_attend_decode(int, int, const void*, int, const void*, const float*, const float*, const int32_t*,
                                  int, float, float*, int32_t*, cudaStream_t);
 int attend_decode_max_queries();
+size_t omp_workspace_bytes(int H, int n, int T, int max_t);
+size_t omp_order_offset(int H, int n, int T, int max_t);
+int omp_launches(int max_t);
+cudaError_t launch_omp_select(int dtype, int d, const void* Q, const void* K, const float* lse2, float c2, int H,
+                              int n, int T, int max_t, const int32_t* offsets, int keep_first, int keep_last,
+                              void* ws, int32_t* idx_out, int32_t* status, cudaStream_t st);
 cudaError_t launch_gram_sym_tc(const void* Ah, const void* Al, const int32_t* offsets, int H, int n, int max_t,
                                int64_t ld, float* C, int64_t ldc, int32_t* status, cudaStream_t st);
 cudaError_t launch_gram_rect_tc(int d, const void* Ah, const void* Al, const void* Bh, const void* Bl,
@@ -119,7 +125,7 @@ struct StageClock {
 struct Layout {
     int64_t ldA;
     int zmax;
-    size_t O, lse2, score, L2, Ah, Al, Oh, Ol, bpart, Vsel, Ckw, G, dinv, swV, swP, rpart, b, f, x, x0, d0, u, r, R, zflag, zlist, nz, piv, S, hs, total;
+    size_t O, lse2, score, L2, Ah, Al, Oh, Ol, bpart, Vsel, Ckw, G, dinv, swV, swP, rpart, b, f, x, x0, d0, u, r, R, zflag, zlist, nz, piv, S, hs, omp, total;
 };
 
 static size_t carve(size_t& cur, size_t bytes) {
@@ -165,6 +171,8 @@ static Layout make_layout(const kvc_problem& p, const kvc_params& prm) {
     L.piv = carve(c, H * 16);
     L.S = carve(c, H * zm * zm * 4);
     L.hs = carve(c, H * sizeof(HeadScalars));
+    // key selection by matching pursuit: the relative mass of every key and the pursuit's state
+    L.omp = (prm.flags & KVC_FLAG_SELECT_OMP) ? carve(c, omp_workspace_bytes(p.H, p.n, p.T, p.max_t)) : 0;
     L.total = (size_t)round_up((int64_t)c, 256);
     return L;
 }
@@ -186,7 +194,8 @@ static kvc_status check_params(const kvc_params& q, int64_t T_total) {
     if (!(q.eps_mu > 0.f) || !(q.eps_lambda > 0.f) || !std::isfinite(q.eps_mu) || !std::isfinite(q.eps_lambda))
         return KVC_ERR_INVALID_ARG;
     if (q.nnls_max_iter < 1 || q.nnls_max_zero < 1 || q.refine_iters < 0) return KVC_ERR_INVALID_ARG;
-    if (q.keep_first < 0 || q.keep_last < 0 || (q.flags & ~(KVC_FLAG_STAGE_TIMING | KVC_FLAG_CHOLESKY_CV)) != 0)
+    if (q.keep_first < 0 || q.keep_last < 0 ||
+        (q.flags & ~(KVC_FLAG_STAGE_TIMING | KVC_FLAG_CHOLESKY_CV | KVC_FLAG_SELECT_OMP)) != 0)
         return KVC_ERR_INVALID_ARG;
     if ((int64_t)q.keep_first + q.keep_last > T_total) return KVC_ERR_INVALID_ARG;
     return KVC_OK;
@@ -246,6 +255,10 @@ kvc_status kvc_workspace_offset(const kvc_problem* p, const kvc_params* prm, int
         case 2: *offset = L.score; break;
         case 3: *offset = L.x; break;
         case 4: *offset = L.hs; break;
+        case 5:
+            if (!(q.flags & KVC_FLAG_SELECT_OMP)) return KVC_ERR_INVALID_ARG;
+            *offset = L.omp + omp_order_offset(p->H, p->n, p->T, p->max_t);
+            break;
         default: return KVC_ERR_INVALID_ARG;
     }
     return KVC_OK;
@@ -299,17 +312,26 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
               launch_validate(budgets, offsets, H, T, mt, chunks, q.keep_first, q.keep_last, head_status, hs, st));
     // bf16 inputs take the tensor-core passes (tcgen05/TMEM/TMA); fp32 inputs
     // the FFMA passes (a tf32 contraction would not keep fp32 accuracy).
+    const bool omp = (q.flags & KVC_FLAG_SELECT_OMP) != 0;
     if (dt == KVC_DTYPE_BF16) {
         KVC_STAGE("attn_fwd", 1, launch_attn_fwd_tc(d, Q_ref, K, V, H, n, T, c2, O, lse2, head_status, qdiv, st));
-        KVC_STAGE("colscore", 1, launch_colscore_tc(d, Q_ref, K, lse2, H, n, T, c2, score, head_status, qdiv, st));
+        if (!omp)
+            KVC_STAGE("colscore", 1,
+                      launch_colscore_tc(d, Q_ref, K, lse2, H, n, T, c2, score, head_status, qdiv, st));
     } else {
         KVC_STAGE("attn_fwd", 1,
                   launch_attn_fwd_simt(dt, d, Q_ref, K, V, H, n, T, c2, O, lse2, head_status, qdiv, st));
-        KVC_STAGE("colscore", 1,
-                  launch_colscore_simt(dt, d, Q_ref, K, lse2, H, n, T, c2, score, head_status, qdiv, st));
+        if (!omp)
+            KVC_STAGE("colscore", 1,
+                      launch_colscore_simt(dt, d, Q_ref, K, lse2, H, n, T, c2, score, head_status, qdiv, st));
     }
-    KVC_STAGE("select", 1,
-              launch_select(score, H, T, offsets, chunks, q.keep_first, q.keep_last, idx_out, head_status, st));
+    if (omp)
+        KVC_STAGE("omp", omp_launches(mt),
+                  launch_omp_select(dt, d, Q_ref, K, lse2, c2, H, n, T, mt, offsets, q.keep_first, q.keep_last,
+                                    ws + L.omp, idx_out, head_status, st));
+    else
+        KVC_STAGE("select", 1,
+                  launch_select(score, H, T, offsets, chunks, q.keep_first, q.keep_last, idx_out, head_status, st));
     void* Ckw = ws + L.Ckw;
     const bool tc = dt == KVC_DTYPE_BF16;
     KVC_STAGE("gather", 1,
@@ -428,6 +450,7 @@ kvc_status kvc_compact_chunked(const kvc_problem* p, const kvc_params* prm, int3
     kvc_params q;
     if (prm) q = *prm; else kvc_default_params(&q);
     if ((s = check_params(q, p->T)) != KVC_OK) return s;
+    if (q.flags & KVC_FLAG_SELECT_OMP) return KVC_ERR_INVALID_ARG;      // the pursuit runs on whole caches only
     if ((s = check_buffers(Q_ref, K, V, budgets, offsets, idx_out, C_k, beta, C_v, head_status)) != KVC_OK) return s;
     return enqueue_compact(&pc, q, chunks, Q_ref, K, V, budgets, offsets, idx_out, C_k, beta, C_v, head_status,
                            workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));

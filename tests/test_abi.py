@@ -89,7 +89,7 @@ def test_rejects_bad_problems_on_host():
     assert _call(good, Q=0x100004) == kvc.ERR_ALIGN
     assert _call(good, ws_bytes=16) == kvc.ERR_WORKSPACE
     assert _call(good, prm=kvc.default_params(eps_mu=0.0)) == kvc.ERR_INVALID_ARG
-    assert _call(good, prm=kvc.default_params(flags=4)) == kvc.ERR_INVALID_ARG
+    assert _call(good, prm=kvc.default_params(flags=8)) == kvc.ERR_INVALID_ARG
     assert _call(good, prm=kvc.default_params(keep_first=200, keep_last=100)) == kvc.ERR_INVALID_ARG
 
 
