@@ -248,6 +248,50 @@ kvc_status kvc_compact_chunked(const kvc_problem* p, const kvc_params* prm, int3
  * Errors: INVALID_ARG. */
 kvc_status kvc_workspace_size_chunked(const kvc_problem* p, const kvc_params* prm, int32_t chunks, size_t* bytes);
 
+/* Thought-aware compaction ("Thought-Aware KV Cache Compaction" explainer,
+ * section 2, on top of Attention Matching): B, segment budgets, and C, pivot
+ * protection.  The segments are given (the page finds them in the text).
+ *   - alpha_j = mean over the n_win window queries (the last tokens'
+ *     queries) of softmax_j(q K^T * scale): the attention key j receives.
+ *   - Pivots: alpha_j > pivot_c * mean_j alpha_j.  They are kept with
+ *     beta = 0 and C_v = V exactly.
+ *   - Segment i = positions [seg_bounds[i], seg_bounds[i+1]) keeps its pivots
+ *     and t_i other keys, t_i ~ sqrt(w_i) * n_i of the budget left after all
+ *     pivots (w_i = sum of alpha over the segment, n_i its non-pivot count),
+ *     capped at n_i with the excess re-shared, made integral by largest
+ *     remainder (ties to the lower segment); computed in double.
+ *   - Inside a segment, the t_i keys of highest RMS attention over the
+ *     reference queries (as kvc_compact).
+ *   - beta and C_v as kvc_compact, with the pivots held fixed: the NNLS and
+ *     the least squares run over the other kept keys and the pivots'
+ *     contribution moves to the targets (ridges over all kept keys).
+ * Arguments as kvc_compact, plus (device unless stated):
+ *   Q_win       [H][n_win][d] dtype, 16B aligned; n_win >= 1 (host)
+ *   seg_bounds  int32 [nseg+1], shared by every head: 0 = b_0 < ... < b_nseg
+ *               = T; 1 <= nseg <= 1024 (host).  Checked on the device: a head
+ *               gets BAD_BUDGET if they are not so
+ *   pivot_c     host; the threshold factor c > 0
+ *   budgets     t_h per head, pivots included (BAD_BUDGET if a head has more
+ *               pivots than t_h)
+ *   seg_budgets_out int32 [H][nseg]: t_i (non-pivot keys kept per segment)
+ *   pivots_out  uint8 [H][T]: 1 where alpha_j is above the threshold
+ *   workspace   at least kvc_workspace_size_tam bytes
+ * prm->keep_first / keep_last must be 0 and KVC_FLAG_SELECT_OMP unset.
+ * Errors: INVALID_ARG, ALIGN, WORKSPACE, CUDA.  Intermediates: the
+ * kvc_workspace_offset items of the same *p and *prm. */
+kvc_status kvc_compact_tam(const kvc_problem* p, const kvc_params* prm,
+                           const void* Q_ref, const void* K, const void* V,
+                           const void* Q_win, int32_t n_win,
+                           const int32_t* seg_bounds, int32_t nseg, float pivot_c,
+                           const int32_t* budgets, const int32_t* offsets,
+                           int32_t* idx_out, void* C_k, float* beta, float* C_v,
+                           int32_t* head_status, int32_t* seg_budgets_out, uint8_t* pivots_out,
+                           void* workspace, size_t workspace_bytes, kvc_stream_t stream);
+
+/* Bytes of workspace kvc_compact_tam needs.  Host-only.  Errors: INVALID_ARG. */
+kvc_status kvc_workspace_size_tam(const kvc_problem* p, const kvc_params* prm, int32_t n_win, int32_t nseg,
+                                  size_t* bytes);
+
 /* Read a compacted cache with a per-key bias (page section 2 objective, and
  * section 5 on use with standard attention kernels):
  *   O_out[h][q] = softmax_i(Q[h][q] . C_k[i] * scale + beta[i]) C_v[i]

@@ -62,8 +62,8 @@ class KvcError(RuntimeError):
 
 _lib = None
 EXPORTS = ("kvc_default_params", "kvc_workspace_size", "kvc_workspace_offset", "kvc_compact",
-           "kvc_compact_noalloc", "kvc_compact_chunked", "kvc_workspace_size_chunked", "kvc_attend",
-           "kvc_stage_times", "kvc_status_string", "kvc_version")
+           "kvc_compact_noalloc", "kvc_compact_chunked", "kvc_workspace_size_chunked", "kvc_compact_tam",
+           "kvc_workspace_size_tam", "kvc_attend", "kvc_stage_times", "kvc_status_string", "kvc_version")
 FLAG_STAGE_TIMING = 1
 FLAG_CHOLESKY_CV = 2
 FLAG_SELECT_OMP = 4
@@ -86,6 +86,9 @@ def lib() -> ctypes.CDLL:
     L.kvc_compact_noalloc.argtypes = [P, PP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.kvc_compact_chunked.argtypes = [P, PP, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.kvc_workspace_size_chunked.argtypes = [P, PP, i32, ctypes.POINTER(sz)]
+    L.kvc_compact_tam.argtypes = [P, PP, vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp,
+                                  vp, vp, vp, sz, vp]
+    L.kvc_workspace_size_tam.argtypes = [P, PP, i32, i32, ctypes.POINTER(sz)]
     L.kvc_attend.argtypes = [P, vp, i32, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp]
     L.kvc_stage_times.argtypes = [ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_float),
                                   ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i32), ctypes.POINTER(i32), i32]
@@ -94,7 +97,8 @@ def lib() -> ctypes.CDLL:
     L.kvc_status_string.restype = ctypes.c_char_p
     L.kvc_version.restype = ctypes.c_char_p
     for f in ("kvc_default_params", "kvc_workspace_size", "kvc_workspace_offset", "kvc_compact",
-              "kvc_compact_noalloc", "kvc_compact_chunked", "kvc_workspace_size_chunked", "kvc_attend"):
+              "kvc_compact_noalloc", "kvc_compact_chunked", "kvc_workspace_size_chunked", "kvc_compact_tam",
+              "kvc_workspace_size_tam", "kvc_attend"):
         getattr(L, f).restype = ctypes.c_int
     _lib = L
     return L
@@ -194,6 +198,27 @@ def compact_chunked(problem: Problem, params: Params | None, chunks: int, Q_ref,
                                      _ptr(Q_ref), _ptr(K), _ptr(V), _ptr(budgets), _ptr(offsets), _ptr(idx_out),
                                      _ptr(C_k), _ptr(beta), _ptr(C_v), _ptr(head_status), _ptr(workspace),
                                      int(workspace_bytes), _stream(stream))
+
+
+def workspace_size_tam(problem: Problem, params: Params | None, n_win: int, nseg: int) -> int:
+    out = ctypes.c_size_t()
+    rc = lib().kvc_workspace_size_tam(ctypes.byref(problem), ctypes.byref(params) if params else None, int(n_win),
+                                      int(nseg), ctypes.byref(out))
+    if rc:
+        raise KvcError(rc, "kvc_workspace_size_tam")
+    return out.value
+
+
+def compact_tam(problem: Problem, params: Params | None, Q_ref, K, V, Q_win, n_win: int, seg_bounds, nseg: int,
+                pivot_c: float, budgets, offsets, idx_out, C_k, beta, C_v, head_status, seg_budgets_out, pivots_out,
+                workspace, workspace_bytes: int, stream=None) -> int:
+    """kvc_compact_tam: thought-aware budgets per segment and exact pivots.
+    Returns the call-level status (0 = enqueued)."""
+    return lib().kvc_compact_tam(ctypes.byref(problem), ctypes.byref(params) if params else None, _ptr(Q_ref),
+                                 _ptr(K), _ptr(V), _ptr(Q_win), int(n_win), _ptr(seg_bounds), int(nseg),
+                                 float(pivot_c), _ptr(budgets), _ptr(offsets), _ptr(idx_out), _ptr(C_k), _ptr(beta),
+                                 _ptr(C_v), _ptr(head_status), _ptr(seg_budgets_out), _ptr(pivots_out),
+                                 _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def attend(problem: Problem, Q, n_q: int, C_k, beta, C_v, offsets, O_out, head_status, scale: float = 0.0,
@@ -310,6 +335,40 @@ def compact_chunked_tensors(Q_ref, K, V, budgets, params: Params | None = None, 
         raise KvcError(rc, "kvc_compact_chunked")
     chunk_prob = make_problem(H * C, n, T // C, d, prob.dtype, max_t)
     return Compacted(idx, Ck, beta, Cv, offsets, status, ws, chunk_prob, prm, C)
+
+
+def compact_tam_tensors(Q_ref, K, V, Q_win, seg_bounds, budgets, pivot_c: float, params: Params | None = None,
+                        stream=None):
+    """Allocate outputs and workspace with torch, then call kvc_compact_tam.
+    seg_bounds: int32 [nseg + 1] on the device.  Returns (Compacted,
+    seg_budgets [H][nseg] int32, pivots [H][T] uint8)."""
+    import torch
+    H, n, d = Q_ref.shape
+    T = K.shape[1]
+    nw = Q_win.shape[1]
+    nseg = seg_bounds.shape[0] - 1
+    dev = Q_ref.device
+    b64 = budgets.to(torch.int64)
+    offsets = torch.zeros(H + 1, dtype=torch.int32, device=dev)
+    offsets[1:] = torch.cumsum(b64, 0).to(torch.int32)
+    total = int(offsets[-1].item())
+    max_t = int(b64.max().item())
+    prob = make_problem(H, n, T, d, torch_dtype_code(Q_ref.dtype), max_t)
+    prm = params if params is not None else default_params()
+    ws_bytes = workspace_size_tam(prob, prm, nw, nseg)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    idx = torch.empty(total, dtype=torch.int32, device=dev)
+    Ck = torch.empty(total, d, dtype=Q_ref.dtype, device=dev)
+    beta = torch.empty(total, dtype=torch.float32, device=dev)
+    Cv = torch.empty(total, d, dtype=torch.float32, device=dev)
+    status = torch.empty(H, dtype=torch.int32, device=dev)
+    segb = torch.empty(H, nseg, dtype=torch.int32, device=dev)
+    piv = torch.empty(H, T, dtype=torch.uint8, device=dev)
+    rc = compact_tam(prob, prm, Q_ref, K, V, Q_win, nw, seg_bounds, nseg, pivot_c, budgets, offsets, idx, Ck, beta,
+                     Cv, status, segb, piv, ws, ws_bytes, stream)
+    if rc:
+        raise KvcError(rc, "kvc_compact_tam")
+    return Compacted(idx, Ck, beta, Cv, offsets, status, ws, prob, prm), segb, piv
 
 
 def workspace_view(c: Compacted, item: int, count: int, dtype):

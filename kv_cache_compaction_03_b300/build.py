@@ -12,7 +12,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libkvc.so")
-SOURCES = ["kvc_api.cu", "tmap.cu", "attn_tc.cu", "gram_tc.cu", "attn_simt.cu", "select.cu", "gram.cu", "linalg.cu", "sweep.cu", "noalloc.cu", "decode.cu", "omp.cu"]
+SOURCES = ["kvc_api.cu", "tmap.cu", "attn_tc.cu", "gram_tc.cu", "attn_simt.cu", "select.cu", "gram.cu", "linalg.cu", "sweep.cu", "noalloc.cu", "decode.cu", "omp.cu", "tam.cu"]
 HEADERS = ["common.cuh", "tc.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

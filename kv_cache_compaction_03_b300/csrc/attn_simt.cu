@@ -156,8 +156,10 @@ __global__ void __launch_bounds__(NT) k_attn_fwd(const TIn* __restrict__ Q, cons
 }
 
 // ---------------------------------------------------------------- key score
-// grid (ceil(T/64), H), block 256.  score [H][T] = sqrt(mean_q P_qj^2).
-template <typename TIn, int D>
+// grid (ceil(T/64), H), block 256.  score [H][T] = sqrt(mean_q P_qj^2), or
+// with MEAN the mean attention mean_q P_qj (the window importance of
+// thought-aware compaction).
+template <typename TIn, int D, bool MEAN = false>
 __global__ void __launch_bounds__(NT) k_colscore(const TIn* __restrict__ Q, const TIn* __restrict__ K,
                                                  const float* __restrict__ lse2, int n, int T, float c2,
                                                  float* __restrict__ score, const int32_t* __restrict__ status,
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(NT) k_colscore(const TIn* __restrict__ Q, cons
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float x = s[i][j] * c2 - Ls[ty * 4 + i];   // log2 of P
-                part += exp2f(x + x);                            // P^2
+                part += MEAN ? exp2f(x) : exp2f(x + x);          // P or P^2
             }
             const float y = part - cmp[j];
             const float tt = acc[j] + y;
@@ -204,7 +206,7 @@ __global__ void __launch_bounds__(NT) k_colscore(const TIn* __restrict__ Q, cons
     if (threadIdx.x < BN && threadIdx.x < kv) {
         double sum = 0.0;
         for (int r = 0; r < 16; ++r) sum += red[r * BN + threadIdx.x];
-        score[(int64_t)h * T + k0 + threadIdx.x] = (float)sqrt(sum / (double)n);
+        score[(int64_t)h * T + k0 + threadIdx.x] = MEAN ? (float)(sum / (double)n) : (float)sqrt(sum / (double)n);
     }
 }
 
@@ -374,6 +376,18 @@ static cudaError_t launch_colscore_simt_t(const void* Q, const void* K, const fl
     return cudaGetLastError();
 }
 template <typename TIn, int D>
+static cudaError_t launch_colmean_simt_t(const void* Q, const void* K, const float* lse2, int H, int n, int T,
+                                         float c2, float* out, const int32_t* status, cudaStream_t st) {
+    constexpr int P = D + 1;
+    size_t smem = (size_t)(BN * P + BM * P + BM) * sizeof(float) + 16 * BN * sizeof(double) + 8;
+    auto kern = k_colscore<TIn, D, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((T + BN - 1) / BN, H);
+    kern<<<grid, NT, smem, st>>>((const TIn*)Q, (const TIn*)K, lse2, n, T, c2, out, status, 1);
+    return cudaGetLastError();
+}
+template <typename TIn, int D>
 static cudaError_t launch_masslogits_t(const void* Q, const void* Ck, const float* lse2, const int32_t* offsets,
                                        int H, int n, int max_t, int64_t ldA, float c2, float* L2,
                                        const int32_t* status, int qdiv, cudaStream_t st) {
@@ -408,6 +422,11 @@ static cudaError_t launch_attend_t(const void* Q, int nq, const void* Ck, const 
 cudaError_t launch_attn_fwd_simt(int dtype, int d, const void* Q, const void* K, const void* V, int H, int n, int T,
                                  float c2, float* O, float* lse2, const int32_t* status, int qdiv, cudaStream_t st) {
     return KVC_DISPATCH(dtype, d, launch_attn_simt_t, Q, K, V, H, n, T, c2, O, lse2, status, qdiv, st);
+}
+// mean_q softmax_j over queries Q (own lse2): out [H][T]
+cudaError_t launch_colmean_simt(int dtype, int d, const void* Q, const void* K, const float* lse2, int H, int n, int T,
+                                float c2, float* out, const int32_t* status, cudaStream_t st) {
+    return KVC_DISPATCH(dtype, d, launch_colmean_simt_t, Q, K, lse2, H, n, T, c2, out, status, st);
 }
 cudaError_t launch_colscore_simt(int dtype, int d, const void* Q, const void* K, const float* lse2, int H, int n,
                                  int T, float c2, float* score, const int32_t* status, int qdiv, cudaStream_t st) {

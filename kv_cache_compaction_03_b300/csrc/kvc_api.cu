@@ -31,6 +31,21 @@ int attend_decode_max_queries();
 size_t omp_workspace_bytes(int H, int n, int T, int max_t);
 size_t omp_order_offset(int H, int n, int T, int max_t);
 int omp_launches(int max_t);
+cudaError_t launch_colmean_simt(int dtype, int d, const void* Q, const void* K, const float* lse2, int H, int n, int T,
+                                float c2, float* out, const int32_t* status, cudaStream_t st);
+int tam_max_segments();
+cudaError_t launch_tam_plan(const float* alpha, int H, int T, const int32_t* bounds, int S, double c,
+                            const int32_t* offsets, uint8_t* pivot, int32_t* seg_bud, int32_t* seg_keep,
+                            int32_t* seg_off, int32_t* status, cudaStream_t st);
+cudaError_t launch_tam_kept(const uint8_t* pivot, int H, int T, int max_t, const int32_t* idx,
+                            const int32_t* offsets, uint8_t* kp, const int32_t* status, cudaStream_t st);
+cudaError_t launch_tam_fix_g(float* G, int64_t ldA, float* f, const uint8_t* kp, const int32_t* offsets, int H,
+                             int max_t, const int32_t* status, cudaStream_t st);
+cudaError_t launch_tam_fix_m(float* M, int64_t ldA, float* R, const float* Vsel, int d, const uint8_t* kp,
+                             const int32_t* offsets, int H, int max_t, const int32_t* status, cudaStream_t st);
+cudaError_t launch_select_seg(const float* score, int H, int T, const int32_t* offsets, const int32_t* bounds,
+                              int nseg, const uint8_t* pivot, const int32_t* seg_keep, const int32_t* seg_off,
+                              int32_t* idx_out, int32_t* status, cudaStream_t st);
 cudaError_t launch_omp_select(int dtype, int d, const void* Q, const void* K, const float* lse2, float c2, int H,
                               int n, int T, int max_t, const int32_t* offsets, int keep_first, int keep_last,
                               void* ws, int32_t* idx_out, int32_t* status, cudaStream_t st);
@@ -56,8 +71,8 @@ cudaError_t launch_cholsolve(int, const float*, const float*, const float*, cons
 cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* offsets, int H, int n, int max_t,
                             int64_t ldA, const float* L2, float* x, float* x0, int8_t* zflag, int32_t* zlist,
                             int32_t* nz, float* S, int32_t* piv, float* u, float* r, float* d0, HeadScalars* hs,
-                            int zmax, int max_iter, int refine_iters, void* rpart_ws, int32_t* status,
-                            cudaStream_t st, int* launches);
+                            int zmax, int max_iter, int refine_iters, void* rpart_ws, const uint8_t* fixed,
+                            int32_t* status, cudaStream_t st, int* launches);
 cudaError_t launch_sweep_inverse(float* A, const int32_t* offsets, int H, int max_t, int64_t ldA, float* U,
                                  void* split, float* P, int32_t* status, cudaStream_t st);
 int sweep_launches(int max_t);
@@ -125,7 +140,9 @@ struct StageClock {
 struct Layout {
     int64_t ldA;
     int zmax;
-    size_t O, lse2, score, L2, Ah, Al, Oh, Ol, bpart, Vsel, Ckw, G, dinv, swV, swP, rpart, b, f, x, x0, d0, u, r, R, zflag, zlist, nz, piv, S, hs, omp, total;
+    size_t O, lse2, score, L2, Ah, Al, Oh, Ol, bpart, Vsel, Ckw, G, dinv, swV, swP, rpart, b, f, x, x0, d0, u, r, R, zflag, zlist, nz, piv, S, hs, omp;
+    size_t tO, tlse, talpha, tkeep, toff, tkp;     // thought-aware planning (n_win > 0)
+    size_t total;
 };
 
 static size_t carve(size_t& cur, size_t bytes) {
@@ -134,7 +151,23 @@ static size_t carve(size_t& cur, size_t bytes) {
     return at;
 }
 
-static Layout make_layout(const kvc_problem& p, const kvc_params& prm) {
+// Window queries and segments of the thought-aware planner; none otherwise.
+struct TamShape {
+    int n_win = 0, nseg = 0;
+};
+
+// Inputs and outputs of the thought-aware planner.
+struct TamInputs {
+    const void* Q_win;          // [H][n_win][d] dtype
+    int n_win;
+    const int32_t* bounds;      // device [nseg + 1]
+    int nseg;
+    double c;
+    int32_t* seg_budgets;       // device [H][nseg]
+    uint8_t* pivots;            // device [H][T]
+};
+
+static Layout make_layout(const kvc_problem& p, const kvc_params& prm, TamShape ts = TamShape{}) {
     Layout L{};
     const size_t H = p.H, n = p.n, T = p.T, d = p.d, mt = p.max_t;
     L.ldA = round_up(p.max_t, 64);
@@ -173,6 +206,14 @@ static Layout make_layout(const kvc_problem& p, const kvc_params& prm) {
     L.hs = carve(c, H * sizeof(HeadScalars));
     // key selection by matching pursuit: the relative mass of every key and the pursuit's state
     L.omp = (prm.flags & KVC_FLAG_SELECT_OMP) ? carve(c, omp_workspace_bytes(p.H, p.n, p.T, p.max_t)) : 0;
+    if (ts.n_win > 0) {
+        L.tO = carve(c, H * (size_t)ts.n_win * d * 4);
+        L.tlse = carve(c, H * (size_t)ts.n_win * 4);
+        L.talpha = carve(c, H * T * 4);
+        L.tkeep = carve(c, H * (size_t)ts.nseg * 4);
+        L.toff = carve(c, H * (size_t)ts.nseg * 4);
+        L.tkp = carve(c, H * mt);
+    }
     L.total = (size_t)round_up((int64_t)c, 256);
     return L;
 }
@@ -275,8 +316,9 @@ namespace kvc {
 static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int chunks, const void* Q_ref,
                                   const void* K, const void* V, const int32_t* budgets, const int32_t* offsets,
                                   int32_t* idx_out, void* C_k, float* beta, float* C_v, int32_t* head_status,
-                                  void* workspace, size_t workspace_bytes, cudaStream_t st) {
-    const Layout L = make_layout(*p, q);
+                                  void* workspace, size_t workspace_bytes, cudaStream_t st,
+                                  const TamInputs* tam = nullptr) {
+    const Layout L = make_layout(*p, q, tam ? TamShape{tam->n_win, tam->nseg} : TamShape{});
     if (!workspace || workspace_bytes < L.total) return KVC_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return KVC_ERR_ALIGN;
 
@@ -313,6 +355,7 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
     // bf16 inputs take the tensor-core passes (tcgen05/TMEM/TMA); fp32 inputs
     // the FFMA passes (a tf32 contraction would not keep fp32 accuracy).
     const bool omp = (q.flags & KVC_FLAG_SELECT_OMP) != 0;
+    uint8_t* kp = tam ? (uint8_t*)(ws + L.tkp) : nullptr;      // kept rows that are pivots
     if (dt == KVC_DTYPE_BF16) {
         KVC_STAGE("attn_fwd", 1, launch_attn_fwd_tc(d, Q_ref, K, V, H, n, T, c2, O, lse2, head_status, qdiv, st));
         if (!omp)
@@ -325,7 +368,23 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
             KVC_STAGE("colscore", 1,
                       launch_colscore_simt(dt, d, Q_ref, K, lse2, H, n, T, c2, score, head_status, qdiv, st));
     }
-    if (omp)
+    if (tam) {
+        float* Ow = (float*)(ws + L.tO);
+        float* lw = (float*)(ws + L.tlse);
+        float* alpha = (float*)(ws + L.talpha);
+        int32_t* skeep = (int32_t*)(ws + L.tkeep);
+        int32_t* soff = (int32_t*)(ws + L.toff);
+        KVC_STAGE("win_attn", 1,
+                  launch_attn_fwd_simt(dt, d, tam->Q_win, K, V, H, tam->n_win, T, c2, Ow, lw, head_status, 1, st));
+        KVC_STAGE("win_alpha", 1,
+                  launch_colmean_simt(dt, d, tam->Q_win, K, lw, H, tam->n_win, T, c2, alpha, head_status, st));
+        KVC_STAGE("tam_plan", 1,
+                  launch_tam_plan(alpha, H, T, tam->bounds, tam->nseg, tam->c, offsets, tam->pivots,
+                                  tam->seg_budgets, skeep, soff, head_status, st));
+        KVC_STAGE("select", 1,
+                  launch_select_seg(score, H, T, offsets, tam->bounds, tam->nseg, tam->pivots, skeep, soff, idx_out,
+                                    head_status, st));
+    } else if (omp)
         KVC_STAGE("omp", omp_launches(mt),
                   launch_omp_select(dt, d, Q_ref, K, lse2, c2, H, n, T, mt, offsets, q.keep_first, q.keep_last,
                                     ws + L.omp, idx_out, head_status, st));
@@ -339,6 +398,7 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
                             head_status, st));
     if (chunks > 1)
         KVC_STAGE("shift_idx", 1, launch_shift_idx(idx_out, offsets, H, T, mt, chunks, head_status, st));
+    if (tam) KVC_STAGE("tam_kept", 1, launch_tam_kept(tam->pivots, H, T, mt, idx_out, offsets, kp, head_status, st));
     if (tc) {
         // the kept keys' per-head copy has ldA rows per head; the map sees H * ldA rows
         KVC_STAGE("masslogits", 1,
@@ -355,13 +415,14 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
     KVC_STAGE("gram_a", 1,
               launch_gram_sym_tc(ws + L.Ah, ws + L.Al, offsets, H, n, mt, L.ldA, G, L.ldA, head_status, st));
     KVC_STAGE("ridge_g", 1, launch_ridge_g(G, b, offsets, H, L.ldA, q.eps_mu, f, hs, head_status, st));
+    if (tam) KVC_STAGE("tam_fix_g", 2, launch_tam_fix_g(G, L.ldA, f, kp, offsets, H, mt, head_status, st));
     KVC_STAGE("inv_h", sweep_launches(mt),
               launch_sweep_inverse(G, offsets, H, mt, L.ldA, dinv, ws + L.swV, (float*)(ws + L.swP),
                                    head_status, st));
     int nnls_launches = 0;
     KVC_STAGE("nnls", nnls_launches,
               launch_nnls_all(G, f, offsets, H, n, mt, L.ldA, L2, x, x0, zflag, zlist, nzv, S, piv, u, r, d0, hs,
-                              L.zmax, q.nnls_max_iter, q.refine_iters, ws + L.rpart, head_status, st,
+                              L.zmax, q.nnls_max_iter, q.refine_iters, ws + L.rpart, kp, head_status, st,
                               &nnls_launches));
     KVC_STAGE("beta", 1, launch_beta_out(x, offsets, H, mt, beta, head_status, st));
     KVC_STAGE("xsoftmax", 1,
@@ -375,6 +436,7 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
               launch_gram_rect_tc(d, ws + L.Ah, ws + L.Al, ws + L.Oh, ws + L.Ol, offsets, H, n, mt, L.ldA, R,
                                   head_status, st));
     KVC_STAGE("ridge_m", 2, launch_ridge_m(d, G, R, Vsel, offsets, H, L.ldA, q.eps_lambda, hs, head_status, st));
+    if (tam) KVC_STAGE("tam_fix_m", 2, launch_tam_fix_m(G, L.ldA, R, Vsel, d, kp, offsets, H, mt, head_status, st));
     if (q.flags & KVC_FLAG_CHOLESKY_CV) {
         KVC_STAGE("chol_m", chol_launches(mt), launch_chol(G, offsets, H, mt, L.ldA, dinv, head_status, st));
         KVC_STAGE("cholsolve", 1, launch_cholsolve(d, G, dinv, R, offsets, H, L.ldA, C_v, head_status, st));
@@ -426,6 +488,45 @@ kvc_status kvc_compact(const kvc_problem* p, const kvc_params* prm, const void* 
     if ((s = check_buffers(Q_ref, K, V, budgets, offsets, idx_out, C_k, beta, C_v, head_status)) != KVC_OK) return s;
     return enqueue_compact(p, q, 1, Q_ref, K, V, budgets, offsets, idx_out, C_k, beta, C_v, head_status, workspace,
                            workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static kvc_status check_tam(const kvc_problem* p, const kvc_params& q, const void* Q_win, int32_t n_win,
+                            const int32_t* bounds, int32_t nseg, float c) {
+    if (!Q_win || !bounds || n_win < 1 || nseg < 1 || nseg > tam_max_segments() || nseg > p->T) return KVC_ERR_INVALID_ARG;
+    if (!(c > 0.f) || !std::isfinite(c)) return KVC_ERR_INVALID_ARG;
+    if (q.keep_first != 0 || q.keep_last != 0 || (q.flags & KVC_FLAG_SELECT_OMP)) return KVC_ERR_INVALID_ARG;
+    if (!aligned(Q_win, 16) || !aligned(bounds, 4)) return KVC_ERR_ALIGN;
+    return KVC_OK;
+}
+
+kvc_status kvc_workspace_size_tam(const kvc_problem* p, const kvc_params* prm, int32_t n_win, int32_t nseg,
+                                  size_t* bytes) {
+    kvc_status s = check_problem(p);
+    if (s != KVC_OK || !bytes || n_win < 1 || nseg < 1 || nseg > tam_max_segments()) return KVC_ERR_INVALID_ARG;
+    kvc_params q;
+    if (prm) q = *prm; else kvc_default_params(&q);
+    if ((s = check_params(q, p->T)) != KVC_OK) return s;
+    *bytes = make_layout(*p, q, TamShape{n_win, nseg}).total;
+    return KVC_OK;
+}
+
+kvc_status kvc_compact_tam(const kvc_problem* p, const kvc_params* prm, const void* Q_ref, const void* K,
+                           const void* V, const void* Q_win, int32_t n_win, const int32_t* seg_bounds, int32_t nseg,
+                           float pivot_c, const int32_t* budgets, const int32_t* offsets, int32_t* idx_out, void* C_k,
+                           float* beta, float* C_v, int32_t* head_status, int32_t* seg_budgets_out,
+                           uint8_t* pivots_out, void* workspace, size_t workspace_bytes, kvc_stream_t stream) {
+    kvc_status s = check_problem(p);
+    if (s != KVC_OK) return s;
+    kvc_params q;
+    if (prm) q = *prm; else kvc_default_params(&q);
+    if ((s = check_params(q, p->T)) != KVC_OK) return s;
+    if ((s = check_tam(p, q, Q_win, n_win, seg_bounds, nseg, pivot_c)) != KVC_OK) return s;
+    if (!seg_budgets_out || !pivots_out) return KVC_ERR_INVALID_ARG;
+    if (!aligned(seg_budgets_out, 4)) return KVC_ERR_ALIGN;
+    if ((s = check_buffers(Q_ref, K, V, budgets, offsets, idx_out, C_k, beta, C_v, head_status)) != KVC_OK) return s;
+    const TamInputs tam{Q_win, n_win, seg_bounds, nseg, (double)pivot_c, seg_budgets_out, pivots_out};
+    return enqueue_compact(p, q, 1, Q_ref, K, V, budgets, offsets, idx_out, C_k, beta, C_v, head_status, workspace,
+                           workspace_bytes, reinterpret_cast<cudaStream_t>(stream), &tam);
 }
 
 kvc_status kvc_workspace_size_chunked(const kvc_problem* p, const kvc_params* prm, int32_t chunks, size_t* bytes) {

@@ -772,6 +772,7 @@ __global__ void __launch_bounds__(256) k_colresid_sum(const dfloat* __restrict__
                                                       const float* __restrict__ x, const int8_t* __restrict__ zflag,
                                                       const int32_t* __restrict__ offsets,
                                                       const HeadScalars* __restrict__ hs, float* __restrict__ r,
+                                                      const uint8_t* __restrict__ fixed,
                                                       const int32_t* __restrict__ status) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
@@ -782,7 +783,8 @@ __global__ void __launch_bounds__(256) k_colresid_sum(const dfloat* __restrict__
     dfloat acc = part[off + c];
     for (int sp = 1; sp < kResidSplit; ++sp) df_add_df(acc, part[(int64_t)sp * part_stride + off + c]);
     df_fma(acc, hs[h].mu, 1.f - x[off + c]);
-    r[off + c] = zflag[off + c] ? 0.f : acc.hi + acc.lo;
+    // weights held fixed (thought-aware pivots) take no refinement step
+    r[off + c] = (zflag[off + c] || (fixed && fixed[off + c])) ? 0.f : acc.hi + acc.lo;
 }
 
 // x += H_FF^{-1} r_F: d0 = H^{-1} r is in `d0`; apply the Schur correction
@@ -890,8 +892,8 @@ cudaError_t launch_symv(const float* Hinv, const float* v, const int32_t* offset
 cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* offsets, int H, int n, int max_t,
                             int64_t ldA, const float* L2, float* x, float* x0, int8_t* zflag, int32_t* zlist,
                             int32_t* nz, float* S, int32_t* piv, float* u, float* r, float* d0, HeadScalars* hs,
-                            int zmax, int max_iter, int refine_iters, void* rpart_ws, int32_t* status,
-                            cudaStream_t st, int* launches) {
+                            int zmax, int max_iter, int refine_iters, void* rpart_ws, const uint8_t* fixed,
+                            int32_t* status, cudaStream_t st, int* launches) {
     dfloat* rpart = static_cast<dfloat*>(rpart_ws);
     const int64_t part_stride = (int64_t)H * max_t;
     BppArgs b{x0, x, zflag, zlist, nz, Hinv, S, piv, offsets, f, ldA, zmax, hs, status};
@@ -913,7 +915,7 @@ cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* of
         k_rowmass<<<dim3((n + 7) / 8, H), 256, 0, st>>>(L2, x, offsets, n, ldA, u, status);
         k_colresid<<<dim3((max_t + 63) / 64, kResidSplit, H), 256, 0, st>>>(L2, u, offsets, n, ldA, part_stride,
                                                                            rpart, status);
-        k_colresid_sum<<<dim3((max_t + 255) / 256, H), 256, 0, st>>>(rpart, part_stride, x, zflag, offsets, hs, r,
+        k_colresid_sum<<<dim3((max_t + 255) / 256, H), 256, 0, st>>>(rpart, part_stride, x, zflag, offsets, hs, r, fixed,
                                                                     status);
         e = launch_symv(Hinv, r, offsets, H, max_t, ldA, d0, nullptr, 0, status, st);
         if (e != cudaSuccess) return e;

@@ -72,40 +72,30 @@ __device__ int block_exclusive_scan(int v, int* sbuf, int* total) {
     return res;
 }
 
-__device__ __forceinline__ uint32_t score_key(const float* sc, int j, int T, int keep_first, int keep_last) {
-    if (j < keep_first || j >= T - keep_last) return 0x7f800000u;          // +inf: forced
-    return __float_as_uint(sc[j]) & 0x7fffffffu;
-}
+// Monotone uint32 key of a non-negative float score; +inf marks a forced key.
+__device__ __forceinline__ uint32_t score_bits(float v) { return __float_as_uint(v) & 0x7fffffffu; }
+constexpr uint32_t kForcedKey = 0x7f800000u;
 
-// ---------------------------------------------------------------- select
-// grid H, block 1024.  idx_out[off .. off+t) = kept positions, ascending.
-// The t-th largest key is found by four 8-bit radix passes over the float
-// bit patterns (monotone for non-negative floats); ties at the threshold go
-// to the lowest positions.
-__global__ void __launch_bounds__(1024) k_select(const float* __restrict__ score, int T, const int32_t* __restrict__ offsets,
-                                                 int chunks, int keep_first, int keep_last,
-                                                 int32_t* __restrict__ idx_out, int32_t* __restrict__ status) {
-    const int h = blockIdx.x;
-    if (!head_ok(status, h)) return;
-    const ForcedRange fr = forced_range(h, T, chunks, keep_first, keep_last);
-    __shared__ int hist[256];
-    __shared__ int sbuf[33];
+// The `keep` largest keys of positions [lo, hi) (key(j) as above), written
+// ascending to out[0 .. keep).  The keep-th largest key is found by four 8-bit
+// radix passes over the key bits; ties at the threshold go to the lowest
+// positions.  Block-wide (1024 threads); returns false if a key is NaN.
+template <typename KeyFn>
+__device__ bool radix_select_range(KeyFn key, int lo, int hi, int keep, int32_t* __restrict__ out, int* hist,
+                                   int* sbuf) {
     __shared__ uint32_t s_digit;
     __shared__ int s_krem, s_nan;
-    const float* sc = score + (int64_t)h * T;
-    const int off = offsets[h];
-    const int t = offsets[h + 1] - off;
     if (threadIdx.x == 0) {
-        s_krem = t;
+        s_krem = keep;
         s_nan = 0;
     }
     uint32_t prefix = 0, pmask = 0;
     for (int shift = 24; shift >= 0; shift -= 8) {
         for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
         __syncthreads();
-        for (int j = threadIdx.x; j < T; j += blockDim.x) {
-            const uint32_t k = score_key(sc, j, T, fr.kf, fr.kl);
-            if (shift == 24 && k > 0x7f800000u) s_nan = 1;
+        for (int j = lo + threadIdx.x; j < hi; j += blockDim.x) {
+            const uint32_t k = key(j);
+            if (shift == 24 && k > kForcedKey) s_nan = 1;
             if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
         }
         __syncthreads();
@@ -127,17 +117,15 @@ __global__ void __launch_bounds__(1024) k_select(const float* __restrict__ score
         prefix |= s_digit << shift;
         pmask |= 255u << shift;
     }
-    if (s_nan) {
-        if (threadIdx.x == 0) set_status(status, h, KVC_ERR_NONFINITE);
-        return;
-    }
+    if (s_nan) return false;
     const uint32_t tau = prefix;
     const int krem = s_krem;                 // keys equal to tau still to take
-    const int chunk = (T + blockDim.x - 1) / blockDim.x;
-    const int j0 = min(T, (int)threadIdx.x * chunk), j1 = min(T, j0 + chunk);
+    const int len = hi - lo;
+    const int chunk = (len + blockDim.x - 1) / blockDim.x;
+    const int j0 = lo + min(len, (int)threadIdx.x * chunk), j1 = min(hi, j0 + chunk);
     int gt = 0, eq = 0;
     for (int j = j0; j < j1; ++j) {
-        const uint32_t k = score_key(sc, j, T, fr.kf, fr.kl);
+        const uint32_t k = key(j);
         gt += k > tau;
         eq += k == tau;
     }
@@ -147,14 +135,62 @@ __global__ void __launch_bounds__(1024) k_select(const float* __restrict__ score
     const int pos0 = block_exclusive_scan(gt + take_eq, sbuf, &tot);
     int pos = pos0, er = eq_before;
     for (int j = j0; j < j1; ++j) {
-        const uint32_t k = score_key(sc, j, T, fr.kf, fr.kl);
+        const uint32_t k = key(j);
         bool take = k > tau;
         if (k == tau) {
             take = er < krem;
             ++er;
         }
-        if (take) idx_out[off + pos++] = j;
+        if (take) out[pos++] = j;
     }
+    return true;
+}
+
+// ---------------------------------------------------------------- select
+// grid H, block 1024.  idx_out[off .. off+t) = kept positions, ascending.
+__global__ void __launch_bounds__(1024) k_select(const float* __restrict__ score, int T, const int32_t* __restrict__ offsets,
+                                                 int chunks, int keep_first, int keep_last,
+                                                 int32_t* __restrict__ idx_out, int32_t* __restrict__ status) {
+    const int h = blockIdx.x;
+    if (!head_ok(status, h)) return;
+    const ForcedRange fr = forced_range(h, T, chunks, keep_first, keep_last);
+    __shared__ int hist[256];
+    __shared__ int sbuf[33];
+    const float* sc = score + (int64_t)h * T;
+    const int off = offsets[h];
+    const int t = offsets[h + 1] - off;
+    auto key = [&](int j) -> uint32_t {
+        return (j < fr.kf || j >= T - fr.kl) ? kForcedKey : score_bits(sc[j]);
+    };
+    if (!radix_select_range(key, 0, T, t, idx_out + off, hist, sbuf) && threadIdx.x == 0)
+        set_status(status, h, KVC_ERR_NONFINITE);
+}
+
+// grid (segments, H), block 1024.  Segment i = positions [bounds[i],
+// bounds[i+1]) keeps its pivots (pivot[h][j] != 0) and its seg_keep[h][i] -
+// pivots highest-scoring other keys, written ascending at
+// idx_out[off + seg_off[h][i] ..]; segments are contiguous, so the head's
+// list is ascending.
+__global__ void __launch_bounds__(1024) k_select_seg(const float* __restrict__ score, int T,
+                                                     const int32_t* __restrict__ offsets,
+                                                     const int32_t* __restrict__ bounds, int nseg,
+                                                     const uint8_t* __restrict__ pivot,
+                                                     const int32_t* __restrict__ seg_keep,
+                                                     const int32_t* __restrict__ seg_off,
+                                                     int32_t* __restrict__ idx_out, int32_t* __restrict__ status) {
+    const int h = blockIdx.y, i = blockIdx.x;
+    if (!head_ok(status, h)) return;
+    __shared__ int hist[256];
+    __shared__ int sbuf[33];
+    const float* sc = score + (int64_t)h * T;
+    const uint8_t* pv = pivot + (int64_t)h * T;
+    const int keep = seg_keep[(int64_t)h * nseg + i];
+    if (keep == 0) return;
+    auto key = [&](int j) -> uint32_t { return pv[j] ? kForcedKey : score_bits(sc[j]); };
+    if (!radix_select_range(key, bounds[i], bounds[i + 1], keep, idx_out + offsets[h] + seg_off[(int64_t)h * nseg + i],
+                            hist, sbuf) &&
+        threadIdx.x == 0)
+        set_status(status, h, KVC_ERR_NONFINITE);
 }
 
 // ---------------------------------------------------------------- gather
@@ -215,6 +251,13 @@ cudaError_t launch_validate(const int32_t* budgets, const int32_t* offsets, int 
 cudaError_t launch_select(const float* score, int H, int T, const int32_t* offsets, int chunks, int keep_first,
                           int keep_last, int32_t* idx_out, int32_t* status, cudaStream_t st) {
     k_select<<<H, 1024, 0, st>>>(score, T, offsets, chunks, keep_first, keep_last, idx_out, status);
+    return cudaGetLastError();
+}
+cudaError_t launch_select_seg(const float* score, int H, int T, const int32_t* offsets, const int32_t* bounds,
+                              int nseg, const uint8_t* pivot, const int32_t* seg_keep, const int32_t* seg_off,
+                              int32_t* idx_out, int32_t* status, cudaStream_t st) {
+    k_select_seg<<<dim3(nseg, H), 1024, 0, st>>>(score, T, offsets, bounds, nseg, pivot, seg_keep, seg_off, idx_out,
+                                                 status);
     return cudaGetLastError();
 }
 cudaError_t launch_shift_idx(int32_t* idx, const int32_t* offsets, int H, int T, int max_t, int chunks,

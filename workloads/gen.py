@@ -30,7 +30,7 @@ import numpy as np
 
 from .configs import Workload
 
-STREAM_CACHE, STREAM_QREF, STREAM_TEST, STREAM_BUDGET = 0, 1, 2, 3
+STREAM_CACHE, STREAM_QREF, STREAM_TEST, STREAM_BUDGET, STREAM_WINDOW = 0, 1, 2, 3, 4
 
 
 def rng_for(w: Workload, h: int, stream: int) -> np.random.Generator:
@@ -206,3 +206,26 @@ def forced_mask(w: Workload) -> np.ndarray:
     if w.keep_last:
         m[w.T - w.keep_last:] = True
     return m
+
+
+# ---------------------------------------------------------------- window
+def segment_bounds(w: Workload) -> np.ndarray:
+    """int32 [S+1]: the segment boundaries the cache was generated with (one
+    segment when the workload has none)."""
+    if not w.segments:
+        return np.array([0, w.T], dtype=np.int32)
+    return np.linspace(0, w.T, w.segments + 1).astype(np.int64).astype(np.int32)
+
+
+def window_queries(w: Workload, h: int, R: int) -> np.ndarray:
+    """Storage-dtype [R][d]: queries of the last R tokens of head h (the
+    selection window of thought-aware compaction), drawn like the reference
+    queries but from positions T - R .. T - 1, rotated at their own positions."""
+    K_pre, _, _, _ = head_cache_f64(w, h)
+    rng = rng_for(w, h, STREAM_WINDOW)
+    j = np.arange(w.T - R, w.T)
+    Q = K_pre[j] + np.sqrt(w.q_noise_var) * rng.standard_normal((R, w.d))
+    if w.rope_theta is not None:
+        Q = rope(Q, j, w.rope_theta)
+    return to_storage(Q, w.dtype)
+
