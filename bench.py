@@ -192,6 +192,8 @@ def time_oracle(w, heads, buds):
 
 
 def config_dict(w, buds, world, select="rms"):
+    if select == "tam":
+        select = f"tam (window {TAM_WINDOW}, c {TAM_C:g}, {max(1, w.segments)} segments, no forced keys)"
     return {"workload": w.name, "heads_per_gpu": w.H, "n": w.n, "T": w.T, "d": w.d, "key_selection": select,
             "t": (w.t if w.t is not None else f"nonuniform mean {float(sum(buds)) / len(buds):.1f}"),
             "input_dtype": w.dtype, "keep_first": w.keep_first, "keep_last": w.keep_last,
@@ -245,6 +247,11 @@ def max_over_ranks(x: float, dist, device) -> float:
     t = torch.tensor([x], device=device, dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+# thought-aware leg (--select tam): window of the last 128 tokens, pivot factor 16
+TAM_WINDOW = 128
+TAM_C = 16.0
 
 
 # --------------------------------------------------------------- decode leg
@@ -344,8 +351,19 @@ def run_ours(args, rank, world, local_rank):
     max_t = int(buds.max())
     prob = kvc.make_problem(w.H, w.n, w.T, w.d, kvc.DTYPE_BF16 if w.dtype == "bf16" else kvc.DTYPE_F32, max_t)
     flags = kvc.FLAG_STAGE_TIMING | (kvc.FLAG_SELECT_OMP if args.select == "omp" else 0)
-    prm = kvc.default_params(keep_first=w.keep_first, keep_last=w.keep_last, flags=flags)
-    ws_bytes = kvc.workspace_size(prob, prm)
+    tam = args.select == "tam"
+    prm = kvc.default_params(keep_first=0 if tam else w.keep_first, keep_last=0 if tam else w.keep_last, flags=flags)
+    if tam:
+        from workloads import segment_bounds, window_queries
+        win = np.stack([window_queries(w, h, TAM_WINDOW) for h in range(w.H)])
+        Qw = dev_tensor(win)
+        seg_bounds = torch.from_numpy(segment_bounds(w)).to(dev)
+        nseg = seg_bounds.numel() - 1
+        seg_out = torch.empty(w.H, nseg, dtype=torch.int32, device=dev)
+        piv_out = torch.empty(w.H, w.T, dtype=torch.uint8, device=dev)
+        ws_bytes = kvc.workspace_size_tam(prob, prm, TAM_WINDOW, nseg)
+    else:
+        ws_bytes = kvc.workspace_size(prob, prm)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     idx = torch.empty(total, dtype=torch.int32, device=dev)
@@ -357,7 +375,11 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        rc = kvc.compact(prob, prm, Q, K, V, b_dev, offsets, idx, Ck, beta, Cv, status, ws, ws_bytes, stream)
+        if tam:
+            rc = kvc.compact_tam(prob, prm, Q, K, V, Qw, TAM_WINDOW, seg_bounds, nseg, TAM_C, b_dev, offsets, idx, Ck,
+                                 beta, Cv, status, seg_out, piv_out, ws, ws_bytes, stream)
+        else:
+            rc = kvc.compact(prob, prm, Q, K, V, b_dev, offsets, idx, Ck, beta, Cv, status, ws, ws_bytes, stream)
         if rc:
             raise kvc.KvcError(rc, "kvc_compact")
 
@@ -513,8 +535,9 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--select", default="rms", choices=["rms", "omp"],
-                    help="key selection: highest RMS attention (default) or orthogonal matching pursuit")
+    ap.add_argument("--select", default="rms", choices=["rms", "omp", "tam"],
+                    help="key selection: highest RMS attention (default), orthogonal matching pursuit, or "
+                         "thought-aware segment budgets with pivots (window of the last 128 tokens, c = 16)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -38,11 +38,14 @@ cudaError_t launch_tam_plan(const float* alpha, int H, int T, const int32_t* bou
                             const int32_t* offsets, uint8_t* pivot, int32_t* seg_bud, int32_t* seg_keep,
                             int32_t* seg_off, int32_t* status, cudaStream_t st);
 cudaError_t launch_tam_kept(const uint8_t* pivot, int H, int T, int max_t, const int32_t* idx,
-                            const int32_t* offsets, uint8_t* kp, const int32_t* status, cudaStream_t st);
-cudaError_t launch_tam_fix_g(float* G, int64_t ldA, float* f, const uint8_t* kp, const int32_t* offsets, int H,
-                             int max_t, const int32_t* status, cudaStream_t st);
+                            const int32_t* offsets, uint8_t* kp, int32_t* plist, int32_t* npk,
+                            const int32_t* status, cudaStream_t st);
+cudaError_t launch_tam_fix_g(float* G, int64_t ldA, float* f, const uint8_t* kp, const int32_t* plist,
+                             const int32_t* npk, const int32_t* offsets, int H, int max_t, const int32_t* status,
+                             cudaStream_t st);
 cudaError_t launch_tam_fix_m(float* M, int64_t ldA, float* R, const float* Vsel, int d, const uint8_t* kp,
-                             const int32_t* offsets, int H, int max_t, const int32_t* status, cudaStream_t st);
+                             const int32_t* plist, const int32_t* npk, const int32_t* offsets, int H, int max_t,
+                             const int32_t* status, cudaStream_t st);
 cudaError_t launch_select_seg(const float* score, int H, int T, const int32_t* offsets, const int32_t* bounds,
                               int nseg, const uint8_t* pivot, const int32_t* seg_keep, const int32_t* seg_off,
                               int32_t* idx_out, int32_t* status, cudaStream_t st);
@@ -141,7 +144,7 @@ struct Layout {
     int64_t ldA;
     int zmax;
     size_t O, lse2, score, L2, Ah, Al, Oh, Ol, bpart, Vsel, Ckw, G, dinv, swV, swP, rpart, b, f, x, x0, d0, u, r, R, zflag, zlist, nz, piv, S, hs, omp;
-    size_t tO, tlse, talpha, tkeep, toff, tkp;     // thought-aware planning (n_win > 0)
+    size_t tO, tlse, talpha, tkeep, toff, tkp, tpl, tnp;     // thought-aware planning (n_win > 0)
     size_t total;
 };
 
@@ -213,6 +216,8 @@ static Layout make_layout(const kvc_problem& p, const kvc_params& prm, TamShape 
         L.tkeep = carve(c, H * (size_t)ts.nseg * 4);
         L.toff = carve(c, H * (size_t)ts.nseg * 4);
         L.tkp = carve(c, H * mt);
+        L.tpl = carve(c, H * mt * 4);
+        L.tnp = carve(c, H * 4);
     }
     L.total = (size_t)round_up((int64_t)c, 256);
     return L;
@@ -374,8 +379,14 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
         float* alpha = (float*)(ws + L.talpha);
         int32_t* skeep = (int32_t*)(ws + L.tkeep);
         int32_t* soff = (int32_t*)(ws + L.toff);
-        KVC_STAGE("win_attn", 1,
-                  launch_attn_fwd_simt(dt, d, tam->Q_win, K, V, H, tam->n_win, T, c2, Ow, lw, head_status, 1, st));
+        // (the tensor-core pass tiles queries by 128; shorter windows take the FFMA pass)
+        if (dt == KVC_DTYPE_BF16 && tam->n_win >= 128)
+            KVC_STAGE("win_attn", 1,
+                      launch_attn_fwd_tc(d, tam->Q_win, K, V, H, tam->n_win, T, c2, Ow, lw, head_status, 1, st));
+        else
+            KVC_STAGE("win_attn", 1,
+                      launch_attn_fwd_simt(dt, d, tam->Q_win, K, V, H, tam->n_win, T, c2, Ow, lw, head_status, 1,
+                                           st));
         KVC_STAGE("win_alpha", 1,
                   launch_colmean_simt(dt, d, tam->Q_win, K, lw, H, tam->n_win, T, c2, alpha, head_status, st));
         KVC_STAGE("tam_plan", 1,
@@ -398,7 +409,11 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
                             head_status, st));
     if (chunks > 1)
         KVC_STAGE("shift_idx", 1, launch_shift_idx(idx_out, offsets, H, T, mt, chunks, head_status, st));
-    if (tam) KVC_STAGE("tam_kept", 1, launch_tam_kept(tam->pivots, H, T, mt, idx_out, offsets, kp, head_status, st));
+    int32_t* plist = tam ? (int32_t*)(ws + L.tpl) : nullptr;   // kept pivot rows, per head
+    int32_t* npk = tam ? (int32_t*)(ws + L.tnp) : nullptr;
+    if (tam)
+        KVC_STAGE("tam_kept", 1,
+                  launch_tam_kept(tam->pivots, H, T, mt, idx_out, offsets, kp, plist, npk, head_status, st));
     if (tc) {
         // the kept keys' per-head copy has ldA rows per head; the map sees H * ldA rows
         KVC_STAGE("masslogits", 1,
@@ -415,7 +430,8 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
     KVC_STAGE("gram_a", 1,
               launch_gram_sym_tc(ws + L.Ah, ws + L.Al, offsets, H, n, mt, L.ldA, G, L.ldA, head_status, st));
     KVC_STAGE("ridge_g", 1, launch_ridge_g(G, b, offsets, H, L.ldA, q.eps_mu, f, hs, head_status, st));
-    if (tam) KVC_STAGE("tam_fix_g", 2, launch_tam_fix_g(G, L.ldA, f, kp, offsets, H, mt, head_status, st));
+    if (tam)
+        KVC_STAGE("tam_fix_g", 2, launch_tam_fix_g(G, L.ldA, f, kp, plist, npk, offsets, H, mt, head_status, st));
     KVC_STAGE("inv_h", sweep_launches(mt),
               launch_sweep_inverse(G, offsets, H, mt, L.ldA, dinv, ws + L.swV, (float*)(ws + L.swP),
                                    head_status, st));
@@ -436,7 +452,9 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
               launch_gram_rect_tc(d, ws + L.Ah, ws + L.Al, ws + L.Oh, ws + L.Ol, offsets, H, n, mt, L.ldA, R,
                                   head_status, st));
     KVC_STAGE("ridge_m", 2, launch_ridge_m(d, G, R, Vsel, offsets, H, L.ldA, q.eps_lambda, hs, head_status, st));
-    if (tam) KVC_STAGE("tam_fix_m", 2, launch_tam_fix_m(G, L.ldA, R, Vsel, d, kp, offsets, H, mt, head_status, st));
+    if (tam)
+        KVC_STAGE("tam_fix_m", 2,
+                  launch_tam_fix_m(G, L.ldA, R, Vsel, d, kp, plist, npk, offsets, H, mt, head_status, st));
     if (q.flags & KVC_FLAG_CHOLESKY_CV) {
         KVC_STAGE("chol_m", chol_launches(mt), launch_chol(G, offsets, H, mt, L.ldA, dinv, head_status, st));
         KVC_STAGE("cholsolve", 1, launch_cholsolve(d, G, dinv, R, offsets, H, L.ldA, C_v, head_status, st));

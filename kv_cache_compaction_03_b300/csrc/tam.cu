@@ -185,21 +185,47 @@ __global__ void __launch_bounds__(1024) k_tam_plan(const float* __restrict__ alp
     }
 }
 
-// grid (ceil(max_t/256), H): kp[off + i] = pivot[h][idx[off + i]].
-__global__ void k_tam_kept(const uint8_t* __restrict__ pivot, int T, const int32_t* __restrict__ idx,
-                           const int32_t* __restrict__ offsets, uint8_t* __restrict__ kp,
-                           const int32_t* __restrict__ status) {
-    const int h = blockIdx.y;
+// grid H, block 1024: kp[off + i] = pivot[h][idx[off + i]], and the kept
+// rows that are pivots listed in ascending order: plist[off ..], count npk[h].
+__global__ void __launch_bounds__(1024) k_tam_kept(const uint8_t* __restrict__ pivot, int T,
+                                                   const int32_t* __restrict__ idx,
+                                                   const int32_t* __restrict__ offsets, uint8_t* __restrict__ kp,
+                                                   int32_t* __restrict__ plist, int32_t* __restrict__ npk,
+                                                   const int32_t* __restrict__ status) {
+    const int h = blockIdx.x;
     if (!head_ok(status, h)) return;
+    __shared__ int wsum[32];
+    __shared__ int base;
     const int off = offsets[h];
     const int t = offsets[h + 1] - off;
-    const int i = blockIdx.x * 256 + threadIdx.x;
-    if (i < t) kp[off + i] = pivot[(int64_t)h * T + idx[off + i]];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) base = 0;
+    __syncthreads();
+    for (int i0 = 0; i0 < t; i0 += 1024) {
+        const int i = i0 + threadIdx.x;
+        const int f = (i < t) ? pivot[(int64_t)h * T + idx[off + i]] : 0;
+        if (i < t) kp[off + i] = (uint8_t)f;
+        const unsigned m = __ballot_sync(0xffffffffu, f);
+        if (lane == 0) wsum[warp] = __popc(m);
+        __syncthreads();
+        int before = 0;
+        for (int w = 0; w < warp; ++w) before += wsum[w];
+        if (f) plist[off + base + before + __popc(m & ((1u << lane) - 1u))] = i;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int tot = 0;
+            for (int w = 0; w < 32; ++w) tot += wsum[w];
+            base += tot;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) npk[h] = base;
 }
 
 // grid (ceil(max_t/256), H), block 256: f_i -= sum_p G_ip over the kept pivots p; f_p = 1.
 __global__ void k_tam_rhs_g(const float* __restrict__ G, int64_t ldA, float* __restrict__ f,
-                            const uint8_t* __restrict__ kp, const int32_t* __restrict__ offsets,
+                            const uint8_t* __restrict__ kp, const int32_t* __restrict__ plist,
+                            const int32_t* __restrict__ npk, const int32_t* __restrict__ offsets,
                             const int32_t* __restrict__ status) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
@@ -213,8 +239,7 @@ __global__ void k_tam_rhs_g(const float* __restrict__ G, int64_t ldA, float* __r
     }
     const float* row = G + ((int64_t)h * ldA + i) * ldA;
     double acc = 0.0;
-    for (int p = 0; p < t; ++p)
-        if (kp[off + p]) acc += (double)row[p];
+    for (int k = 0; k < npk[h]; ++k) acc += (double)row[plist[off + k]];
     f[off + i] -= (float)acc;
 }
 
@@ -222,6 +247,7 @@ __global__ void k_tam_rhs_g(const float* __restrict__ G, int64_t ldA, float* __r
 // R_i -= sum_p M_ip V_p over the kept pivots p.
 __global__ void k_tam_rhs_m(const float* __restrict__ M, int64_t ldA, float* __restrict__ R,
                             const float* __restrict__ Vsel, int d, const uint8_t* __restrict__ kp,
+                            const int32_t* __restrict__ plist, const int32_t* __restrict__ npk,
                             const int32_t* __restrict__ offsets, const int32_t* __restrict__ status) {
     const int h = blockIdx.y, i = blockIdx.x;
     if (!head_ok(status, h)) return;
@@ -235,13 +261,16 @@ __global__ void k_tam_rhs_m(const float* __restrict__ M, int64_t ldA, float* __r
     }
     const float* row = M + ((int64_t)h * ldA + i) * ldA;
     float acc = 0.f;
-    for (int p = 0; p < t; ++p)
-        if (kp[off + p]) acc = fmaf(row[p], Vsel[((int64_t)off + p) * d + c], acc);
+    for (int k = 0; k < npk[h]; ++k) {
+        const int p = plist[off + k];
+        acc = fmaf(row[p], Vsel[((int64_t)off + p) * d + c], acc);
+    }
     R[((int64_t)off + i) * d + c] -= acc;
 }
 
 // grid (ceil(max_t/256), H), block 256: pivot rows and columns -> identity.
 __global__ void k_tam_pin(float* __restrict__ A, int64_t ldA, const uint8_t* __restrict__ kp,
+                          const int32_t* __restrict__ plist, const int32_t* __restrict__ npk,
                           const int32_t* __restrict__ offsets, const int32_t* __restrict__ status) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
@@ -253,8 +282,7 @@ __global__ void k_tam_pin(float* __restrict__ A, int64_t ldA, const uint8_t* __r
     if (kp[off + i]) {
         for (int j = 0; j < t; ++j) row[j] = (j == i) ? 1.f : 0.f;
     } else {
-        for (int p = 0; p < t; ++p)
-            if (kp[off + p]) row[p] = 0.f;
+        for (int k = 0; k < npk[h]; ++k) row[plist[off + k]] = 0.f;
     }
 }
 
@@ -268,24 +296,29 @@ cudaError_t launch_tam_plan(const float* alpha, int H, int T, const int32_t* bou
     k_tam_plan<<<H, 1024, 0, st>>>(alpha, T, bounds, S, c, offsets, pivot, seg_bud, seg_keep, seg_off, status);
     return cudaGetLastError();
 }
+// kp: uint8 [sum t]; plist: int32 [sum t] then npk: int32 [H] (one scratch block)
 cudaError_t launch_tam_kept(const uint8_t* pivot, int H, int T, int max_t, const int32_t* idx,
-                            const int32_t* offsets, uint8_t* kp, const int32_t* status, cudaStream_t st) {
-    k_tam_kept<<<dim3((max_t + 255) / 256, H), 256, 0, st>>>(pivot, T, idx, offsets, kp, status);
+                            const int32_t* offsets, uint8_t* kp, int32_t* plist, int32_t* npk,
+                            const int32_t* status, cudaStream_t st) {
+    (void)max_t;
+    k_tam_kept<<<H, 1024, 0, st>>>(pivot, T, idx, offsets, kp, plist, npk, status);
     return cudaGetLastError();
 }
 // G, f after the ridge: pivots held at w = 1
-cudaError_t launch_tam_fix_g(float* G, int64_t ldA, float* f, const uint8_t* kp, const int32_t* offsets, int H,
-                             int max_t, const int32_t* status, cudaStream_t st) {
+cudaError_t launch_tam_fix_g(float* G, int64_t ldA, float* f, const uint8_t* kp, const int32_t* plist,
+                             const int32_t* npk, const int32_t* offsets, int H, int max_t, const int32_t* status,
+                             cudaStream_t st) {
     dim3 grid((max_t + 255) / 256, H);
-    k_tam_rhs_g<<<grid, 256, 0, st>>>(G, ldA, f, kp, offsets, status);
-    k_tam_pin<<<grid, 256, 0, st>>>(G, ldA, kp, offsets, status);
+    k_tam_rhs_g<<<grid, 256, 0, st>>>(G, ldA, f, kp, plist, npk, offsets, status);
+    k_tam_pin<<<grid, 256, 0, st>>>(G, ldA, kp, plist, npk, offsets, status);
     return cudaGetLastError();
 }
 // M, R after the ridge: pivot rows of C_v held at V
 cudaError_t launch_tam_fix_m(float* M, int64_t ldA, float* R, const float* Vsel, int d, const uint8_t* kp,
-                             const int32_t* offsets, int H, int max_t, const int32_t* status, cudaStream_t st) {
-    k_tam_rhs_m<<<dim3(max_t, H), d, 0, st>>>(M, ldA, R, Vsel, d, kp, offsets, status);
-    k_tam_pin<<<dim3((max_t + 255) / 256, H), 256, 0, st>>>(M, ldA, kp, offsets, status);
+                             const int32_t* plist, const int32_t* npk, const int32_t* offsets, int H, int max_t,
+                             const int32_t* status, cudaStream_t st) {
+    k_tam_rhs_m<<<dim3(max_t, H), d, 0, st>>>(M, ldA, R, Vsel, d, kp, plist, npk, offsets, status);
+    k_tam_pin<<<dim3((max_t + 255) / 256, H), 256, 0, st>>>(M, ldA, kp, plist, npk, offsets, status);
     return cudaGetLastError();
 }
 

@@ -108,6 +108,12 @@ def test_tam_bf16_d64_no_pivots_one_budget_each():
     assert _check(w, [90, 77], R=16, c=1e6) == 0
 
 
+def test_tam_bf16_window_on_tensor_cores():
+    """A window of 128 queries takes the tensor-core attention pass."""
+    w = small_variant(WORKLOADS[4], H=2, n=256, T=1024)
+    _check(w, [150, 130], R=128, c=8.0)
+
+
 def test_tam_fp32():
     w = small_variant(WORKLOADS[4], H=2, n=128, T=512, dtype="f32")
     _check(w, [60, 64], R=16, c=2.0)
