@@ -140,9 +140,10 @@ MUFU_PEAK_TEXP = 148 * 16 * 2.032e9 / 1e12
 def tensor_stages(w) -> set[str]:
     """Stages that run on the tensor cores (bf16 operands, fp32 accumulation)
     for this workload; the others run on the CUDA cores (fp32 FFMA) or are
-    memory-bound.  The Gram products run on the tensor cores for every input
-    dtype (their fp32 operands are split into two bf16 terms)."""
-    grams = {"gram_a", "gram_x", "xto"}
+    memory-bound.  The Gram products and C_v = M^{-1} R run on the tensor
+    cores for every input dtype (their fp32 operands are split into bf16
+    terms)."""
+    grams = {"gram_a", "gram_x", "xto", "apply_minv"}
     return grams | ({"attn_fwd", "colscore", "masslogits"} if w.dtype == "bf16" else set())
 
 

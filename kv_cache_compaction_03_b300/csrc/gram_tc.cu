@@ -269,6 +269,191 @@ __global__ void k_colsum_total(const float* __restrict__ colsum, int ntiles, int
     b[off + c] = (float)v;
 }
 
+// ---------------------------------------------------------------- C_v = M^{-1} R
+// The least-squares values from the explicit inverse of M (symmetric, so
+// C[i][c] = sum_p Minv[p][i] R[p][c]), on the tensor cores with both operands
+// as three exact bf16 terms (hi + mid + lo = the fp32 value) and the six
+// products hi.hi, hi.mid, mid.hi, hi.lo, lo.hi, mid.mid: the dropped products
+// are below 2^-25 of |m||r|, under fp32 rounding, which an inverse with a
+// large condition number needs.  The contraction runs over each head's own
+// t_h rows (64 per stage, two stages); rows past t_h are zero in the split
+// arrays.
+
+__device__ __forceinline__ void split3(float x, __nv_bfloat16& hi, __nv_bfloat16& mid, __nv_bfloat16& lo) {
+    hi = __float2bfloat16_rn(x);
+    const float r1 = x - __bfloat162float(hi);
+    mid = __float2bfloat16_rn(r1);
+    lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+}
+
+// grid (ceil(ldA/256), ldA, H): Minv rows/columns < t_h -> [3][H][ldA][ldA], 0 elsewhere.
+__global__ void k_split3_square(const float* __restrict__ Minv, int64_t ldA, const int32_t* __restrict__ offsets,
+                                __nv_bfloat16* __restrict__ out, int64_t ts, const int32_t* __restrict__ status) {
+    const int h = blockIdx.z;
+    if (!head_ok(status, h)) return;
+    const int t = offsets[h + 1] - offsets[h];
+    const int r = blockIdx.y, c = blockIdx.x * 256 + threadIdx.x;
+    if (c >= ldA) return;
+    const int64_t e = ((int64_t)h * ldA + r) * ldA + c;
+    const float x = (r < t && c < t) ? Minv[e] : 0.f;
+    __nv_bfloat16 a, b, d;
+    split3(x, a, b, d);
+    out[e] = a;
+    out[ts + e] = b;
+    out[2 * ts + e] = d;
+}
+
+// grid (ldA, H), block d: R [sum t][d] -> [3][H][ldA][d], rows past t_h zero.
+__global__ void k_split3_rows(const float* __restrict__ R, int d, int64_t ldA, const int32_t* __restrict__ offsets,
+                              __nv_bfloat16* __restrict__ out, int64_t ts, const int32_t* __restrict__ status) {
+    const int h = blockIdx.y, r = blockIdx.x, c = threadIdx.x;
+    if (!head_ok(status, h)) return;
+    const int off = offsets[h];
+    const int t = offsets[h + 1] - off;
+    const float x = r < t ? R[((int64_t)off + r) * d + c] : 0.f;
+    const int64_t e = ((int64_t)h * ldA + r) * d + c;
+    __nv_bfloat16 a, b, dd;
+    split3(x, a, b, dd);
+    out[e] = a;
+    out[ts + e] = b;
+    out[2 * ts + e] = dd;
+}
+
+constexpr int kApStages = 2;
+
+template <int NB>
+__host__ __device__ constexpr int apply3_stage() {
+    return 3 * 2 * kGBox + 3 * (NB / 64) * kGBox;
+}
+template <int NB>
+__host__ __device__ constexpr int apply3_smem() {
+    return kApStages * apply3_stage<NB>() + 256 + 1024;
+}
+
+// grid (ceil(max_t/128), H), block 192: rows 128 I .. of C_v for head h.
+// Warp 0 TMA, warp 1 MMA and TMEM owner, warps 2..5 epilogue (lane = row).
+template <int NB>
+__global__ void __launch_bounds__(kGThreads, 1)
+    k_apply3_tc(const __grid_constant__ CUtensorMap mM0, const __grid_constant__ CUtensorMap mM1,
+                const __grid_constant__ CUtensorMap mM2, const __grid_constant__ CUtensorMap mR0,
+                const __grid_constant__ CUtensorMap mR1, const __grid_constant__ CUtensorMap mR2,
+                const int32_t* __restrict__ offsets, float* __restrict__ C, int32_t* __restrict__ status) {
+    const int h = blockIdx.y;
+    if (!head_ok(status, h)) return;
+    const int off = offsets[h];
+    const int t = offsets[h + 1] - off;
+    const int I = blockIdx.x;
+    if (I * GB >= t) return;
+    constexpr int kA = 2 * kGBox;                 // one 128-column term of Minv
+    constexpr int kB = (NB / 64) * kGBox;         // one term of R
+    constexpr int kStage = apply3_stage<NB>();
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024g(smem_raw);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kApStages * kStage);
+    uint64_t* full = bars;
+    uint64_t* empty = full + kApStages;
+    uint64_t* acc_full = empty + kApStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kApStages; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, NB < 32 ? 32 : NB);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int nk = (t + GK - 1) / GK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const CUtensorMap* mm[3] = {&mM0, &mM1, &mM2};
+            const CUtensorMap* mr[3] = {&mR0, &mR1, &mR2};
+            int issued = 0;
+            for (int k = 0; k < nk; ++k) {
+                const int s = k % kApStages;
+                if (k >= kApStages && !mbar_wait(empty + s, (uint32_t)((k / kApStages) - 1) & 1u, abort_flag)) break;
+                uint8_t* st = sm + s * kStage;
+                mbar_expect_tx(full + s, (uint32_t)kStage);
+#pragma unroll
+                for (int q = 0; q < 3; ++q) {
+#pragma unroll
+                    for (int b = 0; b < 2; ++b)
+                        tma_load_3d(st + q * kA + b * kGBox, mm[q], full + s, I * GB + 64 * b, k * GK, h);
+#pragma unroll
+                    for (int b = 0; b < NB / 64; ++b)
+                        tma_load_3d(st + 3 * kA + q * kB + b * kGBox, mr[q], full + s, 64 * b, k * GK, h);
+                }
+                issued = k + 1;
+            }
+            for (int k = (issued > kApStages ? issued - kApStages : 0); k < issued; ++k)
+                drain(full + k % kApStages, (uint32_t)(k / kApStages) & 1u);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(128, NB, true, true);
+            // (Minv term, R term) pairs, smallest products first
+            constexpr int pa[6] = {2, 0, 1, 1, 0, 0};
+            constexpr int pb[6] = {0, 2, 1, 0, 1, 0};
+            for (int k = 0; k < nk; ++k) {
+                const int s = k % kApStages;
+                if (!mbar_wait(full + s, (uint32_t)(k / kApStages) & 1u, abort_flag)) break;
+                fence_after_sync();
+                const uint32_t st = smem_addr(sm + s * kStage);
+#pragma unroll
+                for (int kk = 0; kk < GK / 16; ++kk) {
+                    const uint32_t o = (uint32_t)kk * 2048;
+#pragma unroll
+                    for (int m = 0; m < 6; ++m) {
+                        const uint64_t da = sdesc_sw128(st + pa[m] * kA + o, kGBox, 1024);
+                        const uint64_t db = sdesc_sw128(st + 3 * kA + pb[m] * kB + o, kGBox, 1024);
+                        mma_ss(tmem, da, db, idesc, (k > 0 || kk > 0 || m > 0) ? 1u : 0u);
+                    }
+                }
+                mma_commit(empty + s);
+            }
+            mma_commit(acc_full);
+            drain(acc_full, 0);
+        }
+        __syncwarp();
+    } else {
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag));
+        if (ok) {
+            fence_after_sync();
+            const int quarter = warp & 3;
+            const int i = I * GB + quarter * 32 + lane;
+            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+#pragma unroll 1
+            for (int c = 0; c < NB / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + c * 32, r);
+                tmem_ld_wait();
+                if (i < t) {
+                    float* dst = C + ((int64_t)off + i) * NB + c * 32;
+#pragma unroll
+                    for (int q = 0; q < 32; q += 4)
+                        *reinterpret_cast<float4*>(dst + q) =
+                            make_float4(__uint_as_float(r[q]), __uint_as_float(r[q + 1]), __uint_as_float(r[q + 2]),
+                                        __uint_as_float(r[q + 3]));
+                }
+            }
+        }
+    }
+    if (threadIdx.x == 0 && *abort_flag) set_status(status, h, KVC_ERR_TIMEOUT);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (warp == 1) tmem_dealloc(tmem, NB < 32 ? 32 : NB);
+}
+
 }  // namespace
 
 bool make_map_bf16(CUtensorMap* m, const void* base, int cols, int64_t ld, int rows, int H);   // tmap.cu
@@ -334,4 +519,39 @@ cudaError_t launch_split_hilo(bool exp_mode, const float* X, int H, int rows, in
     return cudaGetLastError();
 }
 
+// C [sum t][d] = M^{-1} R on the tensor cores.  Minv: fp32 [H][ldA][ldA]
+// (rows / columns < t_h valid); R: fp32 [sum t][d]; split: scratch of
+// 6 * H * ldA * (ldA + d) bytes (the bf16 terms of both operands).
+size_t apply_inverse_tc_scratch(int H, int64_t ldA, int d) { return (size_t)6 * H * ldA * (ldA + d); }
+
+cudaError_t launch_apply_inverse_tc(int d, const float* Minv, const float* R, const int32_t* offsets, int H,
+                                    int max_t, int64_t ldA, void* split, float* C, int32_t* status, cudaStream_t st) {
+    __nv_bfloat16* Ms = static_cast<__nv_bfloat16*>(split);
+    const int64_t tsm = (int64_t)H * ldA * ldA;
+    __nv_bfloat16* Rs = Ms + 3 * tsm;
+    const int64_t tsr = (int64_t)H * ldA * d;
+    k_split3_square<<<dim3((unsigned)((ldA + 255) / 256), (unsigned)ldA, H), 256, 0, st>>>(Minv, ldA, offsets, Ms, tsm,
+                                                                                         status);
+    k_split3_rows<<<dim3((unsigned)ldA, H), d, 0, st>>>(R, d, ldA, offsets, Rs, tsr, status);
+    CUtensorMap mm[3], mr[3];
+    for (int q = 0; q < 3; ++q)
+        if (!make_map_bf16(&mm[q], Ms + q * tsm, (int)ldA, ldA, (int)ldA, H) ||
+            !make_map_bf16(&mr[q], Rs + q * tsr, d, d, (int)ldA, H))
+            return cudaErrorInvalidValue;
+    dim3 grid((max_t + GB - 1) / GB, H);
+    if (d == 128) {
+        constexpr int smem = apply3_smem<128>();
+        cudaError_t e = cudaFuncSetAttribute(k_apply3_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        k_apply3_tc<128><<<grid, kGThreads, smem, st>>>(mm[0], mm[1], mm[2], mr[0], mr[1], mr[2], offsets, C, status);
+    } else {
+        constexpr int smem = apply3_smem<64>();
+        cudaError_t e = cudaFuncSetAttribute(k_apply3_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        k_apply3_tc<64><<<grid, kGThreads, smem, st>>>(mm[0], mm[1], mm[2], mr[0], mr[1], mr[2], offsets, C, status);
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace kvc
+

@@ -79,8 +79,9 @@ cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* of
 cudaError_t launch_sweep_inverse(float* A, const int32_t* offsets, int H, int max_t, int64_t ldA, float* U,
                                  void* split, float* P, int32_t* status, cudaStream_t st);
 int sweep_launches(int max_t);
-cudaError_t launch_apply_inverse(int d, const float* Minv, const float* R, const int32_t* offsets, int H, int max_t,
-                                 int64_t ldA, float* C, const int32_t* status, cudaStream_t st);
+size_t apply_inverse_tc_scratch(int H, int64_t ldA, int d);
+cudaError_t launch_apply_inverse_tc(int d, const float* Minv, const float* R, const int32_t* offsets, int H,
+                                    int max_t, int64_t ldA, void* split, float* C, int32_t* status, cudaStream_t st);
 cudaError_t launch_attn_fwd_tc(int d, const void* Q, const void* K, const void* V, int H, int n, int T, float c2,
                                float* O, float* lse2, int32_t* status, int qdiv, cudaStream_t st);
 cudaError_t launch_colscore_tc(int d, const void* Q, const void* K, const float* lse2, int H, int n, int T,
@@ -144,6 +145,7 @@ struct Layout {
     int64_t ldA;
     int zmax;
     size_t O, lse2, score, L2, Ah, Al, Oh, Ol, bpart, Vsel, Ckw, G, dinv, swV, swP, rpart, b, f, x, x0, d0, u, r, R, zflag, zlist, nz, piv, S, hs, omp;
+    size_t msplit;                                 // bf16 terms of M^{-1} and R for the C_v product
     size_t tO, tlse, talpha, tkeep, toff, tkp, tpl, tnp;     // thought-aware planning (n_win > 0)
     size_t total;
 };
@@ -207,6 +209,13 @@ static Layout make_layout(const kvc_problem& p, const kvc_params& prm, TamShape 
     L.piv = carve(c, H * 16);
     L.S = carve(c, H * zm * zm * 4);
     L.hs = carve(c, H * sizeof(HeadScalars));
+    // the terms of M^{-1} and R are needed only after the last reader of the
+    // mass logits and the A' / X terms: they share that span when it is large enough
+    {
+        const size_t need = apply_inverse_tc_scratch((int)H, (int64_t)ldA, (int)d);
+        const size_t span = L.Al + H * n * ldA * 2 - L.L2;
+        L.msplit = need <= span ? L.L2 : carve(c, need);
+    }
     // key selection by matching pursuit: the relative mass of every key and the pursuit's state
     L.omp = (prm.flags & KVC_FLAG_SELECT_OMP) ? carve(c, omp_workspace_bytes(p.H, p.n, p.T, p.max_t)) : 0;
     if (ts.n_win > 0) {
@@ -462,7 +471,8 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
         KVC_STAGE("inv_m", sweep_launches(mt),
                   launch_sweep_inverse(G, offsets, H, mt, L.ldA, dinv, ws + L.swV, (float*)(ws + L.swP),
                                        head_status, st));
-        KVC_STAGE("apply_minv", 1, launch_apply_inverse(d, G, R, offsets, H, mt, L.ldA, C_v, head_status, st));
+        KVC_STAGE("apply_minv", 3,
+                  launch_apply_inverse_tc(d, G, R, offsets, H, mt, L.ldA, ws + L.msplit, C_v, head_status, st));
     }
     clk.finish();
     return KVC_OK;

@@ -24,8 +24,6 @@
 //                   is negated, so the matrix ends as +H^{-1}
 //   k_sweep_mirror  copies the lower triangle into the upper one
 //   k_symv          y = H^{-1} v for every head (one warp per row)
-//   k_apply_inverse C_v = M^{-1} R (the least-squares fit of C_v when M is
-//                   inverted by the same sweeps)
 // The sweep keeps the symmetric matrix in its lower triangle (row-major,
 // leading dimension ldA); an entry above the diagonal is read from its
 // mirror image.  The finished inverse is stored in full.
@@ -506,62 +504,6 @@ __global__ void __launch_bounds__(256) k_symv(const float* __restrict__ Hinv, co
     if (lane == 0) y[off + r] = s;
 }
 
-// C[off + i][c] = sum_j Minv[i][j] R[off + j][c] (C_v from the explicit
-// inverse).  grid (ceil(max_t / 64), H), block 256: a CTA computes 64 rows x
-// D columns, each thread 4 rows x D/16 columns, in 64-column steps of j.
-template <int D>
-__global__ void __launch_bounds__(256) k_apply_inverse(const float* __restrict__ Minv, const float* __restrict__ R,
-                                                       const int32_t* __restrict__ offsets, int64_t ldA,
-                                                       float* __restrict__ C, const int32_t* __restrict__ status) {
-    const int h = blockIdx.y;
-    if (!head_ok(status, h)) return;
-    const int off = offsets[h];
-    const int t = offsets[h + 1] - off;
-    const int i0 = blockIdx.x * SB;
-    if (i0 >= t) return;
-    __shared__ float Ms[SB][SB + 1];
-    __shared__ __align__(16) float Rs[SB][D];
-    const float* Mh = Minv + (int64_t)h * ldA * ldA;
-    constexpr int CW = D / 16;                 // columns per thread
-    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-    float acc[4][CW];
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int c = 0; c < CW; ++c) acc[a][c] = 0.f;
-    for (int j0 = 0; j0 < t; j0 += SB) {
-        __syncthreads();
-        for (int e = threadIdx.x; e < SB * SB; e += 256) {
-            const int r = e / SB, c = e % SB;
-            Ms[r][c] = (i0 + r < t && j0 + c < t) ? Mh[(int64_t)(i0 + r) * ldA + j0 + c] : 0.f;
-        }
-        for (int e = threadIdx.x; e < SB * D; e += 256) {
-            const int r = e / D, c = e % D;
-            Rs[r][c] = (j0 + r < t) ? R[((int64_t)off + j0 + r) * D + c] : 0.f;
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int p = 0; p < SB; ++p) {
-            float m[4], r[CW];
-#pragma unroll
-            for (int a = 0; a < 4; ++a) m[a] = Ms[ty * 4 + a][p];
-#pragma unroll
-            for (int c = 0; c < CW; ++c) r[c] = Rs[p][tx + 16 * c];
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int c = 0; c < CW; ++c) acc[a][c] = fmaf(m[a], r[c], acc[a][c]);
-        }
-    }
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-        const int i = i0 + ty * 4 + a;
-        if (i >= t) continue;
-#pragma unroll
-        for (int c = 0; c < CW; ++c) C[((int64_t)off + i) * D + tx + 16 * c] = acc[a][c];
-    }
-}
-
 }  // namespace
 
 int sweep_launches(int max_t) { return 2 * ((max_t + SB - 1) / SB) + 1; }
@@ -594,17 +536,6 @@ cudaError_t launch_sweep_inverse(float* A, const int32_t* offsets, int H, int ma
                                                                                   mv[2], ma, s);
     }
     k_sweep_mirror<<<dim3(ntri, H), 256, 0, st>>>(A, offsets, ldA, status);
-    return cudaGetLastError();
-}
-
-// C_v = M^{-1} R from the explicit inverse: C [sum t][d], R [sum t][d].
-cudaError_t launch_apply_inverse(int d, const float* Minv, const float* R, const int32_t* offsets, int H, int max_t,
-                                 int64_t ldA, float* C, const int32_t* status, cudaStream_t st) {
-    dim3 grid((max_t + SB - 1) / SB, H);
-    if (d == 128)
-        k_apply_inverse<128><<<grid, 256, 0, st>>>(Minv, R, offsets, ldA, C, status);
-    else
-        k_apply_inverse<64><<<grid, 256, 0, st>>>(Minv, R, offsets, ldA, C, status);
     return cudaGetLastError();
 }
 
