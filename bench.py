@@ -518,14 +518,17 @@ def run_ours(args, rank, world, local_rank):
 
 
 def _traffic_for(stage, cfg):
-    """DRAM bytes per launch of `stage` from a committed ncu summary, if any."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per call of `stage` from the committed ncu summary, if any."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         with open(path) as fh:
-            j = json.load(fh)
-        return j.get(f"{stage}/config{cfg}")
+            for line in fh:
+                parts = line.split()
+                if len(parts) == 3 and not line.startswith("#") and parts[0] == stage and parts[1] == f"config{cfg}":
+                    return int(parts[2])
     except (OSError, ValueError):
         return None
+    return None
 
 
 def main():
