@@ -518,16 +518,24 @@ def run_ours(args, rank, world, local_rank):
 
 
 def _traffic_for(stage, cfg):
-    """DRAM bytes per call of `stage` from the committed ncu summary, if any."""
-    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    """DRAM bytes per call of `stage` from the committed ncu summaries
+    (profiles/traffic_*.txt: lines "stage configN bytes"), if any."""
+    pdir = os.path.join(ROOT, "profiles")
     try:
-        with open(path) as fh:
-            for line in fh:
-                parts = line.split()
-                if len(parts) == 3 and not line.startswith("#") and parts[0] == stage and parts[1] == f"config{cfg}":
-                    return int(parts[2])
-    except (OSError, ValueError):
+        names = sorted(f for f in os.listdir(pdir) if f.startswith("traffic_") and f.endswith(".txt"))
+    except OSError:
         return None
+    for name in names:
+        try:
+            with open(os.path.join(pdir, name)) as fh:
+                for line in fh:
+                    parts = line.split()
+                    if line.startswith("#") or len(parts) != 3:
+                        continue
+                    if parts[0] == stage and parts[1] == f"config{cfg}":
+                        return int(parts[2])
+        except (OSError, ValueError):
+            continue
     return None
 
 
