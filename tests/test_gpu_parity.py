@@ -106,6 +106,20 @@ def test_t_equals_T_identity():
         assert np.linalg.norm(g["Cv"][o0:o1] - V) / np.linalg.norm(V) < 1e-3
 
 
+def test_largest_budget():
+    """The solver size limit: t = 4096 kept keys (64 sweep blocks per matrix),
+    n = 4096 queries, a cache of 4100 keys (ragged tails everywhere)."""
+    w = small_variant(WORKLOADS[2], H=1, n=4096, T=4100, t=4096)
+    _check(w, check_intermediates=False)
+
+
+def test_many_heads():
+    """1000 small heads in one call (grids of 1000 in y); a sample of them
+    against the oracle."""
+    w = small_variant(WORKLOADS[2], H=1000, n=64, T=200, t=24, d=64)
+    _check(w, heads=[0, 1, 499, 998, 999], check_intermediates=True)
+
+
 def test_degenerate_tiny_shapes():
     # a single key, a budget of one, very few queries
     for (n, T, t) in [(5, 1, 1), (3, 70, 1), (1, 64, 2), (7, 65, 65)]:
