@@ -36,6 +36,8 @@ namespace kvc {
 using namespace tc;
 
 bool make_map(CUtensorMap* m, const void* base, int d, int rows, int H);   // tmap.cu
+bool make_map_f32(CUtensorMap* m, const void* base, int cols, int64_t ld, int rows, int H);             // tmap.cu
+bool make_map_bf16_rows32(CUtensorMap* m, const void* base, int cols, int64_t ld, int rows, int H);     // tmap.cu
 
 namespace {
 
@@ -513,21 +515,58 @@ __global__ void __launch_bounds__(kColThreads, 1)
 // for t_h <= i < roundup(t_h, 64): one 128 x 128 tile per CTA, S = Q C_k^T on
 // the tensor cores.  The kept keys come from their per-head copy Ckw
 // [H][ldA][d] (bf16) that the gather writes.
+// Epilogue staging (after the product is done it reuses the operand tiles):
+// per epilogue warp one [32 rows][32 columns] fp32 box of log-masses and one
+// [32 rows][64 columns] bf16 box for each of A'_hi, A'_lo, all in the
+// 128-byte swizzled layout of the TMA store maps; then the column-sum
+// exchange, [4 chunks][4 warps][32] fp32.
 template <int D>
 struct MassLayout {
     static constexpr int kTile = (D / 64) * kBox;
     static constexpr int kQ = 0;
     static constexpr int kC = kTile;
-    static constexpr int kBar = 2 * kTile;
+    static constexpr int kWarpStage = 12 * 1024;          // L2 box 4 KB + A'_hi box 4 KB + A'_lo box 4 KB
+    static constexpr int kStage = 0;
+    static constexpr int kRed = kStage + 4 * kWarpStage;
+    static constexpr int kEnd = kRed + 4 * 4 * 32 * 4;
+    static constexpr int kBar = (2 * kTile > kEnd) ? 2 * kTile : kEnd;
     static constexpr int kBytes = kBar + 256 + 1024;
 };
 constexpr int kMassThreads = 192;
 
+// Byte offset of 16-byte chunk j of row r in a box whose rows are 128 bytes,
+// with the 128-byte swizzle (chunk index XOR row mod 8; box base 1024-aligned).
+__device__ __forceinline__ uint32_t sw128_off(int r, int j) { return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4)); }
+
+// Per-column sums of a warp's 32 x 32 block (lane = row, v[k] = column k):
+// a butterfly that halves the columns each lane keeps at every step; lane l
+// ends with the sum of column l in v[0].  Fixed order, so deterministic.
+template <int W>
+__device__ __forceinline__ void colsum_step(float (&v)[32], int lane) {
+    const bool up = (lane & W) != 0;
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+        const float send = up ? v[k] : v[k + W];
+        const float keep = up ? v[k + W] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, W);
+    }
+}
+
+// One CTA = 128 queries x 128 kept keys of one head; the product S = Q C_k^T
+// in one shot (K = d).  Epilogue per thread = one query row, in four chunks
+// of 32 keys: l2 = S * c2 - lse2 (the log2 relative mass, -inf past t_h),
+// A' = exp2(l2) as bf16 hi / lo terms (the Gram operand; 0 past t_h and for
+// rows past n), and the CTA's column sums of A' (one partial of b = A'^T 1
+// per 128-query tile, added in a fixed order by the total kernel).  The
+// three arrays leave through TMA stores of swizzled boxes (rows past n are
+// clipped by the maps); columns are written up to t_h rounded up to 64.
 template <int D>
 __global__ void __launch_bounds__(kMassThreads, 1)
     k_masslogits_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mC,
-                    const float* __restrict__ lse2, const int32_t* __restrict__ offsets, int n, int64_t ldA,
-                    float c2, float* __restrict__ L2, int32_t* __restrict__ status, int qdiv) {
+                    const __grid_constant__ CUtensorMap mL2, const __grid_constant__ CUtensorMap mAh,
+                    const __grid_constant__ CUtensorMap mAl, const float* __restrict__ lse2,
+                    const int32_t* __restrict__ offsets, int n, float c2, float* __restrict__ colpart,
+                    int64_t part_stride, int32_t* __restrict__ status, int qdiv) {
     using L = MassLayout<D>;
     const int h = blockIdx.z;
     if (!head_ok(status, h)) return;
@@ -558,6 +597,9 @@ __global__ void __launch_bounds__(kMassThreads, 1)
     const uint32_t tmem = *tmem_slot;
     if (warp == 0) {
         if (lane == 0) {
+            prefetch_tmap(&mL2);
+            prefetch_tmap(&mAh);
+            prefetch_tmap(&mAl);
             mbar_expect_tx(full, 2u * L::kTile);
             for (int c = 0; c < D / 64; ++c) {
                 tma_load_3d(sm + L::kQ + c * kBox, &mQ, full, c * 64, q0, h / qdiv);
@@ -580,34 +622,86 @@ __global__ void __launch_bounds__(kMassThreads, 1)
         }
         __syncwarp();
     } else {
-        const int quarter = warp & 3;
+        const int quarter = warp & 3;             // TMEM lanes 32 * quarter .. (the warp's rows)
         const int row = quarter * 32 + lane;
+        const int qw = q0 + quarter * 32;         // the warp's first query
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag));
         const int q = q0 + row;
-        if (ok) {
-            fence_after_sync();
-            const float lq = (q < n) ? lse2[(int64_t)h * n + q] : 0.f;
-            float* dst = L2 + ((int64_t)h * n + q) * ldA + i0;
+        const float lq = (ok && q < n) ? lse2[(int64_t)h * n + q] : 0.f;
+        uint8_t* bL = sm + L::kStage + quarter * L::kWarpStage;
+        uint8_t* bH = bL + 4096;
+        uint8_t* bO = bL + 8192;
+        float* red = reinterpret_cast<float*>(sm + L::kRed);      // [chunk][warp][32]
+        const bool store = ok && qw < n;
+        if (ok) fence_after_sync();
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 4; ++c) {
+            const int ib = i0 + c * 32;
+            float x[32];
+            if (ok) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_off + c * 32, r);
                 tmem_ld_wait();
-                const int ib = i0 + c * 32;
-                if (q < n && ib < tpad) {
 #pragma unroll
-                    for (int k = 0; k < 32; k += 4) {
-                        float4 v;
-                        v.x = (ib + k + 0 < th) ? fmaf(__uint_as_float(r[k + 0]), c2, -lq) : -INFINITY;
-                        v.y = (ib + k + 1 < th) ? fmaf(__uint_as_float(r[k + 1]), c2, -lq) : -INFINITY;
-                        v.z = (ib + k + 2 < th) ? fmaf(__uint_as_float(r[k + 2]), c2, -lq) : -INFINITY;
-                        v.w = (ib + k + 3 < th) ? fmaf(__uint_as_float(r[k + 3]), c2, -lq) : -INFINITY;
-                        *reinterpret_cast<float4*>(dst + c * 32 + k) = v;
+                for (int k = 0; k < 32; ++k) {
+                    const float v = (ib + k < th) ? fmaf(__uint_as_float(r[k]), c2, -lq) : -INFINITY;
+                    x[k] = (q < n && ib + k < th) ? exp2f(v) : 0.f;
+                    r[k] = __float_as_uint(v);
+                }
+                if (store && ib < tpad) {
+                    // the previous chunk's boxes must have been read out before we overwrite them
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<float4*>(bL + sw128_off(lane, j)) =
+                            make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        __align__(16) __nv_bfloat16 hv[8], lv[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            hv[e] = __float2bfloat16_rn(x[8 * j + e]);
+                            lv[e] = __float2bfloat16_rn(x[8 * j + e] - __bfloat162float(hv[e]));
+                        }
+                        const uint32_t o = sw128_off(lane, (c & 1) * 4 + j);
+                        *reinterpret_cast<uint4*>(bH + o) = *reinterpret_cast<const uint4*>(hv);
+                        *reinterpret_cast<uint4*>(bO + o) = *reinterpret_cast<const uint4*>(lv);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&mL2, bL, ib, qw, h);
+                        if (c & 1) {
+                            tma_store_3d(&mAh, bH, ib - 32, qw, h);
+                            tma_store_3d(&mAl, bO, ib - 32, qw, h);
+                        }
+                        bulk_commit();
                     }
                 }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) x[k] = 0.f;
             }
+            colsum_step<16>(x, lane);
+            colsum_step<8>(x, lane);
+            colsum_step<4>(x, lane);
+            colsum_step<2>(x, lane);
+            colsum_step<1>(x, lane);
+            red[(c * 4 + quarter) * 32 + lane] = x[0];
         }
+        // every epilogue warp reaches the barrier, whatever `ok` was
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        const int cc = quarter;                   // warp `quarter` totals chunk `quarter`
+        const int col = i0 + cc * 32 + lane;
+        if (ok && col < th) {
+            const float* rc = red + cc * 4 * 32 + lane;
+            colpart[(int64_t)blockIdx.y * part_stride + off + col] = (rc[0] + rc[32]) + (rc[64] + rc[96]);
+        }
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
     }
     if (threadIdx.x == 0 && *abort_flag) set_status(status, h, KVC_ERR_TIMEOUT);
     fence_before_sync();
@@ -648,25 +742,35 @@ cudaError_t launch_col_t(const void* Q, const void* K, const float* lse2, int H,
 
 template <int D>
 cudaError_t launch_mass_t(const void* Q, const void* Ck, const float* lse2, const int32_t* offsets, int H, int n,
-                          int max_t, int64_t ldA, float c2, float* L2, int32_t* status, int qdiv, cudaStream_t st) {
-    CUtensorMap mQ, mC;
-    if (!make_map(&mQ, Q, D, n, H / qdiv) || !make_map(&mC, Ck, D, (int)ldA, H)) return cudaErrorInvalidValue;
+                          int max_t, int64_t ldA, float c2, float* L2, void* Ah, void* Al, float* colpart,
+                          int64_t part_stride, int32_t* status, int qdiv, cudaStream_t st) {
+    CUtensorMap mQ, mC, mL2, mAh, mAl;
+    if (!make_map(&mQ, Q, D, n, H / qdiv) || !make_map(&mC, Ck, D, (int)ldA, H) ||
+        !make_map_f32(&mL2, L2, (int)ldA, ldA, n, H) || !make_map_bf16_rows32(&mAh, Ah, (int)ldA, ldA, n, H) ||
+        !make_map_bf16_rows32(&mAl, Al, (int)ldA, ldA, n, H))
+        return cudaErrorInvalidValue;
     constexpr int smem = MassLayout<D>::kBytes;
     auto kern = k_masslogits_tc<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((max_t + TB - 1) / TB, (n + TB - 1) / TB, H);
-    kern<<<grid, kMassThreads, smem, st>>>(mQ, mC, lse2, offsets, n, ldA, c2, L2, status, qdiv);
+    kern<<<grid, kMassThreads, smem, st>>>(mQ, mC, mL2, mAh, mAl, lse2, offsets, n, c2, colpart, part_stride, status,
+                                           qdiv);
     return cudaGetLastError();
 }
 
 }  // namespace
 
+// L2: fp32 [H][n][ldA] log2 A'; Ah / Al: A' as bf16 hi / lo terms, same
+// layout; colpart: column sums of A' per 128-query tile, [tile][part_stride]
+// (entry off_h + i).  All three required.
 cudaError_t launch_masslogits_tc(int d, const void* Q, const void* Ck, const float* lse2, const int32_t* offsets,
-                                 int H, int n, int max_t, int64_t ldA, float c2, float* L2, int32_t* status,
-                                 int qdiv, cudaStream_t st) {
-    return d == 128 ? launch_mass_t<128>(Q, Ck, lse2, offsets, H, n, max_t, ldA, c2, L2, status, qdiv, st)
-                    : launch_mass_t<64>(Q, Ck, lse2, offsets, H, n, max_t, ldA, c2, L2, status, qdiv, st);
+                                 int H, int n, int max_t, int64_t ldA, float c2, float* L2, void* Ah, void* Al,
+                                 float* colpart, int64_t part_stride, int32_t* status, int qdiv, cudaStream_t st) {
+    return d == 128 ? launch_mass_t<128>(Q, Ck, lse2, offsets, H, n, max_t, ldA, c2, L2, Ah, Al, colpart, part_stride,
+                                         status, qdiv, st)
+                    : launch_mass_t<64>(Q, Ck, lse2, offsets, H, n, max_t, ldA, c2, L2, Ah, Al, colpart, part_stride,
+                                        status, qdiv, st);
 }
 
 cudaError_t launch_attn_fwd_tc(int d, const void* Q, const void* K, const void* V, int H, int n, int T, float c2,

@@ -498,6 +498,13 @@ cudaError_t launch_gram_rect_tc(int d, const void* Ah, const void* Al, const voi
     return cudaGetLastError();
 }
 
+// b[off + c] = sum over the row-tile partials (fixed order).
+cudaError_t launch_colsum_total(const float* part, int ntiles, int64_t stride, const int32_t* offsets, float* b,
+                                int H, int max_cols, const int32_t* status, cudaStream_t st) {
+    k_colsum_total<<<dim3((max_cols + 255) / 256, H), 256, 0, st>>>(part, ntiles, stride, offsets, b, status);
+    return cudaGetLastError();
+}
+
 // fp32 [H][rows][ld] -> bf16 hi / lo.  offsets given: t_h addressed columns
 // per head (padded to 64 with zeros); else `cols` for every head.  exp_mode:
 // stored values are log2.  colsum (optional): b = column sums, through the

@@ -19,8 +19,10 @@ cudaError_t launch_shift_idx(int32_t*, const int32_t*, int, int, int, int, const
 cudaError_t launch_gather(int, int, const void*, const void*, int, int, int, const int32_t*, const int32_t*, void*,
                           float*, void*, int64_t, const int32_t*, cudaStream_t);
 cudaError_t launch_masslogits_tc(int d, const void* Q, const void* Ck, const float* lse2, const int32_t* offsets,
-                                 int H, int n, int max_t, int64_t ldA, float c2, float* L2, int32_t* status,
-                                 int qdiv, cudaStream_t st);
+                                 int H, int n, int max_t, int64_t ldA, float c2, float* L2, void* Ah, void* Al,
+                                 float* colpart, int64_t part_stride, int32_t* status, int qdiv, cudaStream_t st);
+cudaError_t launch_colsum_total(const float* part, int ntiles, int64_t stride, const int32_t* offsets, float* b,
+                                int H, int max_cols, const int32_t* status, cudaStream_t st);
 cudaError_t launch_masslogits(int, int, const void*, const void*, const float*, const int32_t*, int, int, int, int64_t,
                               float, float*, const int32_t*, int, cudaStream_t);
 cudaError_t launch_attend(int, int, const void*, int, const void*, const float*, const float*, const int32_t*, int,
@@ -425,17 +427,21 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
                   launch_tam_kept(tam->pivots, H, T, mt, idx_out, offsets, kp, plist, npk, head_status, st));
     if (tc) {
         // the kept keys' per-head copy has ldA rows per head; the map sees H * ldA rows
+        // the log-masses, A' as bf16 hi / lo terms and the column-sum partials of b in one pass
         KVC_STAGE("masslogits", 1,
-                  launch_masslogits_tc(d, Q_ref, Ckw, lse2, offsets, H, n, mt, L.ldA, c2, L2, head_status, qdiv,
-                                       st));
+                  launch_masslogits_tc(d, Q_ref, Ckw, lse2, offsets, H, n, mt, L.ldA, c2, L2, ws + L.Ah, ws + L.Al,
+                                       (float*)(ws + L.bpart), (int64_t)H * mt, head_status, qdiv, st));
+        KVC_STAGE("colsum", 1,
+                  launch_colsum_total((float*)(ws + L.bpart), (n + 127) / 128, (int64_t)H * mt, offsets, b, H, mt,
+                                      head_status, st));
     } else {
         KVC_STAGE("masslogits", 1,
                   launch_masslogits(dt, d, Q_ref, C_k, lse2, offsets, H, n, mt, L.ldA, c2, L2, head_status, qdiv,
                                     st));
+        KVC_STAGE("split_a", 2,
+                  launch_split_hilo(true, L2, H, n, L.ldA, offsets, 0, mt, ws + L.Ah, ws + L.Al,
+                                    (float*)(ws + L.bpart), b, head_status, st));
     }
-    KVC_STAGE("split_a", 2,
-              launch_split_hilo(true, L2, H, n, L.ldA, offsets, 0, mt, ws + L.Ah, ws + L.Al, (float*)(ws + L.bpart),
-                                b, head_status, st));
     KVC_STAGE("gram_a", 1,
               launch_gram_sym_tc(ws + L.Ah, ws + L.Al, offsets, H, n, mt, L.ldA, G, L.ldA, head_status, st));
     KVC_STAGE("ridge_g", 1, launch_ridge_g(G, b, offsets, H, L.ldA, q.eps_mu, f, hs, head_status, st));

@@ -61,4 +61,10 @@ bool make_map_bf16(CUtensorMap* m, const void* base, int cols, int64_t ld, int r
     return encode3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, ld, rows, H, 64, 64);
 }
 
+// The same bf16 layout with boxes of [32 rows][64 columns]: the store boxes
+// of a warp's 32 rows.
+bool make_map_bf16_rows32(CUtensorMap* m, const void* base, int cols, int64_t ld, int rows, int H) {
+    return encode3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, ld, rows, H, 64, 32);
+}
+
 }  // namespace kvc
