@@ -93,38 +93,64 @@ __global__ void k_ridge_m_diag(float* __restrict__ M, const int32_t* __restrict_
 // terms (the Gram operand format, see gram_tc.cu); padding columns up to the
 // next multiple of 64 are 0.  log2 w_i = beta_i log2 e (beta = ln w, -inf
 // where w = 0).  grid (ceil(n/32), H), block 256: a warp per row, four rows
-// per warp; the CTA's 32 rows share one staged copy of log2 w.
+// per warp; the CTA's 32 rows share one staged copy of log2 w.  Each lane
+// takes four adjacent columns per step (one 16-byte load, two 8-byte
+// stores): a first pass keeps a running maximum and the sum rescaled to it,
+// a second pass writes the normalised terms.
+__device__ __forceinline__ void online_add(float& m, float& s, float v0, float v1, float v2, float v3) {
+    const float mn = fmaxf(fmaxf(m, fmaxf(v0, v1)), fmaxf(v2, v3));
+    if (mn == -INFINITY) return;                     // nothing finite seen yet
+    s = s * exp2f(m - mn) + ((exp2f(v0 - mn) + exp2f(v1 - mn)) + (exp2f(v2 - mn) + exp2f(v3 - mn)));
+    m = mn;
+}
+
 __global__ void __launch_bounds__(256) k_xsoftmax(const float* __restrict__ L2, const float* __restrict__ beta,
                                                   const int32_t* __restrict__ offsets, int n, int64_t ldA,
                                                   __nv_bfloat16* __restrict__ Xh, __nv_bfloat16* __restrict__ Xl,
                                                   const int32_t* __restrict__ status) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
-    extern __shared__ float lw[];
+    extern __shared__ float4 lw4[];
+    float* lw = reinterpret_cast<float*>(lw4);
     const int off = offsets[h];
     const int t = offsets[h + 1] - off;
-    for (int i = threadIdx.x; i < t; i += blockDim.x) lw[i] = beta[off + i] * kLog2e;
+    const int tp = (int)round_up(t, GT);
+    for (int i = threadIdx.x; i < tp; i += blockDim.x) lw[i] = i < t ? beta[off + i] * kLog2e : -INFINITY;
     __syncthreads();
     const int lane = threadIdx.x & 31;
-    const int tp = (int)round_up(t, GT);
     for (int rr = 0; rr < 4; ++rr) {
         const int q = blockIdx.x * 32 + (threadIdx.x >> 5) * 4 + rr;
         if (q >= n) break;
         const int64_t ro = ((int64_t)h * n + q) * ldA;
-        const float* row = L2 + ro;
-        float mx = -INFINITY;
-        for (int i = lane; i < t; i += 32) mx = fmaxf(mx, row[i] + lw[i]);
-        mx = warp_max(mx);
-        float s = 0.f;
-        for (int i = lane; i < t; i += 32) s += exp2f(row[i] + lw[i] - mx);
+        const float4* row = reinterpret_cast<const float4*>(L2 + ro);
+        float m = -INFINITY, s = 0.f;
+        for (int i = 4 * lane; i < t; i += 128) {
+            const float4 a = row[i >> 2], w = lw4[i >> 2];
+            // columns past t carry log2 w = -inf
+            online_add(m, s, a.x + w.x, i + 1 < t ? a.y + w.y : -INFINITY, i + 2 < t ? a.z + w.z : -INFINITY,
+                       i + 3 < t ? a.w + w.w : -INFINITY);
+        }
+        const float mx = warp_max(m);
+        s = (m == -INFINITY) ? 0.f : s * exp2f(m - mx);
         s = warp_sum(s);
         const float inv = (s > 0.f && mx > -INFINITY) ? 1.f / s : 0.f;
-        for (int i = lane; i < tp; i += 32) {
-            float x = 0.f;
-            if (i < t && inv > 0.f) x = exp2f(row[i] + lw[i] - mx) * inv;
-            const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-            Xh[ro + i] = hi;
-            Xl[ro + i] = __float2bfloat16_rn(x - __bfloat162float(hi));
+        for (int i = 4 * lane; i < tp; i += 128) {
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
+            if (inv > 0.f && i < t) {
+                const float4 a = row[i >> 2], w = lw4[i >> 2];
+                const float v[4] = {a.x + w.x, a.y + w.y, a.z + w.z, a.w + w.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (i + j < t) x[j] = exp2f(v[j] - mx) * inv;
+            }
+            __align__(8) __nv_bfloat16 hv[4], lv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                hv[j] = __float2bfloat16_rn(x[j]);
+                lv[j] = __float2bfloat16_rn(x[j] - __bfloat162float(hv[j]));
+            }
+            *reinterpret_cast<uint2*>(Xh + ro + i) = *reinterpret_cast<const uint2*>(hv);
+            *reinterpret_cast<uint2*>(Xl + ro + i) = *reinterpret_cast<const uint2*>(lv);
         }
     }
 }
