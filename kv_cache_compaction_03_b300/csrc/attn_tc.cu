@@ -10,7 +10,9 @@
 //                   leave O with ~1e-3 relative error, which the least-squares
 //                   fit of C_v amplifies past its tolerance.
 //   k_masslogits_tc log2 of the relative mass matrix A' for the kept keys,
-//                   S = Q C_k^T on the tensor cores.
+//                   S = Q C_k^T on the tensor cores; the epilogue also
+//                   writes A' as bf16 hi / lo terms (the Gram operand) and
+//                   per-tile column sums of A' (partials of b = A'^T 1).
 //   k_colscore_tc   K-major pass: S^T = K Q^T per key tile, then every key
 //                   row sums exp(2 (S - lse)) over all queries: the RMS
 //                   attention score of each key (key selection aggregated

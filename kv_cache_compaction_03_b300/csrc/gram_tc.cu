@@ -9,8 +9,9 @@
 // C[i][j] = sum_q A[q][i] B[q][j] over the n reference queries.  Every fp32
 // operand value x is stored as two bf16 terms, hi = bf16(x) and
 // lo = bf16(x - hi) (round to nearest), in separate [H][n][ld] arrays
-// written once by the pass that produces the operand (k_split_hilo below for
-// A' and O, the biased softmax for X).  The products run on the tcgen05
+// written once by the pass that produces the operand (the tensor-core mass
+// logits' epilogue for A' with bf16 inputs, k_split_hilo below for A' with
+// fp32 inputs and for O, the biased softmax for X).  The products run on the tcgen05
 // tensor cores in bf16: C accumulates A_hi B_hi + A_hi B_lo + A_lo B_hi in
 // fp32.  The split carries ~2^-17 of each value and the dropped A_lo B_lo
 // term is ~2^-18 relative; both errors have random sign, so a sum over the
