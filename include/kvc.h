@@ -81,7 +81,7 @@ typedef struct kvc_params {
     float eps_mu;         /* NNLS ridge toward w = 1: mu = eps_mu * tr(G)/t (1e-2) */
     float eps_lambda;     /* C_v ridge toward V[idx]: lambda = eps_lambda *
                              tr(X^T X)/t (1e-2)                                   */
-    int32_t nnls_max_iter;  /* block-pivoting iterations (default 12)             */
+    int32_t nnls_max_iter;  /* block-pivoting iterations (default 32)             */
     int32_t nnls_max_zero;  /* cap on weights held at zero (default 512)          */
     int32_t refine_iters;   /* NNLS iterative-refinement steps (default 2)        */
     int32_t keep_first;     /* positions [0, keep_first) are always kept          */

@@ -195,7 +195,7 @@ static Layout make_layout(const kvc_problem& p, const kvc_params& prm, TamShape 
     L.G = carve(c, H * ldA * ldA * 4);
     L.dinv = carve(c, H * ldA * 64 * 4);      // Cholesky diagonal inverses; sweep U panel
     L.swV = carve(c, 6 * H * 64 * ldA * 2);   // sweep: U^T and V as three bf16 terms each
-    L.swP = carve(c, H * 64 * 64 * 4);        // sweep: pivot block inverse
+    L.swP = carve(c, 4 * H * 64 * 64 * 4);    // sweep: pivot block inverse, next block inputs, its inverse
     L.b = carve(c, H * mt * 4);
     L.f = carve(c, H * mt * 4);
     L.x = carve(c, H * mt * 4);
@@ -281,7 +281,7 @@ kvc_status kvc_default_params(kvc_params* prm) {
     prm->scale = 0.f;
     prm->eps_mu = 1e-2f;
     prm->eps_lambda = 1e-2f;
-    prm->nnls_max_iter = 12;
+    prm->nnls_max_iter = 32;
     prm->nnls_max_zero = 512;
     prm->refine_iters = 2;
     return KVC_OK;

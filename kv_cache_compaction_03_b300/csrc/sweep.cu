@@ -13,15 +13,20 @@
 // complement and stays positive definite, so no pivoting is needed.  Rows
 // and columns past t act as an identity block.
 //
-//   k_sweep_pivot   grid (blocks, H): every CTA sweeps the 64 x 64 pivot
-//                   block in registers (64 scalar sweeps over 4 x 8 thread
-//                   tiles, giving -P), then computes U_i = A_ik P for its row
-//                   block i (stored transposed) and copies V_i = A_ki
-//   k_sweep_update_tc  grid (lower 128 x 128 tiles, H): A_ij -= U_i V_j on
+//   k_sweep_pivot   grid (blocks, H): every CTA takes the inverse P of the
+//                   64 x 64 pivot block (the first block's it forms itself,
+//                   by 16 four-pivot sweeps in registers), then computes
+//                   U_i = A_ik P for its row block i (stored transposed) and
+//                   copies V_i = A_ki; the CTA of row block k + 1 also copies
+//                   the next pivot block's inputs
+//   k_sweep_update_tc  grid (1 + lower 128 x 128 tiles, H): A_ij -= U_i V_j on
 //                   the tcgen05 tensor cores (operands as three exact bf16
 //                   terms, six products), with the pivot row / column copies
 //                   in the epilogue; on a head's last block the stored result
-//                   is negated, so the matrix ends as +H^{-1}
+//                   is negated, so the matrix ends as +H^{-1}.  CTA 0 of each
+//                   head meanwhile forms the next pivot block as this step
+//                   leaves it and inverts it (look-ahead), so the dependent
+//                   chain of step k + 1 overlaps the update of step k
 //   k_sweep_mirror  copies the lower triangle into the upper one
 //   k_symv          y = H^{-1} v for every head (one warp per row)
 // The sweep keeps the symmetric matrix in its lower triangle (row-major,
@@ -40,12 +45,15 @@ struct SweepArgs {
     float* U;                 // [H][64][ldA]  U^T: U[p][r] = (A_ik P)[r][p]
     __nv_bfloat16* Us;        // [3][H][64][ldA]  U^T as three bf16 terms
     __nv_bfloat16* Vs;        // [3][H][64][ldA]  V[p][r] = A_kr[p][r], three bf16 terms
-    float* P;                 // [H][64][64]
+    float* P;                 // [H][64][64]  P = A_kk^{-1} of this step
+    float* Xnext;             // [H][2][64][64]  A_{k,k+1} and the stored A_{k+1,k+1} before this step's update
+    float* Pnext;             // [H][64][64]  P of the next step, formed while this step's update runs
     const int32_t* offsets;
     int64_t ldA;
     int64_t ts;               // elements between the terms of Us / Vs (H * 64 * ldA)
     int k0;                   // first row of the pivot block
     int32_t* status;
+    int have_p;               // P of this step was formed by the previous update launch
 };
 
 // x = hi + mid + lo exactly (three bf16 terms of 8 significant bits each;
@@ -58,24 +66,149 @@ __device__ __forceinline__ void split3(float x, __nv_bfloat16& hi, __nv_bfloat16
 }
 
 
-// grid (blocks, H), block 128.  Every CTA first inverts the 64 x 64 pivot
-// block by 64 scalar sweeps, then (row blocks i != k) forms U_i = A_ik P.
-//
-// The scalar sweeps are a dependent chain, so their cost is the latency of
-// one step: the owner threads publish the pivot row through shared memory,
-// one barrier, every thread reads what it needs and updates its entries.
-// Each thread holds a 4 x 8 register tile (rows 4 ty .., columns 8 tx ..),
-// so a step reads only 8 + 4 pivot-row values per thread (by symmetry the
-// pivot row also provides the pivot column): the shared-memory return
-// traffic of those broadcast reads, not the barrier, sets the step time.
-// The chain loop runs as 8 x 8 with the inner 8 unrolled, so the row and
-// column a step pivots on have static register indices.
 constexpr int kPS = SB + 4;      // padded smem row, 16-byte aligned
 constexpr int kPivThreads = 128;
 constexpr int kCR = 4;           // chain tile rows per thread (columns: 8)
 
+// The 64 x 64 pivot block's inverse in place: Dn holds the block (its lower
+// triangle is what is read; rows / columns past t act as identity) and ends
+// holding P = D^{-1}.  Run by 128 threads (tid 0..127) that synchronise on
+// named barrier 1.
+//
+// The inversion is a dependent chain, so its cost is the latency of one
+// step times the number of steps.  It sweeps four pivots per step (16 steps
+// instead of 64 scalar ones): the owner threads publish the group's four
+// rows through shared memory, one barrier, then every thread forms the
+// group's 4 x 4 inverse in registers and applies it to its own entries.
+// Each thread holds a 4 x 8 register tile (rows 4 ty .., columns 8 tx ..);
+// the group loop runs as 8 x 2 with the inner 2 unrolled, so the group's
+// columns have static register indices.  A non-positive or non-finite
+// pivot sets *bad.
+__device__ __forceinline__ void sync128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void chain_invert(float (*Dn)[kPS], float (*grp)[4][SB], int* bad_p, int tid, int k0,
+                                             int t) {
+    constexpr int R = kCR;
+    volatile int& bad = *bad_p;
+    const int tx = tid & 7, ty = tid >> 3;
+    float a[R][8];
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int r = R * ty + i, c = 8 * tx + j;
+            const bool in = (k0 + r < t) && (k0 + c < t);    // rows / columns past t: identity
+            a[i][j] = in ? ((c <= r) ? Dn[r][c] : Dn[c][r]) : (r == c ? 1.f : 0.f);
+        }
+    // 16 block steps, each sweeping four pivots at once (rows / columns
+    // 4g .. 4g + 3).  With D the group's 4 x 4 block, Qn = -D^{-1}:
+    //   a_ij += (a_ig Qn) a_gj,  a_ig <- -(a_ig Qn),  a_gj <- -(Qn a_gj),
+    //   a_gg <- Qn,
+    // which is exactly four scalar sweeps applied together.  The threads that
+    // own the group's rows (ty == g) publish them; after one barrier every
+    // thread reads D, the group rows over its own columns and (by symmetry)
+    // the group columns over its own rows, forms Qn by four scalar sweeps of
+    // D in registers, and updates its tile.
+#pragma unroll 1
+    for (int gp = 0; gp < 8; ++gp) {
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int g = 2 * gp + h2;
+            float(*Rg)[SB] = grp[h2];
+            if (ty == g) {
+#pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    *reinterpret_cast<float4*>(&Rg[i][8 * tx]) = make_float4(a[i][0], a[i][1], a[i][2], a[i][3]);
+                    *reinterpret_cast<float4*>(&Rg[i][8 * tx + 4]) = make_float4(a[i][4], a[i][5], a[i][6], a[i][7]);
+                }
+            }
+            sync128();
+            float q[4][4], cg[4][4], rg[4][8];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float4 d4 = *reinterpret_cast<const float4*>(&Rg[m][4 * g]);
+                const float4 c4 = *reinterpret_cast<const float4*>(&Rg[m][R * ty]);
+                const float4 x0 = *reinterpret_cast<const float4*>(&Rg[m][8 * tx]);
+                const float4 x1 = *reinterpret_cast<const float4*>(&Rg[m][8 * tx + 4]);
+                q[m][0] = d4.x; q[m][1] = d4.y; q[m][2] = d4.z; q[m][3] = d4.w;
+                cg[m][0] = c4.x; cg[m][1] = c4.y; cg[m][2] = c4.z; cg[m][3] = c4.w;
+                rg[m][0] = x0.x; rg[m][1] = x0.y; rg[m][2] = x0.z; rg[m][3] = x0.w;
+                rg[m][4] = x1.x; rg[m][5] = x1.y; rg[m][6] = x1.z; rg[m][7] = x1.w;
+            }
+            // q <- -D^{-1} by four scalar sweeps
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                float d = q[p][p];
+                if (!(d > 0.f) || !isfinite(d)) {
+                    bad = 1;
+                    d = 1.f;
+                }
+                // reciprocal: hardware approximation plus one Newton step (~1 ulp)
+                float inv;
+                asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(d));
+                inv = inv * fmaf(-d, inv, 2.f);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (i == p) continue;
+                    const float f = q[i][p] * inv;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (j != p) q[i][j] = fmaf(-f, q[p][j], q[i][j]);
+                    q[i][p] = f;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (j != p) q[p][j] *= inv;
+                q[p][p] = -inv;
+            }
+            // one update for every row, so no warp runs two paths: for the
+            // group's own rows w = -Qn[i][:] and the old entry is dropped
+            // (a_gj <- -(Qn a_gj)); for the others w = a_ig Qn (a_ig = a_gi
+            // by symmetry) and a_ij += w a_gj; the group's columns then
+            // become -w (a_ig <- -(a_ig Qn), a_gg <- Qn)
+            const bool grow = (ty == g);
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                float w[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    float v = 0.f;
+#pragma unroll
+                    for (int l = 0; l < 4; ++l) v = fmaf(cg[l][i], q[l][m], v);
+                    w[m] = grow ? -q[i][m] : v;
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float v = grow ? 0.f : a[i][j];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) v = fmaf(w[m], rg[m][j], v);
+                    a[i][j] = v;
+                }
+                if (tx == gp) {
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) a[i][4 * h2 + jj] = -w[jj];
+                }
+            }
+        }
+    }
+    // the block now holds -P: store P
+    sync128();
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        *reinterpret_cast<float4*>(&Dn[R * ty + i][8 * tx]) = make_float4(-a[i][0], -a[i][1], -a[i][2], -a[i][3]);
+        *reinterpret_cast<float4*>(&Dn[R * ty + i][8 * tx + 4]) = make_float4(-a[i][4], -a[i][5], -a[i][6], -a[i][7]);
+    }
+    sync128();
+}
+
+// grid (blocks, H), block 128.  Every CTA takes the pivot block's inverse P
+// (formed here for the first block, else by the previous update launch),
+// then (row blocks i != k) forms U_i = A_ik P.  The CTA of row block k + 1
+// also copies A_{k,k+1} and A_{k+1,k+1} for the update launch, whose first
+// CTA forms the next pivot block D' = A_{k+1,k+1} - U_{k+1} A_{k,k+1} from
+// them (the other CTAs rewrite A meanwhile) and inverts it.
 __global__ void __launch_bounds__(kPivThreads) k_sweep_pivot(SweepArgs s) {
-    constexpr int NT = kPivThreads, R = kCR;
+    constexpr int NT = kPivThreads;
     const int h = blockIdx.y;
     if (!head_ok(s.status, h)) return;
     const int t = s.offsets[h + 1] - s.offsets[h];
@@ -85,20 +218,25 @@ __global__ void __launch_bounds__(kPivThreads) k_sweep_pivot(SweepArgs s) {
     if (r0 >= t) return;
     __shared__ __align__(16) float Dn[SB][kPS];     // pivot block, then P
     __shared__ __align__(16) float At[SB][kPS];     // At[p][r] = A_ik[r][p]
-    __shared__ __align__(16) float rowb[2][SB];
+    __shared__ __align__(16) float grp[2][4][SB];    // a pivot group's rows, double-buffered
     __shared__ int bad;
     const float* A = s.A + (int64_t)h * s.ldA * s.ldA;
     const int tid = threadIdx.x;
     const bool diag = (r0 == k0);
-    // stage the pivot block (its stored lower triangle is what gets used) and
-    // A_ik (rows below the pivot: stored directly; above: the transpose of
-    // the stored tile (k, i)); every load is issued before the first store
+    const bool nextblk = (r0 == k0 + SB);      // row block k + 1: hands the next pivot block's inputs on
+    // stage the pivot block (its stored lower triangle is what gets used) or
+    // its inverse when that is already formed, and A_ik (rows below the
+    // pivot: stored directly; above: the transpose of the stored tile
+    // (k, i)); every load is issued before the first store
     {
-        float4 dv[8], av[8];
+        const float* Pn = s.Pnext + (int64_t)h * SB * SB;
+        float4 dv[8], av[8], xv[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const int e = tid + NT * q, r = e >> 4, c4 = (e & 15) * 4;
-            dv[q] = *reinterpret_cast<const float4*>(A + (int64_t)(k0 + r) * s.ldA + k0 + c4);
+            dv[q] = s.have_p ? *reinterpret_cast<const float4*>(Pn + r * SB + c4)
+                             : *reinterpret_cast<const float4*>(A + (int64_t)(k0 + r) * s.ldA + k0 + c4);
+            if (nextblk) xv[q] = *reinterpret_cast<const float4*>(A + (int64_t)(r0 + r) * s.ldA + r0 + c4);
             if (!diag) {
                 if (r0 > k0) av[q] = *reinterpret_cast<const float4*>(A + (int64_t)(r0 + r) * s.ldA + k0 + c4);
                 else av[q] = *reinterpret_cast<const float4*>(A + (int64_t)(k0 + r) * s.ldA + r0 + c4);
@@ -108,6 +246,7 @@ __global__ void __launch_bounds__(kPivThreads) k_sweep_pivot(SweepArgs s) {
         for (int q = 0; q < 8; ++q) {
             const int e = tid + NT * q, r = e >> 4, c4 = (e & 15) * 4;
             *reinterpret_cast<float4*>(&Dn[r][c4]) = dv[q];
+            if (nextblk) *reinterpret_cast<float4*>(s.Xnext + ((int64_t)h * 2 + 1) * SB * SB + r * SB + c4) = xv[q];
             if (!diag) {
                 const float x[4] = {av[q].x, av[q].y, av[q].z, av[q].w};
                 if (r0 > k0) {
@@ -122,73 +261,29 @@ __global__ void __launch_bounds__(kPivThreads) k_sweep_pivot(SweepArgs s) {
             }
         }
     }
-    if (tid == 0) bad = 0;
     __syncthreads();
-    const int tx = tid & 7, ty = tid >> 3;
-    float a[R][8];
+    if (nextblk) {
+        // the next pivot block is D' = A_{k+1,k+1} - U_{k+1} A_{k,k+1}; the
+        // update launch forms it (with U_{k+1} from U) and inverts it, from
+        // copies of A_{k,k+1} and of A_{k+1,k+1}, which that launch rewrites
+        float* X = s.Xnext + (int64_t)h * 2 * SB * SB;
 #pragma unroll
-    for (int i = 0; i < R; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int r = R * ty + i, c = 8 * tx + j;
-            const bool in = (k0 + r < t) && (k0 + c < t);    // rows / columns past t: identity
-            a[i][j] = in ? ((c <= r) ? Dn[r][c] : Dn[c][r]) : (r == c ? 1.f : 0.f);
-        }
-    for (int pb = 0; pb < 8; ++pb) {
-#pragma unroll
-        for (int m0 = 0; m0 < 8; ++m0) {
-            const int p = 8 * pb + m0;
-            float* rb = rowb[m0 & 1];
-            if (ty == p / R) {
-#pragma unroll
-                for (int i = 0; i < R; ++i)
-                    if (i == p % R) {
-                        *reinterpret_cast<float4*>(rb + 8 * tx) = make_float4(a[i][0], a[i][1], a[i][2], a[i][3]);
-                        *reinterpret_cast<float4*>(rb + 8 * tx + 4) = make_float4(a[i][4], a[i][5], a[i][6], a[i][7]);
-                    }
-            }
-            __syncthreads();
-            const float4 x0 = *reinterpret_cast<const float4*>(rb + 8 * tx);
-            const float4 x1 = *reinterpret_cast<const float4*>(rb + 8 * tx + 4);
-            const float4 c4 = *reinterpret_cast<const float4*>(rb + R * ty);
-            const float row[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            const float col[R] = {c4.x, c4.y, c4.z, c4.w};
-            float d = rb[p];
-            if (!(d > 0.f) || !isfinite(d)) {
-                bad = 1;
-                d = 1.f;
-            }
-            // reciprocal: hardware approximation plus one Newton step (~1 ulp)
-            float inv;
-            asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(d));
-            inv = inv * fmaf(-d, inv, 2.f);
-#pragma unroll
-            for (int i = 0; i < R; ++i) {
-                if (R * ty + i == p) {
-                    // row p becomes a_pc / d, the pivot -1 / d
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) a[i][j] *= inv;
-                    if (tx == pb) a[i][m0] = -inv;
-                } else {
-                    // a_ic -= a_ip a_pc / d; column p itself becomes a_ip / d
-                    const float f = col[i] * inv;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) a[i][j] = fmaf(-f, row[j], a[i][j]);
-                    if (tx == pb) a[i][m0] = f;
-                }
-            }
+        for (int q = 0; q < 8; ++q) {
+            const int e = tid + NT * q, r = e >> 4, c4 = (e & 15) * 4;
+            *reinterpret_cast<float4*>(X + r * SB + c4) = *reinterpret_cast<const float4*>(&At[r][c4]);
         }
     }
-    __syncthreads();
-    if (bad) {
-        if (blockIdx.x == 0 && tid == 0) set_status(s.status, h, KVC_ERR_NOT_SPD);
-        return;
-    }
-    // the block now holds -P
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-        *reinterpret_cast<float4*>(&Dn[R * ty + i][8 * tx]) = make_float4(-a[i][0], -a[i][1], -a[i][2], -a[i][3]);
-        *reinterpret_cast<float4*>(&Dn[R * ty + i][8 * tx + 4]) = make_float4(-a[i][4], -a[i][5], -a[i][6], -a[i][7]);
+    // the first pivot block is inverted here; later ones by the previous
+    // update launch (look-ahead)
+    if (!s.have_p) {
+        if (tid == 0) bad = 0;
+        __syncthreads();
+        chain_invert(Dn, grp, &bad, tid, k0, t);
+        __syncthreads();
+        if (bad) {
+            if (blockIdx.x == 0 && tid == 0) set_status(s.status, h, KVC_ERR_NOT_SPD);
+            return;
+        }
     }
     __syncthreads();
     if (diag) {
@@ -298,12 +393,75 @@ __global__ void __launch_bounds__(kUThreads, 2)
     const int t = s.offsets[h + 1] - s.offsets[h];
     const int k0 = s.k0;
     if (k0 >= t) return;
-    int I, J;
-    tri_tile(blockIdx.x, I, J);
-    if (I * UB >= t) return;
-    const float sg = (k0 + SB >= t) ? -1.f : 1.f;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    if (blockIdx.x == 0) {
+        // look-ahead, while the other CTAs update the tiles: the next pivot
+        // block D' = A_{k+1,k+1} - U_{k+1} A_{k,k+1} from the copies the pivot
+        // launch took and its U_{k+1}, then its inverse, for the next pivot
+        // launch.  The arrays are addressed from a shared-memory symbol (no
+        // integer round trip), so the compiler emits shared loads.
+        const int tid = threadIdx.x;
+        const int r1 = k0 + SB;
+        if (r1 >= t || tid >= kPivThreads) return;
+        float(*Dn)[kPS] = reinterpret_cast<float(*)[kPS]>(smem_raw);                        // D', then P
+        float(*Ut)[kPS] = reinterpret_cast<float(*)[kPS]>(smem_raw + SB * kPS * 4);         // Ut[p][r] = U_{k+1}[r][p]
+        float(*Vt)[kPS] = reinterpret_cast<float(*)[kPS]>(smem_raw + 2 * SB * kPS * 4);     // Vt[p][c] = A_{k,k+1}[p][c]
+        float(*grp)[4][SB] = reinterpret_cast<float(*)[4][SB]>(smem_raw + 3 * SB * kPS * 4);
+        int* bad = reinterpret_cast<int*>(smem_raw + 3 * SB * kPS * 4 + 2 * 4 * SB * 4);
+        const float* X = s.Xnext + (int64_t)h * 2 * SB * SB;
+        const float* Uh = s.U + (int64_t)h * SB * s.ldA + r1;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = tid + kPivThreads * q, r = e >> 4, c4 = (e & 15) * 4;
+            *reinterpret_cast<float4*>(&Vt[r][c4]) = *reinterpret_cast<const float4*>(X + r * SB + c4);
+            *reinterpret_cast<float4*>(&Dn[r][c4]) = *reinterpret_cast<const float4*>(X + SB * SB + r * SB + c4);
+            *reinterpret_cast<float4*>(&Ut[r][c4]) = *reinterpret_cast<const float4*>(Uh + r * s.ldA + c4);
+        }
+        sync128();
+        // D'[r][c] for the stored (lower) entries; thread (uy, ux): rows
+        // 8 uy .., columns 4 ux ..; each thread rewrites only its own entries
+        const int ux = tid & 15, uy = tid >> 4;
+        float dn[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 d4 = *reinterpret_cast<const float4*>(&Dn[8 * uy + i][4 * ux]);
+            dn[i][0] = d4.x; dn[i][1] = d4.y; dn[i][2] = d4.z; dn[i][3] = d4.w;
+        }
+#pragma unroll 4
+        for (int p = 0; p < SB; ++p) {
+            const float4 u0 = *reinterpret_cast<const float4*>(&Ut[p][8 * uy]);
+            const float4 u1 = *reinterpret_cast<const float4*>(&Ut[p][8 * uy + 4]);
+            const float4 v4 = *reinterpret_cast<const float4*>(&Vt[p][4 * ux]);
+            const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) dn[i][j] = fmaf(-uv[i], vv[j], dn[i][j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float4*>(&Dn[8 * uy + i][4 * ux]) = make_float4(dn[i][0], dn[i][1], dn[i][2], dn[i][3]);
+        if (tid == 0) *bad = 0;
+        sync128();
+        chain_invert(Dn, grp, bad, tid, r1, t);
+        if (*reinterpret_cast<volatile int*>(bad)) {
+            if (tid == 0) set_status(s.status, h, KVC_ERR_NOT_SPD);
+            return;
+        }
+        float* Ph = s.Pnext + (int64_t)h * SB * SB;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = tid + kPivThreads * q, r = e >> 4, c4 = (e & 15) * 4;
+            *reinterpret_cast<float4*>(Ph + r * SB + c4) = *reinterpret_cast<const float4*>(&Dn[r][c4]);
+        }
+        return;
+    }
+    int I, J;
+    tri_tile(blockIdx.x - 1, I, J);
+    if (I * UB >= t) return;
+    const float sg = (k0 + SB >= t) ? -1.f : 1.f;
     uint8_t* smA = sm;                       // A boxes (after the MMAs): (row quarter q, chunk c) at (4 q + c) * kABox
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + kUOps);
     uint64_t* fullA = full + 1;
@@ -512,7 +670,9 @@ bool make_map_bf16(CUtensorMap* m, const void* base, int cols, int64_t ld, int r
 bool make_map_f32(CUtensorMap* m, const void* base, int cols, int64_t ld, int rows, int H);    // tmap.cu
 
 // H^{-1} in place for every head (max_t bounds t_h).  U: fp32 [H][64][ldA];
-// split: bf16 [6][H][64][ldA] (U^T and V as three terms each); P: [H][64][64].
+// split: bf16 [6][H][64][ldA] (U^T and V as three terms each); P: fp32
+// [4][H][64][64] (the step's pivot inverse, the next pivot block's two inputs,
+// its inverse).
 cudaError_t launch_sweep_inverse(float* A, const int32_t* offsets, int H, int max_t, int64_t ldA, float* U,
                                  void* split, float* P, int32_t* status, cudaStream_t st) {
     const int nb = (max_t + SB - 1) / SB;
@@ -529,11 +689,14 @@ cudaError_t launch_sweep_inverse(float* A, const int32_t* offsets, int H, int ma
     if (!make_map_f32(&ma, A, (int)ldA, ldA, (int)ldA, H)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(k_sweep_update_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
     if (e != cudaSuccess) return e;
+    float* Xn = P + (int64_t)H * SB * SB;
+    float* Pn = P + 3 * (int64_t)H * SB * SB;
     for (int k = 0; k < nb; ++k) {
-        SweepArgs s{A, U, Us, Vs, P, offsets, ldA, ts, k * SB, status};
+        SweepArgs s{A, U, Us, Vs, P, Xn, Pn, offsets, ldA, ts, k * SB, status, k > 0};
         k_sweep_pivot<<<dim3(nb, H), kPivThreads, 0, st>>>(s);
-        k_sweep_update_tc<<<dim3(nu * (nu + 1) / 2, H), kUThreads, kUSmem, st>>>(mu[0], mu[1], mu[2], mv[0], mv[1],
-                                                                                  mv[2], ma, s);
+        // CTA 0 of each head forms and inverts the next pivot block
+        k_sweep_update_tc<<<dim3(nu * (nu + 1) / 2 + 1, H), kUThreads, kUSmem, st>>>(mu[0], mu[1], mu[2], mv[0],
+                                                                                      mv[1], mv[2], ma, s);
     }
     k_sweep_mirror<<<dim3(ntri, H), 256, 0, st>>>(A, offsets, ldA, status);
     return cudaGetLastError();
