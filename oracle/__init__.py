@@ -19,4 +19,5 @@ from .am import (  # noqa: F401
 )
 from .chunked import compact_chunked  # noqa: F401
 from .omp import compact_head_omp, omp_residual, omp_select  # noqa: F401
+from .periodic import attention_biased, compact_head_biased, periodic_compaction  # noqa: F401
 from .tam import compact_head_tam, plan_head  # noqa: F401

@@ -30,7 +30,7 @@ import numpy as np
 
 from .configs import Workload
 
-STREAM_CACHE, STREAM_QREF, STREAM_TEST, STREAM_BUDGET, STREAM_WINDOW = 0, 1, 2, 3, 4
+STREAM_CACHE, STREAM_QREF, STREAM_TEST, STREAM_BUDGET, STREAM_WINDOW, STREAM_BIAS = 0, 1, 2, 3, 4, 5
 
 
 def rng_for(w: Workload, h: int, stream: int) -> np.random.Generator:
@@ -229,3 +229,26 @@ def window_queries(w: Workload, h: int, R: int) -> np.ndarray:
         Q = rope(Q, j, w.rope_theta)
     return to_storage(Q, w.dtype)
 
+
+
+def compacted_cache_extras(w: Workload, h: int, n_old: int, V_f64: np.ndarray, off_frac: float = 0.03):
+    """Seeded stand-ins for what an earlier compaction leaves on the first
+    n_old positions of head h's cache (periodic compaction: t compacted
+    entries followed by new tokens):
+      bias  float32 [T]: log of a weight drawn from U(0.3, 4) on the first
+            n_old positions, -inf on a share `off_frac` of them (entries an
+            earlier fit switched off, never position 0), 0 on the new tokens;
+      V     float32 [T][d]: the cache's values with N(0, 0.05^2) added on the
+            first n_old positions (refitted values are not bfloat16 numbers),
+            unchanged on the new tokens.
+    Random numbers only: the values carry no compaction arithmetic."""
+    rng = rng_for(w, h, STREAM_BIAS)
+    T = V_f64.shape[0]
+    bias = np.zeros(T)
+    bias[:n_old] = np.log(rng.uniform(0.3, 4.0, n_old))
+    off = rng.random(n_old) < off_frac
+    off[0] = False
+    bias[:n_old][off] = -np.inf
+    V = np.array(V_f64, dtype=np.float64)
+    V[:n_old] += 0.05 * rng.standard_normal((n_old, V.shape[1]))
+    return bias.astype(np.float32), V.astype(np.float32)
