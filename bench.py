@@ -7,6 +7,12 @@ matrix, NNLS for beta, least squares for C_v), inputs resident in HBM.
 Metric: compacted head-tokens per second = sum over heads of T / step time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+                  [--layers L] [--select rms|omp|tam]
+
+The default workload is the largest one that fits one GPU: the 32-layer x
+8-KV-head Llama-3-8B-shaped cache (256 heads, T = 32768, n = 8192,
+t = 655).  --layers L keeps the first L layers of a multi-layer workload
+(same per-head shapes; for profiler captures of a bounded size).
 
 N > 1 runs one independent replica per GPU (launched by torch.distributed.run):
 heads are independent, so each rank compacts its own sequences with no
@@ -65,7 +71,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
@@ -116,25 +122,30 @@ def stage_work(w, buds):
     t = [int(x) for x in buds]
     st = sum(t)
     return {
+        "v_f16": ("bytes", 3.0 * 2 * T * d * H),
         "attn_fwd": ("flops", 4.0 * n * T * d * H),
         "colscore": ("flops", 2.0 * n * T * d * H),
         "select": ("bytes", 4.0 * T * H + 4.0 * st),
         "gather": ("bytes", 2.0 * st * d * b_in + st * d * (b_in + 4) + 4.0 * st),
         "masslogits": ("flops", 2.0 * n * d * st),
         "gram_a": ("flops", float(sum(n * ti * (ti + 1) for ti in t))),
-        "inv_h": ("flops", float(sum(float(ti) ** 3 for ti in t))),
+        # the inversions count the method's work, a factorisation of the t x t
+        # system (t^3 / 3), not the explicit inverse's t^3
+        "inv_h": ("flops", float(sum(float(ti) ** 3 / 3.0 for ti in t))),
         "gram_x": ("flops", float(sum(n * ti * (ti + 1) for ti in t))),
         "xto": ("flops", 2.0 * n * d * st),
         "chol_m": ("flops", float(sum(ti ** 3 / 3.0 for ti in t))),
         "cholsolve": ("flops", float(sum(2.0 * ti * ti * d for ti in t))),
-        "inv_m": ("flops", float(sum(float(ti) ** 3 for ti in t))),
+        "inv_m": ("flops", float(sum(float(ti) ** 3 / 3.0 for ti in t))),
         "apply_minv": ("flops", float(sum(2.0 * ti * ti * d for ti in t))),
     }
 
 
-# MUFU ex2 rate of a B300 (148 SMs x 16 per clock x 2032 MHz): the attention
-# passes take one exponential per logit and are co-bound by it.
-MUFU_PEAK_TEXP = 148 * 16 * 2.032e9 / 1e12
+# MUFU ex2 rate of a B300: 148 SMs x 32 per clock x 2032 MHz (Blackwell
+# Ultra doubled the special-function rate for attention; a probe of
+# independent ex2.approx chains sustained 29.8 per SM per clock).  The
+# attention passes take one exponential per logit and are co-bound by it.
+MUFU_PEAK_TEXP = 148 * 32 * 2.032e9 / 1e12
 
 
 def tensor_stages(w) -> set[str]:
@@ -240,6 +251,23 @@ def rank_workload(base, rank: int, world: int):
     return dataclasses.replace(base, seq_offset=base.seq_offset + rank * base.seqs)
 
 
+def limit_layers(w, layers):
+    """The first `layers` layers of a multi-layer workload (None: all)."""
+    import dataclasses
+    if not layers or layers >= w.layers:
+        return w
+    return dataclasses.replace(w, layers=layers, name=f"{w.name}-first{layers}layers")
+
+
+def oracle_sample(w):
+    """Heads the CPU baseline times: every head of a workload of at most 8,
+    else 4 heads evenly spaced over the flat head index (so over sequences,
+    layers and KV heads), whose mean time stands for every head."""
+    if w.H <= 8:
+        return list(range(w.H))
+    return [round(i * (w.H - 1) / 3) for i in range(4)]
+
+
 def max_over_ranks(x: float, dist, device) -> float:
     """Largest value of x over all ranks (the job's time is its slowest rank's)."""
     if dist is None:
@@ -325,7 +353,7 @@ def run_ours(args, rank, world, local_rank):
     import kv_cache_compaction_03_b300 as kvc
     from workloads.batch import generate
 
-    w = rank_workload(WORKLOADS[args.config], rank, world)
+    w = rank_workload(limit_layers(WORKLOADS[args.config], args.layers), rank, world)
     TENSOR_STAGES.clear()
     TENSOR_STAGES.update(tensor_stages(w))
     buds = make_budgets(w)
@@ -551,11 +579,12 @@ def run_ours(args, rank, world, local_rank):
     # ---- CPU oracle on a bounded sample (rank 0, N = 1 only)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        sample_heads = list(range(min(w.H, 8)))
+        sample_heads = oracle_sample(w)
         times, cores = time_oracle(w, sample_heads, buds)
         per_head = sum(times) / len(times)
+        extra = "" if len(times) == w.H else f"; {w.H} x the mean per-head time (extrapolated)"
         cpu = {"value": round(w.T / per_head, 2), "unit": "head-tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{len(times)} of {w.H} KV heads, {per_head:.2f} s per head (float64 numpy)"}
+               "sample": f"heads {sample_heads} of {w.H}, {per_head:.2f} s per head (float64 numpy){extra}"}
 
     line = {
         "metric": "compacted KV head-tokens/sec", "value": round(value, 1), "unit": "head-tokens/s",
@@ -610,7 +639,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", type=int, default=2, choices=sorted(WORKLOADS))
+    ap.add_argument("--config", type=int, default=3, choices=sorted(WORKLOADS))
+    ap.add_argument("--layers", type=int, default=0,
+                    help="keep only the first L layers of a multi-layer workload (profiling captures)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--select", default="rms", choices=["rms", "omp", "tam"],

@@ -53,11 +53,17 @@ typedef enum kvc_status {
                                   keys than t_h                                     */
     KVC_ERR_NOT_SPD = 17,      /* a Cholesky pivot was not positive                 */
     KVC_ERR_NNLS_MAXITER = 18, /* NNLS pivoting hit its iteration or set-size cap;
-                                  outputs hold the last (clamped) iterate           */
+                                  the head's outputs are not written; workspace
+                                  item W holds the last clamped iterate        */
     KVC_ERR_NONFINITE = 19,    /* NaN/Inf in the inputs or an intermediate          */
-    KVC_ERR_TIMEOUT = 20       /* a bounded device-side wait gave up (about one
-                                  second without progress); the kernel released
-                                  its resources and left the head unfinished       */
+    KVC_ERR_TIMEOUT = 20,      /* a bounded device-side wait gave up (after
+                                  kvc_params.wait_timeout_us, one second by
+                                  default); the kernel released its resources
+                                  and left the head unfinished                 */
+    KVC_ERR_DEBUG_BOUNDS = 21  /* debug build only (libkvc_debug.so, compiled
+                                  with KVC_DEBUG): a kernel found an index read
+                                  from data outside the buffer it addresses and
+                                  skipped the access                           */
 } kvc_status;
 
 typedef enum kvc_dtype { KVC_DTYPE_BF16 = 0, KVC_DTYPE_F32 = 1 } kvc_dtype;
@@ -83,10 +89,26 @@ typedef struct kvc_params {
                              tr(X^T X)/t (1e-2)                                   */
     int32_t nnls_max_iter;  /* block-pivoting iterations (default 32)             */
     int32_t nnls_max_zero;  /* cap on weights held at zero (default 512)          */
-    int32_t refine_iters;   /* NNLS iterative-refinement steps (default 2)        */
+    int32_t refine_iters;   /* NNLS iterative-refinement steps (default 1: the
+                               residual is formed from A' itself and the ridge
+                               from the exact squares of A', and one step
+                               reaches the fixed point to ~1e-5 in beta)   */
     int32_t keep_first;     /* positions [0, keep_first) are always kept          */
     int32_t keep_last;      /* positions [T-keep_last, T) are always kept         */
     uint32_t flags;         /* KVC_FLAG_* bits; other bits must be 0              */
+    uint32_t wait_timeout_us; /* limit of every bounded device-side wait of the
+                             tensor-core kernels, in microseconds at the
+                             device's peak SM clock (default 1000000, i.e.
+                             one second; must be >= 1).  A wait that runs out
+                             ends its kernel's work on that head: the kernel
+                             waits (under its own one-second limit) for the
+                             copies and tensor-core operations it has already
+                             issued, releases its tensor memory and writes
+                             KVC_ERR_TIMEOUT for the head.  Limits below about
+                             half a millisecond are polled without suspending
+                             the waiting thread.  Short limits are for tests
+                             of that path: a limit below the normal latency
+                             of a tile load times out on purpose.            */
 } kvc_params;
 
 /* kvc_params.flags: record a CUDA event on the stream after every stage of
@@ -132,6 +154,12 @@ kvc_status kvc_workspace_size(const kvc_problem* p, const kvc_params* prm, size_
  *            size and iterations)
  *   5 ORDER  int32 [H][max_t]: keys in the order the pursuit chose them
  *            (KVC_FLAG_SELECT_OMP only; INVALID_ARG otherwise)
+ *   6 L2     fp32 [H][n][ldA], ldA = max_t rounded up to a multiple of 64:
+ *            log2 of the kept keys' relative mass A'_qi = exp(S_q,idx_i -
+ *            lse_q) in columns i < t_h of head h (later columns
+ *            unspecified).  Intact after the call only with
+ *            KVC_FLAG_CHOLESKY_CV: the default C_v solve reuses this region
+ *            for its operand terms once the log-masses have been read.
  * prm->keep_first / keep_last are not checked against p->T here (the layout
  * does not depend on them).
  * Host-only.  Errors: INVALID_ARG (bad problem/params or unknown item). */
@@ -242,6 +270,52 @@ kvc_status kvc_compact_chunked(const kvc_problem* p, const kvc_params* prm, int3
                                int32_t* idx_out, void* C_k, float* beta, float* C_v,
                                int32_t* head_status,
                                void* workspace, size_t workspace_bytes, kvc_stream_t stream);
+
+/* Compact a cache that carries per-key biases and fp32 values: a compacted
+ * cache, compacted again.  This is the step of periodic compaction
+ * ("Thought-Aware KV Cache Compaction" explainer, section 2 D "Compaction
+ * periodique": every P new tokens the t compacted entries plus the P new
+ * tokens are compacted back to t, so the cache stays between t and t + P;
+ * "Fast KV Compaction via Attention Matching", section 4, "Compaction en
+ * ligne": repeated compaction during decoding).
+ *
+ * The caller concatenates, per head, the compacted entries (C_k, beta, C_v of
+ * an earlier call) and the new tokens (their keys, bias 0, their values in
+ * fp32).  The steps are those of kvc_compact with the biases in the logits,
+ * S_qj = q . K_j * scale + bias_j, so that the targets (attention mass and
+ * outputs of the reference queries) are those of the cache as it stands:
+ *   1. lse and O = softmax(S) V over the biased cache;
+ *   2. key scores sqrt(mean_q exp(S_qj - lse_q)^2); the t_h largest kept;
+ *   3. w' >= 0 by the NNLS on A'_qi = exp(S_q,idx_i - lse_q) (biases
+ *      included) with ridge mu ||w' - 1||^2, so that the fit scales the kept
+ *      entries' existing weights and pulls toward "no change";
+ *   4. beta_out = bias_idx + log w' (-INFINITY where w' = 0 or the bias
+ *      is -INFINITY);
+ *   5. C_v by least squares against O with ridge lambda ||C_v - V[idx]||^2.
+ * Keeping every entry (t_h = T) returns the cache unchanged (beta = bias,
+ * C_v = V, up to rounding).
+ *
+ * Arguments as kvc_compact, except (device):
+ *   K        [H][T][d] dtype (the kept keys are exact copies of these rows)
+ *   bias     fp32 [H][T] natural-log units; -INFINITY switches an entry off
+ *            (its attention is 0); NaN or +INFINITY -> NONFINITE for the head;
+ *            4-byte aligned
+ *   V        fp32 [H][T][d], 16-byte aligned
+ *   workspace at least kvc_workspace_size_biased bytes
+ * A head whose every key is switched off gets NONFINITE.  KVC_FLAG_SELECT_OMP
+ * must be unset (INVALID_ARG); keep_first / keep_last apply as in kvc_compact.
+ * Errors: INVALID_ARG, ALIGN, WORKSPACE, CUDA (nothing enqueued on the first
+ * three). */
+kvc_status kvc_compact_biased(const kvc_problem* p, const kvc_params* prm,
+                              const void* Q_ref, const void* K, const float* bias, const float* V,
+                              const int32_t* budgets, const int32_t* offsets,
+                              int32_t* idx_out, void* C_k, float* beta, float* C_v,
+                              int32_t* head_status,
+                              void* workspace, size_t workspace_bytes, kvc_stream_t stream);
+
+/* Bytes of workspace kvc_compact_biased needs.  Host-only.  Errors:
+ * INVALID_ARG. */
+kvc_status kvc_workspace_size_biased(const kvc_problem* p, const kvc_params* prm, size_t* bytes);
 
 /* Bytes of workspace kvc_compact_chunked needs for *p cut into `chunks`
  * chunks per head (that of the per-chunk problem).  Host-only.

@@ -15,7 +15,10 @@ import os
 from dataclasses import dataclass
 
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG_DIR, "libkvc.so")
+# KVC_LIBRARY=debug loads the build whose kernels check data-derived indices
+# (python -m kv_cache_compaction_03_b300.build --debug)
+LIB_NAME = "libkvc_debug.so" if os.environ.get("KVC_LIBRARY") == "debug" else "libkvc.so"
+LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
 # status codes (include/kvc.h)
 OK = 0
@@ -30,11 +33,12 @@ ERR_NOT_SPD = 17
 ERR_NNLS_MAXITER = 18
 ERR_NONFINITE = 19
 ERR_TIMEOUT = 20
+ERR_DEBUG_BOUNDS = 21
 
 DTYPE_BF16 = 0
 DTYPE_F32 = 1
 
-WS_O, WS_LSE2, WS_SCORE, WS_W, WS_HEAD, WS_ORDER = 0, 1, 2, 3, 4, 5
+WS_O, WS_LSE2, WS_SCORE, WS_W, WS_HEAD, WS_ORDER, WS_L2 = 0, 1, 2, 3, 4, 5, 6
 
 
 class Problem(ctypes.Structure):
@@ -46,7 +50,8 @@ class Params(ctypes.Structure):
     _fields_ = [("scale", ctypes.c_float), ("eps_mu", ctypes.c_float), ("eps_lambda", ctypes.c_float),
                 ("nnls_max_iter", ctypes.c_int32), ("nnls_max_zero", ctypes.c_int32),
                 ("refine_iters", ctypes.c_int32), ("keep_first", ctypes.c_int32),
-                ("keep_last", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+                ("keep_last", ctypes.c_int32), ("flags", ctypes.c_uint32),
+                ("wait_timeout_us", ctypes.c_uint32)]
 
 
 class HeadRecord(ctypes.Structure):
@@ -63,7 +68,8 @@ class KvcError(RuntimeError):
 _lib = None
 EXPORTS = ("kvc_default_params", "kvc_workspace_size", "kvc_workspace_offset", "kvc_compact",
            "kvc_compact_noalloc", "kvc_compact_chunked", "kvc_workspace_size_chunked", "kvc_compact_tam",
-           "kvc_workspace_size_tam", "kvc_attend", "kvc_stage_times", "kvc_status_string", "kvc_version")
+           "kvc_workspace_size_tam", "kvc_compact_biased", "kvc_workspace_size_biased", "kvc_attend",
+           "kvc_stage_times", "kvc_status_string", "kvc_version")
 FLAG_STAGE_TIMING = 1
 FLAG_CHOLESKY_CV = 2
 FLAG_SELECT_OMP = 4
@@ -75,7 +81,8 @@ def lib() -> ctypes.CDLL:
     if _lib is not None:
         return _lib
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"libkvc.so not built at {LIB_PATH}; run python -m kv_cache_compaction_03_b300.build")
+        raise ImportError(f"{LIB_NAME} not built at {LIB_PATH}; run python -m kv_cache_compaction_03_b300.build"
+                          + (" --debug" if LIB_NAME != "libkvc.so" else ""))
     L = ctypes.CDLL(LIB_PATH)
     vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
     P, PP = ctypes.POINTER(Problem), ctypes.POINTER(Params)
@@ -89,6 +96,8 @@ def lib() -> ctypes.CDLL:
     L.kvc_compact_tam.argtypes = [P, PP, vp, vp, vp, vp, i32, vp, i32, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp,
                                   vp, vp, vp, sz, vp]
     L.kvc_workspace_size_tam.argtypes = [P, PP, i32, i32, ctypes.POINTER(sz)]
+    L.kvc_compact_biased.argtypes = [P, PP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.kvc_workspace_size_biased.argtypes = [P, PP, ctypes.POINTER(sz)]
     L.kvc_attend.argtypes = [P, vp, i32, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp]
     L.kvc_stage_times.argtypes = [ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_float),
                                   ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i32), ctypes.POINTER(i32), i32]
@@ -98,7 +107,7 @@ def lib() -> ctypes.CDLL:
     L.kvc_version.restype = ctypes.c_char_p
     for f in ("kvc_default_params", "kvc_workspace_size", "kvc_workspace_offset", "kvc_compact",
               "kvc_compact_noalloc", "kvc_compact_chunked", "kvc_workspace_size_chunked", "kvc_compact_tam",
-              "kvc_workspace_size_tam", "kvc_attend"):
+              "kvc_workspace_size_tam", "kvc_compact_biased", "kvc_workspace_size_biased", "kvc_attend"):
         getattr(L, f).restype = ctypes.c_int
     _lib = L
     return L
@@ -221,6 +230,26 @@ def compact_tam(problem: Problem, params: Params | None, Q_ref, K, V, Q_win, n_w
                                  _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
+def workspace_size_biased(problem: Problem, params: Params | None = None) -> int:
+    out = ctypes.c_size_t()
+    rc = lib().kvc_workspace_size_biased(ctypes.byref(problem), ctypes.byref(params) if params else None,
+                                         ctypes.byref(out))
+    if rc:
+        raise KvcError(rc, "kvc_workspace_size_biased")
+    return out.value
+
+
+def compact_biased(problem: Problem, params: Params | None, Q_ref, K, bias, V, budgets, offsets, idx_out, C_k, beta,
+                   C_v, head_status, workspace, workspace_bytes: int, stream=None) -> int:
+    """kvc_compact_biased: compaction of a cache whose keys carry biases and
+    whose values are fp32 (periodic compaction).  Returns the call-level
+    status (0 = enqueued)."""
+    return lib().kvc_compact_biased(ctypes.byref(problem), ctypes.byref(params) if params else None, _ptr(Q_ref),
+                                    _ptr(K), _ptr(bias), _ptr(V), _ptr(budgets), _ptr(offsets), _ptr(idx_out),
+                                    _ptr(C_k), _ptr(beta), _ptr(C_v), _ptr(head_status), _ptr(workspace),
+                                    int(workspace_bytes), _stream(stream))
+
+
 def attend(problem: Problem, Q, n_q: int, C_k, beta, C_v, offsets, O_out, head_status, scale: float = 0.0,
            stream=None) -> int:
     """kvc_attend on caller-owned buffers.  Returns the call-level status."""
@@ -301,6 +330,37 @@ def compact_tensors(Q_ref, K, V, budgets, params: Params | None = None, stream=N
     rc = compact(prob, prm, Q_ref, K, V, budgets, offsets, idx, Ck, beta, Cv, status, ws, ws_bytes, stream)
     if rc:
         raise KvcError(rc, "kvc_compact")
+    return Compacted(idx, Ck, beta, Cv, offsets, status, ws, prob, prm)
+
+
+def compact_biased_tensors(Q_ref, K, bias, V, budgets, params: Params | None = None, stream=None) -> Compacted:
+    """Allocate outputs and workspace with torch, then call kvc_compact_biased.
+
+    Q_ref [H][n][d] and K [H][T][d] (bf16 or fp32), bias fp32 [H][T], V fp32
+    [H][T][d], budgets int32 [H], all on the same CUDA device.
+    """
+    import torch
+    H, n, d = Q_ref.shape
+    T = K.shape[1]
+    dev = Q_ref.device
+    b64 = budgets.to(torch.int64)
+    offsets = torch.zeros(H + 1, dtype=torch.int32, device=dev)
+    offsets[1:] = torch.cumsum(b64, 0).to(torch.int32)
+    total = int(offsets[-1].item())
+    max_t = int(b64.max().item())
+    prob = make_problem(H, n, T, d, torch_dtype_code(Q_ref.dtype), max_t)
+    prm = params if params is not None else default_params()
+    ws_bytes = workspace_size_biased(prob, prm)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    idx = torch.empty(total, dtype=torch.int32, device=dev)
+    Ck = torch.empty(total, d, dtype=Q_ref.dtype, device=dev)
+    beta = torch.empty(total, dtype=torch.float32, device=dev)
+    Cv = torch.empty(total, d, dtype=torch.float32, device=dev)
+    status = torch.empty(H, dtype=torch.int32, device=dev)
+    rc = compact_biased(prob, prm, Q_ref, K, bias, V, budgets, offsets, idx, Ck, beta, Cv, status, ws, ws_bytes,
+                        stream)
+    if rc:
+        raise KvcError(rc, "kvc_compact_biased")
     return Compacted(idx, Ck, beta, Cv, offsets, status, ws, prob, prm)
 
 

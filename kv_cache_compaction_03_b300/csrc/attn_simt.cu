@@ -7,6 +7,9 @@
 // They serve every dtype and shape; the bf16 hot path also has tensor-core
 // versions.  Logits are carried in log2 units (x * scale * log2 e) so that
 // every kernel rounds them the same way; lse is stored in the same units.
+// An optional per-key input bias (bias2, log2 units, [H][Tb] with Tb = T
+// rounded up to 256; -inf switches a key off) is added to the logits: the cache of an earlier compaction, whose
+// keys carry their fitted biases (periodic compaction).
 #include "common.cuh"
 
 namespace kvc {
@@ -69,7 +72,8 @@ template <typename TIn, int D>
 __global__ void __launch_bounds__(NT) k_attn_fwd(const TIn* __restrict__ Q, const TIn* __restrict__ K,
                                                  const TIn* __restrict__ V, int n, int T, float c2,
                                                  float* __restrict__ O, float* __restrict__ lse2,
-                                                 const int32_t* __restrict__ status, int qdiv) {
+                                                 int32_t* __restrict__ status, int qdiv,
+                                                 const float* __restrict__ bias2) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     extern __shared__ float sm[];
@@ -108,7 +112,8 @@ __global__ void __launch_bounds__(NT) k_attn_fwd(const TIn* __restrict__ Q, cons
             float mx = -INFINITY;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                s[i][j] = (tx + 16 * j < kv) ? s[i][j] * c2 : -INFINITY;
+                const float b = bias2 && tx + 16 * j < kv ? bias2[h * round_up(T, 256) + k0 + tx + 16 * j] : 0.f;
+                s[i][j] = (tx + 16 * j < kv) ? fmaf(s[i][j], c2, b) : -INFINITY;
                 mx = fmaxf(mx, s[i][j]);
             }
 #pragma unroll
@@ -118,7 +123,8 @@ __global__ void __launch_bounds__(NT) k_attn_fwd(const TIn* __restrict__ Q, cons
             float rs = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                float p = exp2f(s[i][j] - mnew);
+                // (mnew = -inf only while every key so far is switched off)
+                float p = s[i][j] == -INFINITY ? 0.f : exp2f(s[i][j] - mnew);
                 Ps[(ty * 4 + i) * (BN + 1) + tx + 16 * j] = p;
                 rs += p;
             }
@@ -151,6 +157,8 @@ __global__ void __launch_bounds__(NT) k_attn_fwd(const TIn* __restrict__ Q, cons
 #pragma unroll
             for (int c = 0; c < DC; ++c) O[((int64_t)h * n + q) * D + tx + 16 * c] = o[i][c] * inv;
             if (tx == 0) lse2[(int64_t)h * n + q] = m[i] + log2f(l[i]);
+            // every key switched off by its bias: no attention to match
+            if (tx == 0 && !(l[i] > 0.f)) set_status(status, h, KVC_ERR_NONFINITE);
         }
     }
 }
@@ -163,7 +171,7 @@ template <typename TIn, int D, bool MEAN = false>
 __global__ void __launch_bounds__(NT) k_colscore(const TIn* __restrict__ Q, const TIn* __restrict__ K,
                                                  const float* __restrict__ lse2, int n, int T, float c2,
                                                  float* __restrict__ score, const int32_t* __restrict__ status,
-                                                 int qdiv) {
+                                                 int qdiv, const float* __restrict__ bias2) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     extern __shared__ float sm[];
@@ -177,6 +185,10 @@ __global__ void __launch_bounds__(NT) k_colscore(const TIn* __restrict__ Q, cons
     const int kv = min(BN, T - k0);
     load_tile<TIn, D>(Ks, K + ((int64_t)h * T + k0) * D, kv, D);
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, cmp[4] = {0.f, 0.f, 0.f, 0.f};   // Kahan sums per key
+    float kb[4];                                                          // the keys' input biases
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        kb[j] = bias2 && tx + 16 * j < kv ? bias2[h * round_up(T, 256) + k0 + tx + 16 * j] : 0.f;
     for (int q0 = 0; q0 < n; q0 += BM) {
         const int qv = min(BM, n - q0);
         __syncthreads();
@@ -190,7 +202,7 @@ __global__ void __launch_bounds__(NT) k_colscore(const TIn* __restrict__ Q, cons
             float part = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float x = s[i][j] * c2 - Ls[ty * 4 + i];   // log2 of P
+                const float x = fmaf(s[i][j], c2, kb[j]) - Ls[ty * 4 + i];   // log2 of P
                 part += MEAN ? exp2f(x) : exp2f(x + x);          // P or P^2
             }
             const float y = part - cmp[j];
@@ -211,13 +223,15 @@ __global__ void __launch_bounds__(NT) k_colscore(const TIn* __restrict__ Q, cons
 }
 
 // ---------------------------------------------------------------- mass logits
-// grid (ceil(max_t/64), ceil(n/64), H).  l2[h][q][i] = S c2 - lse2_q for i < t_h,
-// -inf for t_h <= i < round_up(t_h, 64).  C_k is the compacted key buffer.
+// grid (ceil(max_t/64), ceil(n/64), H).  l2[h][q][i] = S c2 + bk_i - lse2_q
+// for i < t_h, -inf for t_h <= i < round_up(t_h, 64).  C_k is the compacted
+// key buffer; bk (optional, [sum t], log2 units) the kept keys' input biases.
 template <typename TIn, int D>
 __global__ void __launch_bounds__(NT) k_masslogits(const TIn* __restrict__ Q, const TIn* __restrict__ Ck,
                                                    const float* __restrict__ lse2, const int32_t* __restrict__ offsets,
                                                    int n, int64_t ldA, float c2, float* __restrict__ L2,
-                                                   const int32_t* __restrict__ status, int qdiv) {
+                                                   const int32_t* __restrict__ status, int qdiv,
+                                                   const float* __restrict__ bk) {
     const int h = blockIdx.z;
     if (!head_ok(status, h)) return;
     const int off = offsets[h];
@@ -245,7 +259,7 @@ __global__ void __launch_bounds__(NT) k_masslogits(const TIn* __restrict__ Q, co
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int c = i0 + tx + 16 * j;
-            row[c] = (c < th) ? s[i][j] * c2 - l : -INFINITY;
+            row[c] = (c < th) ? fmaf(s[i][j], c2, bk ? bk[off + c] : 0.f) - l : -INFINITY;
         }
     }
 }
@@ -353,26 +367,28 @@ __global__ void __launch_bounds__(NT) k_attend(const TIn* __restrict__ Q, int nq
 // ---------------------------------------------------------------- launchers
 template <typename TIn, int D>
 static cudaError_t launch_attn_simt_t(const void* Q, const void* K, const void* V, int H, int n, int T, float c2,
-                                      float* O, float* lse2, const int32_t* status, int qdiv, cudaStream_t st) {
+                                      float* O, float* lse2, int32_t* status, int qdiv, const float* bias2,
+                                      cudaStream_t st) {
     constexpr int P = D + 1;
     size_t smem = (size_t)(BM * P + BN * P + BN * D + BM * (BN + 1)) * sizeof(float);
     auto kern = k_attn_fwd<TIn, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((n + BM - 1) / BM, H);
-    kern<<<grid, NT, smem, st>>>((const TIn*)Q, (const TIn*)K, (const TIn*)V, n, T, c2, O, lse2, status, qdiv);
+    kern<<<grid, NT, smem, st>>>((const TIn*)Q, (const TIn*)K, (const TIn*)V, n, T, c2, O, lse2, status, qdiv, bias2);
     return cudaGetLastError();
 }
 template <typename TIn, int D>
 static cudaError_t launch_colscore_simt_t(const void* Q, const void* K, const float* lse2, int H, int n, int T,
-                                          float c2, float* score, const int32_t* status, int qdiv, cudaStream_t st) {
+                                          float c2, float* score, const int32_t* status, int qdiv,
+                                          const float* bias2, cudaStream_t st) {
     constexpr int P = D + 1;
     size_t smem = (size_t)(BN * P + BM * P + BM) * sizeof(float) + 16 * BN * sizeof(double) + 8;
     auto kern = k_colscore<TIn, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((T + BN - 1) / BN, H);
-    kern<<<grid, NT, smem, st>>>((const TIn*)Q, (const TIn*)K, lse2, n, T, c2, score, status, qdiv);
+    kern<<<grid, NT, smem, st>>>((const TIn*)Q, (const TIn*)K, lse2, n, T, c2, score, status, qdiv, bias2);
     return cudaGetLastError();
 }
 template <typename TIn, int D>
@@ -384,20 +400,20 @@ static cudaError_t launch_colmean_simt_t(const void* Q, const void* K, const flo
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((T + BN - 1) / BN, H);
-    kern<<<grid, NT, smem, st>>>((const TIn*)Q, (const TIn*)K, lse2, n, T, c2, out, status, 1);
+    kern<<<grid, NT, smem, st>>>((const TIn*)Q, (const TIn*)K, lse2, n, T, c2, out, status, 1, nullptr);
     return cudaGetLastError();
 }
 template <typename TIn, int D>
 static cudaError_t launch_masslogits_t(const void* Q, const void* Ck, const float* lse2, const int32_t* offsets,
                                        int H, int n, int max_t, int64_t ldA, float c2, float* L2,
-                                       const int32_t* status, int qdiv, cudaStream_t st) {
+                                       const int32_t* status, int qdiv, const float* bk, cudaStream_t st) {
     constexpr int P = D + 1;
     size_t smem = (size_t)(BM * P + BN * P) * sizeof(float);
     auto kern = k_masslogits<TIn, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((max_t + BN - 1) / BN, (n + BM - 1) / BM, H);
-    kern<<<grid, NT, smem, st>>>((const TIn*)Q, (const TIn*)Ck, lse2, offsets, n, ldA, c2, L2, status, qdiv);
+    kern<<<grid, NT, smem, st>>>((const TIn*)Q, (const TIn*)Ck, lse2, offsets, n, ldA, c2, L2, status, qdiv, bk);
     return cudaGetLastError();
 }
 template <typename TIn, int D>
@@ -419,9 +435,11 @@ static cudaError_t launch_attend_t(const void* Q, int nq, const void* Ck, const 
          ? ((d) == 128 ? FN<__nv_bfloat16, 128>(__VA_ARGS__) : FN<__nv_bfloat16, 64>(__VA_ARGS__)) \
          : ((d) == 128 ? FN<float, 128>(__VA_ARGS__) : FN<float, 64>(__VA_ARGS__)))
 
+// bias2 (optional): per-key input bias [H][round_up(T, 256)], log2 units.
 cudaError_t launch_attn_fwd_simt(int dtype, int d, const void* Q, const void* K, const void* V, int H, int n, int T,
-                                 float c2, float* O, float* lse2, const int32_t* status, int qdiv, cudaStream_t st) {
-    return KVC_DISPATCH(dtype, d, launch_attn_simt_t, Q, K, V, H, n, T, c2, O, lse2, status, qdiv, st);
+                                 float c2, float* O, float* lse2, int32_t* status, int qdiv, const float* bias2,
+                                 cudaStream_t st) {
+    return KVC_DISPATCH(dtype, d, launch_attn_simt_t, Q, K, V, H, n, T, c2, O, lse2, status, qdiv, bias2, st);
 }
 // mean_q softmax_j over queries Q (own lse2): out [H][T]
 cudaError_t launch_colmean_simt(int dtype, int d, const void* Q, const void* K, const float* lse2, int H, int n, int T,
@@ -429,14 +447,15 @@ cudaError_t launch_colmean_simt(int dtype, int d, const void* Q, const void* K, 
     return KVC_DISPATCH(dtype, d, launch_colmean_simt_t, Q, K, lse2, H, n, T, c2, out, status, st);
 }
 cudaError_t launch_colscore_simt(int dtype, int d, const void* Q, const void* K, const float* lse2, int H, int n,
-                                 int T, float c2, float* score, const int32_t* status, int qdiv, cudaStream_t st) {
-    return KVC_DISPATCH(dtype, d, launch_colscore_simt_t, Q, K, lse2, H, n, T, c2, score, status, qdiv, st);
+                                 int T, float c2, float* score, const int32_t* status, int qdiv, const float* bias2,
+                                 cudaStream_t st) {
+    return KVC_DISPATCH(dtype, d, launch_colscore_simt_t, Q, K, lse2, H, n, T, c2, score, status, qdiv, bias2, st);
 }
 cudaError_t launch_masslogits(int dtype, int d, const void* Q, const void* Ck, const float* lse2,
                               const int32_t* offsets, int H, int n, int max_t, int64_t ldA, float c2, float* L2,
-                              const int32_t* status, int qdiv, cudaStream_t st) {
+                              const int32_t* status, int qdiv, const float* bk, cudaStream_t st) {
     return KVC_DISPATCH(dtype, d, launch_masslogits_t, Q, Ck, lse2, offsets, H, n, max_t, ldA, c2, L2, status, qdiv,
-                        st);
+                        bk, st);
 }
 cudaError_t launch_attend(int dtype, int d, const void* Q, int nq, const void* Ck, const float* beta,
                           const float* Cv, const int32_t* offsets, int H, float c2, float* O, int32_t* status,

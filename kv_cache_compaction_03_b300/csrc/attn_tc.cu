@@ -1,18 +1,22 @@
 // Tensor-core (tcgen05 + TMEM + TMA) kernels for the two attention passes of
 // the compaction ("Fast KV Compaction via Attention Matching", section 2):
 //
-//   k_attn_fwd_tc   Q-major flash pass: S = Q K^T * scale on the tensor cores,
-//                   online softmax in registers, P written back into tensor
-//                   memory as two bf16 terms (P = P_hi + P_lo, ~16 significant
-//                   bits), O += P_hi V + P_lo V on the tensor cores; outputs
-//                   the reference outputs O = softmax(S) V (fp32) and the
-//                   log-mass lse_q (log2 units).  A single bf16 term would
-//                   leave O with ~1e-3 relative error, which the least-squares
-//                   fit of C_v amplifies past its tolerance.
+//   k_attn_fwd_tc   Q-major flash pass: S = Q K^T * scale on the tensor cores
+//                   (bf16), online softmax in registers, P written back into
+//                   tensor memory as fp16 (11 significant bits), O += P V16
+//                   on the tensor cores with V16 the values in fp16 under a
+//                   per-head power-of-two scale (vconv.cu); outputs the
+//                   reference outputs O = softmax(S) V (fp32) and the
+//                   log-mass lse_q (log2 units).  A bf16 P (8 bits) would
+//                   leave O with ~1e-3 relative error, which the
+//                   least-squares fit of C_v carries past its tolerance; fp16
+//                   leaves ~5e-5.
 //   k_masslogits_tc log2 of the relative mass matrix A' for the kept keys,
 //                   S = Q C_k^T on the tensor cores; the epilogue also
-//                   writes A' as bf16 hi / lo terms (the Gram operand) and
-//                   per-tile column sums of A' (partials of b = A'^T 1).
+//                   writes A' as bf16 hi / lo terms (the Gram operand),
+//                   per-tile column sums of A' (partials of b = A'^T 1) and
+//                   per-tile sums of A'^2 (partials of tr(A'^T A'), the
+//                   scale of the NNLS ridge).
 //   k_colscore_tc   K-major pass: S^T = K Q^T per key tile, then every key
 //                   row sums exp(2 (S - lse)) over all queries: the RMS
 //                   attention score of each key (key selection aggregated
@@ -20,6 +24,14 @@
 //
 // Q heads: head h reads reference queries of head h / qdiv (qdiv > 1 when
 // several chunks of one cache share its queries).
+//
+// With BIAS the keys carry an input bias (the cache of an earlier
+// compaction: periodic compaction), bias2 [H][Tb] fp32 in log2 units with Tb
+// = T rounded up to 256 and -inf padding; it is added to every logit.  The
+// forward pass brings each tile's 128 biases into shared memory with the K
+// tile (one 512-byte bulk copy on the same barrier); the key-score pass
+// holds its row's bias in a register; the mass pass reads the kept keys'
+// biases bk [sum t] (log2 units).
 //
 // bf16 inputs, fp32 accumulation.  One CTA = 10 warps and two 128-row
 // tiles (query tiles for the forward pass, key tiles for the scores):
@@ -64,33 +76,34 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_addr, int kk) {
 }
 
 // ------------------------------------------------------------ attention forward
-template <int D, int NS>
+template <int D, int NS, bool BIAS>
 struct FwdLayout {
     static constexpr int kTile = (D / 64) * kBox;
     static constexpr int kQ = 0;                  // two query tiles
     static constexpr int kK = kQ + 2 * kTile;
     static constexpr int kV = kK + NS * kTile;
-    static constexpr int kBar = kV + NS * kTile;
+    static constexpr int kBias = kV + NS * kTile; // [NS][128] fp32 key biases (BIAS)
+    static constexpr int kBar = kBias + (BIAS ? NS * TB * 4 : 0);
     static constexpr int kBytes = kBar + 256 + 1024;     // + alignment slack
 };
 constexpr int kFwdThreads = 320;          // TMA warp, MMA warp, two softmax warpgroups
 
 // One CTA = two query tiles g = 0, 1 of 128 rows (rows q0 + 128 g ..).  TMEM
-// columns: tile g owns S_g at 256 g (128 columns; after the softmax P_hi
-// sits in its first 64 columns and P_lo in the next 64) and O_g at
-// 256 g + 128.  The MMA thread interleaves the tiles so that one tile's
+// columns: tile g owns S_g at 256 g (128 columns; after the softmax the fp16
+// P sits in its first 64 columns) and O_g at 256 g + 128.  The MMA thread interleaves the tiles so that one tile's
 // softmax overlaps the other tile's products:
 //   QK_0[j], PV_1[j-1], QK_1[j], PV_0[j], QK_0[j+1], PV_1[j], ...
 // tcgen05 operations of one thread complete in issue order, so when S_g[j]
 // is complete every earlier P V product of tile g is too: the softmax may
 // rescale O_g in place without another wait, and QK_g[j+1] may overwrite
 // the P_g[j] that PV_g[j] read.
-template <int D, int NS>
+template <int D, int NS, bool BIAS>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     k_attn_fwd_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                   const __grid_constant__ CUtensorMap mV, int n, int T, float c2, float* __restrict__ O,
-                  float* __restrict__ lse2, int32_t* __restrict__ status, int qdiv) {
-    using L = FwdLayout<D, NS>;
+                  float* __restrict__ lse2, const int32_t* __restrict__ vexp, int32_t* __restrict__ status,
+                  int qdiv, long long wait_limit, const float* __restrict__ bias2, int Tb) {
+    using L = FwdLayout<D, NS, BIAS>;
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     extern __shared__ uint8_t smem_raw[];
@@ -145,10 +158,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             int issued = 0;
             for (int j = 0; j < nt; ++j) {
                 const int s = j % NS;
-                if (j >= NS && !mbar_wait(kv_empty + s, (uint32_t)((j / NS) - 1) & 1u, abort_flag)) break;
-                mbar_expect_tx(k_full + s, kTileBytes);
+                if (j >= NS && !mbar_wait(kv_empty + s, (uint32_t)((j / NS) - 1) & 1u, abort_flag, wait_limit)) break;
+                mbar_expect_tx(k_full + s, kTileBytes + (BIAS ? TB * 4u : 0u));
                 for (int c = 0; c < D / 64; ++c)
                     tma_load_3d(sm + L::kK + s * L::kTile + c * kBox, &mK, k_full + s, c * 64, j * TB, h);
+                if (BIAS) bulk_load(sm + L::kBias + s * TB * 4, bias2 + (int64_t)h * Tb + (int64_t)j * TB, TB * 4u,
+                                    k_full + s);
                 mbar_expect_tx(v_full + s, kTileBytes);
                 for (int c = 0; c < D / 64; ++c)
                     tma_load_3d(sm + L::kV + s * L::kTile + c * kBox, &mV, v_full + s, c * 64, j * TB, h);
@@ -165,7 +180,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+            constexpr uint32_t idesc_pv = idesc_f16(128, D, false, true);
             const uint32_t aQ0 = smem_addr(sm + L::kQ);
             auto qk = [&](int g, int j) {
                 const uint32_t aQ = aQ0 + (uint32_t)(g * L::kTile);
@@ -184,29 +199,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 for (int kk = 0; kk < TB / 16; ++kk) {
                     const uint64_t bV = sdesc_sw128(aV + kk * 2048, kBox, 1024);
                     mma_ts(dO, aP + kk * 8, bV, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-                    mma_ts(dO, aP + 64 + kk * 8, bV, idesc_pv, 1u);
                 }
                 if (j == nt - 1) mma_commit(o_final + g);
             };
-            bool ok = mbar_wait(q_full, 0, abort_flag);
+            bool ok = mbar_wait(q_full, 0, abort_flag, wait_limit);
             for (int j = 0; ok && j <= nt; ++j) {
                 if (j < nt) {
-                    if (!mbar_wait(k_full + j % NS, (uint32_t)(j / NS) & 1u, abort_flag)) break;
+                    if (!mbar_wait(k_full + j % NS, (uint32_t)(j / NS) & 1u, abort_flag, wait_limit)) break;
                     fence_after_sync();
                     qk(0, j);
                 }
                 if (j >= 1) {
                     const int jp = j - 1;
-                    if (!mbar_wait(p_full + 1, (uint32_t)jp & 1u, abort_flag)) break;
-                    if (!mbar_wait(v_full + jp % NS, (uint32_t)(jp / NS) & 1u, abort_flag)) break;
+                    if (!mbar_wait(p_full + 1, (uint32_t)jp & 1u, abort_flag, wait_limit)) break;
+                    if (!mbar_wait(v_full + jp % NS, (uint32_t)(jp / NS) & 1u, abort_flag, wait_limit)) break;
                     fence_after_sync();
                     pv(1, jp);
                     mma_commit(kv_empty + jp % NS);      // both tiles are done with K, V [jp]
                 }
                 if (j < nt) {
                     qk(1, j);
-                    if (!mbar_wait(p_full + 0, (uint32_t)j & 1u, abort_flag)) break;
-                    if (!mbar_wait(v_full + j % NS, (uint32_t)(j / NS) & 1u, abort_flag)) break;
+                    if (!mbar_wait(p_full + 0, (uint32_t)j & 1u, abort_flag, wait_limit)) break;
+                    if (!mbar_wait(v_full + j % NS, (uint32_t)(j / NS) & 1u, abort_flag, wait_limit)) break;
                     fence_after_sync();
                     pv(0, j);
                 }
@@ -226,30 +240,44 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(s_full + g, (uint32_t)j & 1u, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full + g, (uint32_t)j & 1u, abort_flag, wait_limit));
+            // the tile's key biases came with K (complete by now; the wait
+            // makes the bulk copy's shared-memory writes visible here)
+            if (BIAS && ok)
+                ok = __all_sync(0xffffffffu, mbar_wait(k_full + j % NS, (uint32_t)(j / NS) & 1u, abort_flag, wait_limit));
             if (!ok) break;
             fence_after_sync();
             float s[128];
-            {
-                uint32_t r[32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(tS + c * 32, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
-                }
-            }
+            tmem_ld128_wait(tS, s);             // the whole row in one load
             const int kv = T - j * TB;          // valid keys in this tile (>= 1)
             if (kv < TB) {
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
                     if (c >= kv) s[c] = -INFINITY;
             }
-            float mx = s[0];
+            if (BIAS) {
+                // logits in log2 units with the key biases (-inf for switched-off keys)
+                const float4* b4 = reinterpret_cast<const float4*>(sm + L::kBias + (j % NS) * TB * 4);
+                const float2 cc2 = make_float2(c2, c2);
 #pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-            mx *= c2;                           // c2 > 0: the maximum commutes with the scale
+                for (int c = 0; c < 128; c += 4) {
+                    const float4 b = b4[c / 4];
+                    const float2 x01 = ffma2(make_float2(s[c], s[c + 1]), cc2, make_float2(b.x, b.y));
+                    const float2 x23 = ffma2(make_float2(s[c + 2], s[c + 3]), cc2, make_float2(b.z, b.w));
+                    s[c] = x01.x;
+                    s[c + 1] = x01.y;
+                    s[c + 2] = x23.x;
+                    s[c + 3] = x23.y;
+                }
+            }
+            float m0 = s[0], m1 = s[1];
+#pragma unroll
+            for (int c = 2; c < 126; c += 4) {
+                m0 = fmax3(m0, s[c], s[c + 1]);
+                m1 = fmax3(m1, s[c + 2], s[c + 3]);
+            }
+            float mx = fmax3(m0, m1, fmaxf(s[126], s[127]));
+            if (!BIAS) mx *= c2;                // c2 > 0: the maximum commutes with the scale
             // Conditional rescaling: the reference maximum only moves when a
             // row's maximum grows by more than 2^8, so P stays <= 256.
             const bool need = mx > m_used + 8.f;
@@ -259,31 +287,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 corr = ex2(m_used - mx);
                 m_used = mx;
             }
-            const float nm = -m_used;
-            // P_hi overwrites columns 0..63 of S, P_lo columns 64..127
-            float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
+            // (with biases the reference stays -inf while every key so far is
+            // switched off; those keys' P is then ex2(-inf) = 0)
+            const float nm = (BIAS && m_used == -INFINITY) ? 0.f : -m_used;
+            const float cs = BIAS ? 1.f : c2;   // scale still to apply to s
+            // the fp16 P overwrites columns 0..63 of S (P <= 256)
+            const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(nm, nm);
+            float2 ps01 = make_float2(0.f, 0.f), ps23 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-                uint32_t hi[16], lo[16];
+                uint32_t pw[16];
 #pragma unroll
                 for (int c = 0; c < 32; c += 4) {
                     const int k = cc * 32 + c;
-                    const float p0 = ex2(fmaf(s[k], c2, nm)), p1 = ex2(fmaf(s[k + 1], c2, nm));
-                    const float p2 = ex2(fmaf(s[k + 2], c2, nm)), p3 = ex2(fmaf(s[k + 3], c2, nm));
-                    ps0 += p0;
-                    ps1 += p1;
-                    ps2 += p2;
-                    ps3 += p3;
-                    const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
-                    hi[c / 2] = h01;
-                    hi[c / 2 + 1] = h23;
-                    lo[c / 2] = pack_bf16(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
-                    lo[c / 2 + 1] = pack_bf16(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+                    const float2 x01 = ffma2(make_float2(s[k], s[k + 1]), cs2, nm2);
+                    const float2 x23 = ffma2(make_float2(s[k + 2], s[k + 3]), cs2, nm2);
+                    const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
+                    const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
+                    ps01 = fadd2(ps01, p01);
+                    ps23 = fadd2(ps23, p23);
+                    pw[c / 2] = pack_f16(p01.x, p01.y);
+                    pw[c / 2 + 1] = pack_f16(p23.x, p23.y);
                 }
-                tmem_st16(tS + cc * 16, hi);
-                tmem_st16(tS + 64 + cc * 16, lo);
+                tmem_st16(tS + cc * 16, pw);
             }
-            l = l * corr + ((ps0 + ps1) + (ps2 + ps3));
+            l = l * corr + ((ps01.x + ps01.y) + (ps23.x + ps23.y));
             if (any && j > 0) {
                 // S_g[j] complete => every earlier P V product of this tile is too
 #pragma unroll 1
@@ -300,11 +328,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             fence_before_sync();
             mbar_arrive(p_full + g);
         }
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final + g, 0, abort_flag));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final + g, 0, abort_flag, wait_limit));
         if (ok) {
             fence_after_sync();
             const int q = q0 + g * TB + row;
-            const float inv = 1.f / l;
+            // undo the values' scale 2^-e (vconv.cu)
+            const float inv = __uint_as_float((uint32_t)(127 + vexp[h]) << 23) / l;
             float* orow = O + ((int64_t)h * n + q) * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
@@ -321,6 +350,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
             }
             if (q < n) lse2[(int64_t)h * n + q] = m_used + log2f(l);
+            // every key switched off by its bias: nothing to match
+            if (BIAS && q < n && !(l > 0.f)) set_status(status, h, KVC_ERR_NONFINITE);
         }
     }
     if (threadIdx.x == 0 && *abort_flag) set_status(status, h, KVC_ERR_TIMEOUT);
@@ -348,13 +379,14 @@ struct ColLayout {
 // MMA thread computes S^T_g = K_g Q_i^T into TMEM buffer (g, i % 2) (columns
 // 256 g + 128 (i % 2)); consumer warpgroup g reads its row (one key per
 // thread), frees the buffer and adds exp2(2 (S c2 - lse2_q)) over the 128
-// queries.  The log-masses are kept doubled in shared memory so that one
-// FFMA forms the exponent.
-template <int D, int NS>
+// queries.  The log-masses are kept doubled and negated in shared memory so
+// that one FFMA (two, paired, per instruction) forms the exponent.
+template <int D, int NS, bool BIAS>
 __global__ void __launch_bounds__(kColThreads, 1)
     k_colscore_tc(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
                   const float* __restrict__ lse2, int n, int T, float c2, float* __restrict__ score,
-                  int32_t* __restrict__ status, int qdiv) {
+                  int32_t* __restrict__ status, int qdiv, long long wait_limit, const float* __restrict__ bias2,
+                  int Tb) {
     using L = ColLayout<D, NS>;
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
@@ -406,7 +438,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
             int issued = 0;
             for (int i = 0; i < nq; ++i) {
                 const int s = i % NS;
-                if (i >= NS && !mbar_wait(q_empty + s, (uint32_t)((i / NS) - 1) & 1u, abort_flag)) break;
+                if (i >= NS && !mbar_wait(q_empty + s, (uint32_t)((i / NS) - 1) & 1u, abort_flag, wait_limit)) break;
                 mbar_expect_tx(q_full + s, kTileBytes);
                 for (int c = 0; c < D / 64; ++c)
                     tma_load_3d(sm + L::kQ + s * L::kTile + c * kBox, &mQ, q_full + s, c * 64, i * TB, h / qdiv);
@@ -421,14 +453,14 @@ __global__ void __launch_bounds__(kColThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
             const uint32_t aK0 = smem_addr(sm + L::kK);
-            bool ok = mbar_wait(k_full, 0, abort_flag);
+            bool ok = mbar_wait(k_full, 0, abort_flag, wait_limit);
             for (int i = 0; ok && i < nq; ++i) {
                 const int s = i % NS;
-                if (!mbar_wait(q_full + s, (uint32_t)(i / NS) & 1u, abort_flag)) break;
+                if (!mbar_wait(q_full + s, (uint32_t)(i / NS) & 1u, abort_flag, wait_limit)) break;
                 const uint32_t aQ = smem_addr(sm + L::kQ + s * L::kTile);
                 for (int g = 0; g < 2; ++g) {
                     const int b = g * 2 + (i & 1);
-                    if (i >= 2 && !mbar_wait(s_empty + b, (uint32_t)((i >> 1) - 1) & 1u, abort_flag)) {
+                    if (i >= 2 && !mbar_wait(s_empty + b, (uint32_t)((i >> 1) - 1) & 1u, abort_flag, wait_limit)) {
                         ok = false;
                         break;
                     }
@@ -455,6 +487,8 @@ __global__ void __launch_bounds__(kColThreads, 1)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const int ct = threadIdx.x - 64;            // 0..255 over both warpgroups
         const float c2x = 2.f * c2;
+        // this row's key bias, doubled like the logit (the grid covers Tb keys)
+        const float kb2 = BIAS ? 2.f * bias2[(int64_t)h * Tb + k0 + g * TB + row] : 0.f;
         double acc = 0.0;
         bool ok = true;
         // Every consumer warp runs all iterations (after an abort it only
@@ -468,39 +502,36 @@ __global__ void __launch_bounds__(kColThreads, 1)
                 asm volatile("bar.sync 1, 256;" ::: "memory");
                 for (int e = ct; e < cnt; e += 256) {
                     const int q = qb + e;
-                    lse_s[e] = (q < n) ? 2.f * lse2[(int64_t)h * n + q] : INFINITY;
+                    lse_s[e] = (q < n) ? -2.f * lse2[(int64_t)h * n + q] : -INFINITY;
                 }
                 asm volatile("bar.sync 1, 256;" ::: "memory");
             }
             const int b = g * 2 + (i & 1);
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (uint32_t)(i >> 1) & 1u, abort_flag));
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (uint32_t)(i >> 1) & 1u, abort_flag, wait_limit));
             if (!ok) continue;
             fence_after_sync();
             const uint32_t sbase = tmem + lane_off + (uint32_t)(g * 256 + (i & 1) * 128);
             float s[128];
-            {
-                uint32_t r[32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(sbase + c * 32, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(r[k]);
-                }
-            }
+            tmem_ld128_wait(sbase, s);          // the whole row in one load
             fence_before_sync();
             mbar_arrive(s_empty + b);
             const float4* ls = reinterpret_cast<const float4*>(lse_s + (qb % kLseChunk));
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            const float2 cx2 = make_float2(c2x, c2x), kb = make_float2(kb2, kb2);
+            float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < 128; c += 4) {
-                const float4 l4 = ls[c / 4];
-                a0 += ex2(fmaf(s[c], c2x, -l4.x));
-                a1 += ex2(fmaf(s[c + 1], c2x, -l4.y));
-                a2 += ex2(fmaf(s[c + 2], c2x, -l4.z));
-                a3 += ex2(fmaf(s[c + 3], c2x, -l4.w));
+                const float4 l4 = ls[c / 4];    // -2 lse2 of four queries
+                float2 n01 = make_float2(l4.x, l4.y), n23 = make_float2(l4.z, l4.w);
+                if (BIAS) {
+                    n01 = fadd2(n01, kb);
+                    n23 = fadd2(n23, kb);
+                }
+                const float2 x01 = ffma2(make_float2(s[c], s[c + 1]), cx2, n01);
+                const float2 x23 = ffma2(make_float2(s[c + 2], s[c + 3]), cx2, n23);
+                a01 = fadd2(a01, make_float2(ex2(x01.x), ex2(x01.y)));
+                a23 = fadd2(a23, make_float2(ex2(x23.x), ex2(x23.y)));
             }
-            acc += (double)((a0 + a1) + (a2 + a3));
+            acc += (double)((a01.x + a01.y) + (a23.x + a23.y));
         }
         const int key = k0 + g * TB + row;
         if (ok && key < T) score[(int64_t)h * T + key] = (float)sqrt(acc / (double)n);
@@ -530,7 +561,8 @@ struct MassLayout {
     static constexpr int kWarpStage = 12 * 1024;          // L2 box 4 KB + A'_hi box 4 KB + A'_lo box 4 KB
     static constexpr int kStage = 0;
     static constexpr int kRed = kStage + 4 * kWarpStage;
-    static constexpr int kEnd = kRed + 4 * 4 * 32 * 4;
+    static constexpr int kRedSq = kRed + 4 * 4 * 32 * 4;      // [4 warps] double
+    static constexpr int kEnd = kRedSq + 4 * 8;
     static constexpr int kBar = (2 * kTile > kEnd) ? 2 * kTile : kEnd;
     static constexpr int kBytes = kBar + 256 + 1024;
 };
@@ -562,13 +594,21 @@ __device__ __forceinline__ void colsum_step(float (&v)[32], int lane) {
 // per 128-query tile, added in a fixed order by the total kernel).  The
 // three arrays leave through TMA stores of swizzled boxes (rows past n are
 // clipped by the maps); columns are written up to t_h rounded up to 64.
+// The CTA's sum of A'^2 (fp32 over each thread's 32-column chunk, double
+// from there on) goes to sqpart[h][blockIdx.y][blockIdx.x], zeroed by the
+// caller: the NNLS
+// ridge mu = eps tr(A'^T A') / t is formed from these exact squares of the
+// fp32 A' rather than from the bf16-term Gram, whose diagonal misses the
+// lo * lo products (~2^-18 of each square, always the same sign) and would
+// shift mu, and so the solution of the refinement, by ~1e-5.
 template <int D>
 __global__ void __launch_bounds__(kMassThreads, 1)
     k_masslogits_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mC,
                     const __grid_constant__ CUtensorMap mL2, const __grid_constant__ CUtensorMap mAh,
                     const __grid_constant__ CUtensorMap mAl, const float* __restrict__ lse2,
                     const int32_t* __restrict__ offsets, int n, float c2, float* __restrict__ colpart,
-                    int64_t part_stride, int32_t* __restrict__ status, int qdiv) {
+                    int64_t part_stride, double* __restrict__ sqpart, int32_t* __restrict__ status, int qdiv,
+                    long long wait_limit, const float* __restrict__ bk) {
     using L = MassLayout<D>;
     const int h = blockIdx.z;
     if (!head_ok(status, h)) return;
@@ -612,7 +652,7 @@ __global__ void __launch_bounds__(kMassThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            if (mbar_wait(full, 0, abort_flag)) {
+            if (mbar_wait(full, 0, abort_flag, wait_limit)) {
                 fence_after_sync();
                 constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
                 const uint32_t aQ = smem_addr(sm + L::kQ), aC = smem_addr(sm + L::kC);
@@ -628,7 +668,7 @@ __global__ void __launch_bounds__(kMassThreads, 1)
         const int row = quarter * 32 + lane;
         const int qw = q0 + quarter * 32;         // the warp's first query
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag));
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, wait_limit));
         const int q = q0 + row;
         const float lq = (ok && q < n) ? lse2[(int64_t)h * n + q] : 0.f;
         uint8_t* bL = sm + L::kStage + quarter * L::kWarpStage;
@@ -636,6 +676,7 @@ __global__ void __launch_bounds__(kMassThreads, 1)
         uint8_t* bO = bL + 8192;
         float* red = reinterpret_cast<float*>(sm + L::kRed);      // [chunk][warp][32]
         const bool store = ok && qw < n;
+        double sq = 0.0;
         if (ok) fence_after_sync();
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -645,12 +686,18 @@ __global__ void __launch_bounds__(kMassThreads, 1)
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_off + c * 32, r);
                 tmem_ld_wait();
+                // the kept keys' input biases (lane k holds column ib + k)
+                const float bl = (bk && ib + lane < th) ? bk[off + ib + lane] : 0.f;
+                float sqc = 0.f;
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
-                    const float v = (ib + k < th) ? fmaf(__uint_as_float(r[k]), c2, -lq) : -INFINITY;
+                    const float bkk = bk ? __shfl_sync(0xffffffffu, bl, k) : 0.f;
+                    const float v = (ib + k < th) ? fmaf(__uint_as_float(r[k]), c2, bkk - lq) : -INFINITY;
                     x[k] = (q < n && ib + k < th) ? exp2f(v) : 0.f;
                     r[k] = __float_as_uint(v);
+                    sqc = fmaf(x[k], x[k], sqc);
                 }
+                sq += (double)sqc;
                 if (store && ib < tpad) {
                     // the previous chunk's boxes must have been read out before we overwrite them
                     if (lane == 0) bulk_wait_read_all();
@@ -694,8 +741,15 @@ __global__ void __launch_bounds__(kMassThreads, 1)
             colsum_step<1>(x, lane);
             red[(c * 4 + quarter) * 32 + lane] = x[0];
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        double* redsq = reinterpret_cast<double*>(sm + L::kRedSq);
+        if (lane == 0) redsq[quarter] = sq;
         // every epilogue warp reaches the barrier, whatever `ok` was
         asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (ok && quarter == 0 && lane == 0)
+            sqpart[((int64_t)h * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x] =
+                (redsq[0] + redsq[1]) + (redsq[2] + redsq[3]);
         const int cc = quarter;                   // warp `quarter` totals chunk `quarter`
         const int col = i0 + cc * 32 + lane;
         if (ok && col < th) {
@@ -713,39 +767,44 @@ __global__ void __launch_bounds__(kMassThreads, 1)
 }
 
 // ------------------------------------------------------------ host side
-template <int D, int NS>
+template <int D, int NS, bool BIAS>
 cudaError_t launch_fwd_t(const void* Q, const void* K, const void* V, int H, int n, int T, float c2, float* O,
-                         float* lse2, int32_t* status, int qdiv, cudaStream_t st) {
+                         float* lse2, const int32_t* vexp, int32_t* status, int qdiv, long long wait_limit,
+                         const float* bias2, cudaStream_t st) {
     CUtensorMap mQ, mK, mV;
     if (!make_map(&mQ, Q, D, n, H / qdiv) || !make_map(&mK, K, D, T, H) || !make_map(&mV, V, D, T, H))
         return cudaErrorInvalidValue;
-    constexpr int smem = FwdLayout<D, NS>::kBytes;
-    auto kern = k_attn_fwd_tc<D, NS>;
+    constexpr int smem = FwdLayout<D, NS, BIAS>::kBytes;
+    auto kern = k_attn_fwd_tc<D, NS, BIAS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((n + 2 * TB - 1) / (2 * TB), H);
-    kern<<<grid, kFwdThreads, smem, st>>>(mQ, mK, mV, n, T, c2, O, lse2, status, qdiv);
+    kern<<<grid, kFwdThreads, smem, st>>>(mQ, mK, mV, n, T, c2, O, lse2, vexp, status, qdiv, wait_limit, bias2,
+                                          (int)round_up(T, 256));
     return cudaGetLastError();
 }
 
-template <int D, int NS>
+template <int D, int NS, bool BIAS>
 cudaError_t launch_col_t(const void* Q, const void* K, const float* lse2, int H, int n, int T, float c2,
-                         float* score, int32_t* status, int qdiv, cudaStream_t st) {
+                         float* score, int32_t* status, int qdiv, long long wait_limit, const float* bias2,
+                         cudaStream_t st) {
     CUtensorMap mK, mQ;
     if (!make_map(&mK, K, D, T, H) || !make_map(&mQ, Q, D, n, H / qdiv)) return cudaErrorInvalidValue;
     constexpr int smem = ColLayout<D, NS>::kBytes;
-    auto kern = k_colscore_tc<D, NS>;
+    auto kern = k_colscore_tc<D, NS, BIAS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((T + 2 * TB - 1) / (2 * TB), H);
-    kern<<<grid, kColThreads, smem, st>>>(mK, mQ, lse2, n, T, c2, score, status, qdiv);
+    kern<<<grid, kColThreads, smem, st>>>(mK, mQ, lse2, n, T, c2, score, status, qdiv, wait_limit, bias2,
+                                          (int)round_up(T, 256));
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_mass_t(const void* Q, const void* Ck, const float* lse2, const int32_t* offsets, int H, int n,
                           int max_t, int64_t ldA, float c2, float* L2, void* Ah, void* Al, float* colpart,
-                          int64_t part_stride, int32_t* status, int qdiv, cudaStream_t st) {
+                          int64_t part_stride, double* sqpart, int32_t* status, int qdiv, long long wait_limit,
+                          const float* bk, cudaStream_t st) {
     CUtensorMap mQ, mC, mL2, mAh, mAl;
     if (!make_map(&mQ, Q, D, n, H / qdiv) || !make_map(&mC, Ck, D, (int)ldA, H) ||
         !make_map_f32(&mL2, L2, (int)ldA, ldA, n, H) || !make_map_bf16_rows32(&mAh, Ah, (int)ldA, ldA, n, H) ||
@@ -756,8 +815,8 @@ cudaError_t launch_mass_t(const void* Q, const void* Ck, const float* lse2, cons
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((max_t + TB - 1) / TB, (n + TB - 1) / TB, H);
-    kern<<<grid, kMassThreads, smem, st>>>(mQ, mC, mL2, mAh, mAl, lse2, offsets, n, c2, colpart, part_stride, status,
-                                           qdiv);
+    kern<<<grid, kMassThreads, smem, st>>>(mQ, mC, mL2, mAh, mAl, lse2, offsets, n, c2, colpart, part_stride, sqpart,
+                                           status, qdiv, wait_limit, bk);
     return cudaGetLastError();
 }
 
@@ -765,26 +824,50 @@ cudaError_t launch_mass_t(const void* Q, const void* Ck, const float* lse2, cons
 
 // L2: fp32 [H][n][ldA] log2 A'; Ah / Al: A' as bf16 hi / lo terms, same
 // layout; colpart: column sums of A' per 128-query tile, [tile][part_stride]
-// (entry off_h + i).  All three required.
+// (entry off_h + i); sqpart: sums of A'^2 per CTA, double
+// [H][ceil(n/128)][ceil(max_t/128)], zeroed here first.  All required but
+// bk: the kept keys' input biases [sum t] (log2 units), or null.
 cudaError_t launch_masslogits_tc(int d, const void* Q, const void* Ck, const float* lse2, const int32_t* offsets,
                                  int H, int n, int max_t, int64_t ldA, float c2, float* L2, void* Ah, void* Al,
-                                 float* colpart, int64_t part_stride, int32_t* status, int qdiv, cudaStream_t st) {
+                                 float* colpart, int64_t part_stride, double* sqpart, int32_t* status, int qdiv,
+                                 long long wait_limit, const float* bk, cudaStream_t st) {
+    const size_t nsq = (size_t)H * ((n + TB - 1) / TB) * ((max_t + TB - 1) / TB);
+    cudaError_t e = cudaMemsetAsync(sqpart, 0, nsq * sizeof(double), st);
+    if (e != cudaSuccess) return e;
     return d == 128 ? launch_mass_t<128>(Q, Ck, lse2, offsets, H, n, max_t, ldA, c2, L2, Ah, Al, colpart, part_stride,
-                                         status, qdiv, st)
+                                         sqpart, status, qdiv, wait_limit, bk, st)
                     : launch_mass_t<64>(Q, Ck, lse2, offsets, H, n, max_t, ldA, c2, L2, Ah, Al, colpart, part_stride,
-                                        status, qdiv, st);
+                                        sqpart, status, qdiv, wait_limit, bk, st);
 }
 
-cudaError_t launch_attn_fwd_tc(int d, const void* Q, const void* K, const void* V, int H, int n, int T, float c2,
-                               float* O, float* lse2, int32_t* status, int qdiv, cudaStream_t st) {
-    return d == 128 ? launch_fwd_t<128, 2>(Q, K, V, H, n, T, c2, O, lse2, status, qdiv, st)
-                    : launch_fwd_t<64, 3>(Q, K, V, H, n, T, c2, O, lse2, status, qdiv, st);
+// V16: the values in fp16 with per-head exponents vexp (launch_v_to_f16).
+// bias2 (optional): key biases [H][round_up(T, 256)], log2 units, -inf padded.
+cudaError_t launch_attn_fwd_tc(int d, const void* Q, const void* K, const void* V16, const int32_t* vexp, int H,
+                               int n, int T, float c2, float* O, float* lse2, int32_t* status, int qdiv,
+                               long long wait_limit, const float* bias2, cudaStream_t st) {
+    if (bias2)
+        return d == 128 ? launch_fwd_t<128, 2, true>(Q, K, V16, H, n, T, c2, O, lse2, vexp, status, qdiv, wait_limit,
+                                                     bias2, st)
+                        : launch_fwd_t<64, 3, true>(Q, K, V16, H, n, T, c2, O, lse2, vexp, status, qdiv, wait_limit,
+                                                    bias2, st);
+    return d == 128 ? launch_fwd_t<128, 2, false>(Q, K, V16, H, n, T, c2, O, lse2, vexp, status, qdiv, wait_limit,
+                                                  nullptr, st)
+                    : launch_fwd_t<64, 3, false>(Q, K, V16, H, n, T, c2, O, lse2, vexp, status, qdiv, wait_limit,
+                                                 nullptr, st);
 }
 
 cudaError_t launch_colscore_tc(int d, const void* Q, const void* K, const float* lse2, int H, int n, int T,
-                               float c2, float* score, int32_t* status, int qdiv, cudaStream_t st) {
-    return d == 128 ? launch_col_t<128, 3>(Q, K, lse2, H, n, T, c2, score, status, qdiv, st)
-                    : launch_col_t<64, 6>(Q, K, lse2, H, n, T, c2, score, status, qdiv, st);
+                               float c2, float* score, int32_t* status, int qdiv, long long wait_limit,
+                               const float* bias2, cudaStream_t st) {
+    if (bias2)
+        return d == 128 ? launch_col_t<128, 3, true>(Q, K, lse2, H, n, T, c2, score, status, qdiv, wait_limit, bias2,
+                                                     st)
+                        : launch_col_t<64, 6, true>(Q, K, lse2, H, n, T, c2, score, status, qdiv, wait_limit, bias2,
+                                                    st);
+    return d == 128 ? launch_col_t<128, 3, false>(Q, K, lse2, H, n, T, c2, score, status, qdiv, wait_limit, nullptr,
+                                                  st)
+                    : launch_col_t<64, 6, false>(Q, K, lse2, H, n, T, c2, score, status, qdiv, wait_limit, nullptr,
+                                                 st);
 }
 
 }  // namespace kvc

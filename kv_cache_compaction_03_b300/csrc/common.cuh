@@ -26,6 +26,22 @@ __device__ __forceinline__ void set_status(int32_t* status, int h, int32_t code)
     atomicCAS(reinterpret_cast<int*>(status + h), KVC_OK, code);
 }
 
+// Index checks of the debug build (KVC_DEBUG): an index read from data (a
+// kept position, a zero-set entry, a head's row range) is compared with the
+// extent of the buffer it addresses; a bad one records KVC_ERR_DEBUG_BOUNDS
+// for the head and the access is skipped (no trap).  In the normal build the
+// check is compiled out and the index is trusted (the arguments were
+// validated on entry).
+#ifdef KVC_DEBUG
+__device__ __forceinline__ bool debug_in_range(bool ok, const int32_t* status, int h) {
+    if (!ok) set_status(const_cast<int32_t*>(status), h, KVC_ERR_DEBUG_BOUNDS);
+    return ok;
+}
+#define KVC_IN_RANGE(cond, status, h) (::kvc::debug_in_range((cond), (status), (h)))
+#else
+#define KVC_IN_RANGE(cond, status, h) (true)
+#endif
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

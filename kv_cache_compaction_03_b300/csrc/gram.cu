@@ -25,17 +25,33 @@ __device__ double block_trace(const float* Gh, int t, int64_t ld, double* sred) 
     return tot;
 }
 
-// NNLS ridge: mu = eps * tr(G)/t; G += mu I; f = b + mu.  grid H, block 256.
+// Sum of a head's `count` trace parts in a fixed order (block-wide).
+__device__ double block_parts(const double* p, int64_t count, double* sred) {
+    double s = 0.0;
+    for (int64_t k = threadIdx.x; k < count; k += blockDim.x) s += p[k];
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((threadIdx.x & 31) == 0) sred[threadIdx.x >> 5] = s;
+    __syncthreads();
+    double tot = 0.0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += sred[w];
+    __syncthreads();
+    return tot;
+}
+
+// NNLS ridge: mu = eps * tr(A'^T A')/t; G += mu I; f = b + mu.  The trace
+// comes from the exact sums of squares of A' (sqpart, sq_count parts per
+// head) when given, else from the diagonal of G.  grid H, block 256.
 __global__ void k_ridge_g(float* __restrict__ G, const float* __restrict__ b, const int32_t* __restrict__ offsets,
-                          int64_t ldA, float eps, float* __restrict__ f, HeadScalars* __restrict__ hs,
-                          int32_t* __restrict__ status) {
+                          int64_t ldA, float eps, const double* __restrict__ sqpart, int64_t sq_count,
+                          float* __restrict__ f, HeadScalars* __restrict__ hs, int32_t* __restrict__ status) {
     const int h = blockIdx.x;
     if (!head_ok(status, h)) return;
     __shared__ double sred[32];
     const int off = offsets[h];
     const int t = offsets[h + 1] - off;
     float* Gh = G + (int64_t)h * ldA * ldA;
-    const double tr = block_trace(Gh, t, ldA, sred);
+    const double tr = sqpart ? block_parts(sqpart + (int64_t)h * sq_count, sq_count, sred)
+                             : block_trace(Gh, t, ldA, sred);
     const float mu = (float)(eps * tr / t);
     if (!isfinite(tr) || !(tr > 0.0)) {
         if (threadIdx.x == 0) set_status(status, h, KVC_ERR_NONFINITE);
@@ -91,8 +107,8 @@ __global__ void k_ridge_m_diag(float* __restrict__ M, const int32_t* __restrict_
 
 // X_qi = softmax_i(l2_qi + log2 w_i) over i < t, written as bf16 hi / lo
 // terms (the Gram operand format, see gram_tc.cu); padding columns up to the
-// next multiple of 64 are 0.  log2 w_i = beta_i log2 e (beta = ln w, -inf
-// where w = 0).  grid (ceil(n/32), H), block 256: a warp per row, four rows
+// next multiple of 64 are 0.  log2 w_i from the fitted weights (-inf where
+// w = 0).  grid (ceil(n/32), H), block 256: a warp per row, four rows
 // per warp; the CTA's 32 rows share one staged copy of log2 w.  Each lane
 // takes four adjacent columns per step (one 16-byte load, two 8-byte
 // stores): a first pass keeps a running maximum and the sum rescaled to it,
@@ -104,7 +120,7 @@ __device__ __forceinline__ void online_add(float& m, float& s, float v0, float v
     m = mn;
 }
 
-__global__ void __launch_bounds__(256) k_xsoftmax(const float* __restrict__ L2, const float* __restrict__ beta,
+__global__ void __launch_bounds__(256) k_xsoftmax(const float* __restrict__ L2, const float* __restrict__ wfit,
                                                   const int32_t* __restrict__ offsets, int n, int64_t ldA,
                                                   __nv_bfloat16* __restrict__ Xh, __nv_bfloat16* __restrict__ Xl,
                                                   const int32_t* __restrict__ status) {
@@ -115,7 +131,12 @@ __global__ void __launch_bounds__(256) k_xsoftmax(const float* __restrict__ L2, 
     const int off = offsets[h];
     const int t = offsets[h + 1] - off;
     const int tp = (int)round_up(t, GT);
-    for (int i = threadIdx.x; i < tp; i += blockDim.x) lw[i] = i < t ? beta[off + i] * kLog2e : -INFINITY;
+    // log2 of the fitted weights (not beta: on a biased cache the log-masses
+    // already hold the kept keys' input biases, which beta also carries)
+    for (int i = threadIdx.x; i < tp; i += blockDim.x) {
+        const float w = i < t ? wfit[off + i] : 0.f;
+        lw[i] = w > 0.f ? log2f(w) : -INFINITY;
+    }
     __syncthreads();
     const int lane = threadIdx.x & 31;
     for (int rr = 0; rr < 4; ++rr) {
@@ -156,9 +177,10 @@ __global__ void __launch_bounds__(256) k_xsoftmax(const float* __restrict__ L2, 
 }
 
 // ---------------------------------------------------------------- launchers
-cudaError_t launch_ridge_g(float* G, const float* b, const int32_t* offsets, int H, int64_t ldA, float eps, float* f,
+cudaError_t launch_ridge_g(float* G, const float* b, const int32_t* offsets, int H, int64_t ldA, float eps,
+                           const double* sqpart, int64_t sq_count, float* f,
                            HeadScalars* hs, int32_t* status, cudaStream_t st) {
-    k_ridge_g<<<H, 256, 0, st>>>(G, b, offsets, ldA, eps, f, hs, status);
+    k_ridge_g<<<H, 256, 0, st>>>(G, b, offsets, ldA, eps, sqpart, sq_count, f, hs, status);
     return cudaGetLastError();
 }
 cudaError_t launch_ridge_m(int d, float* M, float* R, const float* Vsel, const int32_t* offsets, int H, int64_t ldA,
@@ -172,13 +194,14 @@ cudaError_t launch_ridge_m(int d, float* M, float* R, const float* Vsel, const i
     k_ridge_m_diag<<<H, 256, 0, st>>>(M, offsets, ldA, hs, status);
     return cudaGetLastError();
 }
-cudaError_t launch_xsoftmax(const float* L2, const float* beta, const int32_t* offsets, int H, int n, int64_t ldA,
+// wfit: the fitted NNLS weights (clamped at 0), [sum t].
+cudaError_t launch_xsoftmax(const float* L2, const float* wfit, const int32_t* offsets, int H, int n, int64_t ldA,
                             void* Xh, void* Xl, const int32_t* status, cudaStream_t st) {
     dim3 grid((n + 31) / 32, H);
     const size_t smem = (size_t)ldA * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(k_xsoftmax, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_xsoftmax<<<grid, 256, smem, st>>>(L2, beta, offsets, n, ldA, (__nv_bfloat16*)Xh, (__nv_bfloat16*)Xl, status);
+    k_xsoftmax<<<grid, 256, smem, st>>>(L2, wfit, offsets, n, ldA, (__nv_bfloat16*)Xh, (__nv_bfloat16*)Xl, status);
     return cudaGetLastError();
 }
 

@@ -60,6 +60,7 @@ struct GramArgs {
     int n;
     int nb;                      // B operand columns (rect mode: d)
     int32_t* status;
+    long long wait_limit;        // bounded-wait limit, SM clock cycles
 };
 
 // grid (tiles, H), block 192.  SYM: lower tiles of the t x t product of A
@@ -70,6 +71,7 @@ template <bool SYM, int NB>
 __global__ void __launch_bounds__(kGThreads, 1)
     k_gram_tc(const __grid_constant__ CUtensorMap mAh, const __grid_constant__ CUtensorMap mAl,
               const __grid_constant__ CUtensorMap mBh, const __grid_constant__ CUtensorMap mBl, GramArgs g) {
+    const long long wait_limit = g.wait_limit;
     const int h = blockIdx.y;
     if (!head_ok(g.status, h)) return;
     const int off = g.offsets[h];
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             int issued = 0;
             for (int k = 0; k < nk; ++k) {
                 const int s = k % kStages;
-                if (k >= kStages && !mbar_wait(empty + s, (uint32_t)((k / kStages) - 1) & 1u, abort_flag)) break;
+                if (k >= kStages && !mbar_wait(empty + s, (uint32_t)((k / kStages) - 1) & 1u, abort_flag, wait_limit)) break;
                 uint8_t* st = sm + s * kStage;
                 mbar_expect_tx(full + s, (uint32_t)kStage);
                 for (int b = 0; b < 2; ++b) {
@@ -141,7 +143,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             constexpr uint32_t idesc = idesc_bf16(128, NB, true, true);
             for (int k = 0; k < nk; ++k) {
                 const int s = k % kStages;
-                if (!mbar_wait(full + s, (uint32_t)(k / kStages) & 1u, abort_flag)) break;
+                if (!mbar_wait(full + s, (uint32_t)(k / kStages) & 1u, abort_flag, wait_limit)) break;
                 fence_after_sync();
                 const uint32_t st = smem_addr(sm + s * kStage);
 #pragma unroll
@@ -163,7 +165,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         __syncwarp();
     } else {
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag));
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, wait_limit));
         if (ok) {
             fence_after_sync();
             const int quarter = warp & 3;
@@ -218,14 +220,16 @@ constexpr int gram_smem() {
 // fp32 [H][rows][ld] (first `cols` columns) -> bf16 hi / lo arrays of the same
 // shape; EXP: the stored values are log2 x.  Columns in [cols, cpad) are
 // written as 0.  When colsum is given, the CTA's 128-row column sums of x go
-// to colsum[rowtile][off + c] (fp32), to be added in a fixed order.
+// to colsum[rowtile][off + c] (fp32), to be added in a fixed order; when
+// sqpart is given, the CTA's sum of x^2 (double-float per thread) goes to
+// sqpart[h][blockIdx.y][blockIdx.x] (the exact trace of x^T x, by parts).
 // grid (ceil(cpad / 64), ceil(rows / 128), H), block 256 (64 columns x 4 row groups).
 template <bool EXP>
 __global__ void __launch_bounds__(256) k_split_hilo(const float* __restrict__ X, int rows, int64_t ld,
                                                     const int32_t* __restrict__ offsets, int fixed_cols,
                                                     __nv_bfloat16* __restrict__ Xh, __nv_bfloat16* __restrict__ Xl,
                                                     float* __restrict__ colsum, int64_t colsum_stride,
-                                                    const int32_t* __restrict__ status) {
+                                                    double* __restrict__ sqpart, const int32_t* __restrict__ status) {
     const int h = blockIdx.z;
     if (!head_ok(status, h)) return;
     const int off = offsets ? offsets[h] : 0;
@@ -236,6 +240,7 @@ __global__ void __launch_bounds__(256) k_split_hilo(const float* __restrict__ X,
     const int rg = threadIdx.x >> 6;
     const int q0 = blockIdx.y * 128;
     float s = 0.f;
+    dfloat sq{0.f, 0.f};
     for (int q = q0 + rg; q < min(rows, q0 + 128); q += 4) {
         const int64_t e = ((int64_t)h * rows + q) * ld + c;
         float x = 0.f;
@@ -244,6 +249,18 @@ __global__ void __launch_bounds__(256) k_split_hilo(const float* __restrict__ X,
         Xh[e] = hi;
         Xl[e] = __float2bfloat16_rn(x - __bfloat162float(hi));
         s += x;
+        df_fma(sq, x, x);
+    }
+    if (sqpart) {
+        __shared__ double wsq[8];
+        sq = warp_sum_df(sq);
+        if ((threadIdx.x & 31) == 0) wsq[threadIdx.x >> 5] = (double)sq.hi + (double)sq.lo;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double tot = 0.0;
+            for (int w = 0; w < 8; ++w) tot += wsq[w];
+            sqpart[((int64_t)h * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x] = tot;
+        }
     }
     if (colsum) {
         __shared__ float red[4][64];
@@ -338,7 +355,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     k_apply3_tc(const __grid_constant__ CUtensorMap mM0, const __grid_constant__ CUtensorMap mM1,
                 const __grid_constant__ CUtensorMap mM2, const __grid_constant__ CUtensorMap mR0,
                 const __grid_constant__ CUtensorMap mR1, const __grid_constant__ CUtensorMap mR2,
-                const int32_t* __restrict__ offsets, float* __restrict__ C, int32_t* __restrict__ status) {
+                const int32_t* __restrict__ offsets, float* __restrict__ C, int32_t* __restrict__ status,
+                long long wait_limit) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     const int off = offsets[h];
@@ -380,7 +398,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             int issued = 0;
             for (int k = 0; k < nk; ++k) {
                 const int s = k % kApStages;
-                if (k >= kApStages && !mbar_wait(empty + s, (uint32_t)((k / kApStages) - 1) & 1u, abort_flag)) break;
+                if (k >= kApStages && !mbar_wait(empty + s, (uint32_t)((k / kApStages) - 1) & 1u, abort_flag, wait_limit)) break;
                 uint8_t* st = sm + s * kStage;
                 mbar_expect_tx(full + s, (uint32_t)kStage);
 #pragma unroll
@@ -406,7 +424,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             constexpr int pb[6] = {0, 2, 1, 0, 1, 0};
             for (int k = 0; k < nk; ++k) {
                 const int s = k % kApStages;
-                if (!mbar_wait(full + s, (uint32_t)(k / kApStages) & 1u, abort_flag)) break;
+                if (!mbar_wait(full + s, (uint32_t)(k / kApStages) & 1u, abort_flag, wait_limit)) break;
                 fence_after_sync();
                 const uint32_t st = smem_addr(sm + s * kStage);
 #pragma unroll
@@ -426,7 +444,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         __syncwarp();
     } else {
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag));
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, wait_limit));
         if (ok) {
             fence_after_sync();
             const int quarter = warp & 3;
@@ -462,7 +480,8 @@ bool make_map_bf16(CUtensorMap* m, const void* base, int cols, int64_t ld, int r
 // C = A^T A (lower tiles, mirrored) from the hi / lo arrays of A
 // ([H][n][ld] bf16), t_h columns per head.
 cudaError_t launch_gram_sym_tc(const void* Ah, const void* Al, const int32_t* offsets, int H, int n, int max_t,
-                               int64_t ld, float* C, int64_t ldc, int32_t* status, cudaStream_t st) {
+                               int64_t ld, float* C, int64_t ldc, int32_t* status, long long wait_limit,
+                               cudaStream_t st) {
     CUtensorMap mh, ml;
     if (!make_map_bf16(&mh, Ah, (int)ld, ld, n, H) || !make_map_bf16(&ml, Al, (int)ld, ld, n, H))
         return cudaErrorInvalidValue;
@@ -470,7 +489,7 @@ cudaError_t launch_gram_sym_tc(const void* Ah, const void* Al, const int32_t* of
     cudaError_t e = cudaFuncSetAttribute(k_gram_tc<true, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int nt = (max_t + GB - 1) / GB;
-    GramArgs g{C, offsets, ldc, n, 0, status};
+    GramArgs g{C, offsets, ldc, n, 0, status, wait_limit};
     k_gram_tc<true, 128><<<dim3(nt * (nt + 1) / 2, H), kGThreads, smem, st>>>(mh, ml, mh, ml, g);
     return cudaGetLastError();
 }
@@ -478,12 +497,12 @@ cudaError_t launch_gram_sym_tc(const void* Ah, const void* Al, const int32_t* of
 // C[off + i][j] = sum_q A[q][i] B[q][j] from hi / lo arrays: A [H][n][ld], B [H][n][d].
 cudaError_t launch_gram_rect_tc(int d, const void* Ah, const void* Al, const void* Bh, const void* Bl,
                                 const int32_t* offsets, int H, int n, int max_t, int64_t ld, float* C,
-                                int32_t* status, cudaStream_t st) {
+                                int32_t* status, long long wait_limit, cudaStream_t st) {
     CUtensorMap mah, mal, mbh, mbl;
     if (!make_map_bf16(&mah, Ah, (int)ld, ld, n, H) || !make_map_bf16(&mal, Al, (int)ld, ld, n, H) ||
         !make_map_bf16(&mbh, Bh, d, d, n, H) || !make_map_bf16(&mbl, Bl, d, d, n, H))
         return cudaErrorInvalidValue;
-    GramArgs g{C, offsets, d, n, d, status};
+    GramArgs g{C, offsets, d, n, d, status, wait_limit};
     dim3 grid((max_t + GB - 1) / GB, H);
     if (d == 128) {
         constexpr int smem = gram_smem<128>();
@@ -511,17 +530,21 @@ cudaError_t launch_colsum_total(const float* part, int ntiles, int64_t stride, c
 // stored values are log2.  colsum (optional): b = column sums, through the
 // per-row-tile partials in `part` ([ceil(rows/128)][H * max_t]).
 cudaError_t launch_split_hilo(bool exp_mode, const float* X, int H, int rows, int64_t ld, const int32_t* offsets,
-                              int cols, int max_cols, void* Xh, void* Xl, float* part, float* colsum,
+                              int cols, int max_cols, void* Xh, void* Xl, float* part, float* colsum, double* sqpart,
                               const int32_t* status, cudaStream_t st) {
     const int rt = (rows + 127) / 128;
     const int64_t stride = (int64_t)H * max_cols;
     dim3 grid((unsigned)((round_up(max_cols, 64) + 63) / 64), rt, H);
+    if (sqpart) {
+        cudaError_t e = cudaMemsetAsync(sqpart, 0, sizeof(double) * grid.x * grid.y * H, st);
+        if (e != cudaSuccess) return e;
+    }
     if (exp_mode)
         k_split_hilo<true><<<grid, 256, 0, st>>>(X, rows, ld, offsets, cols, (__nv_bfloat16*)Xh, (__nv_bfloat16*)Xl,
-                                                 colsum ? part : nullptr, stride, status);
+                                                 colsum ? part : nullptr, stride, sqpart, status);
     else
         k_split_hilo<false><<<grid, 256, 0, st>>>(X, rows, ld, offsets, cols, (__nv_bfloat16*)Xh, (__nv_bfloat16*)Xl,
-                                                  colsum ? part : nullptr, stride, status);
+                                                  colsum ? part : nullptr, stride, sqpart, status);
     if (colsum && offsets)
         k_colsum_total<<<dim3((max_cols + 255) / 256, H), 256, 0, st>>>(part, rt, stride, offsets, colsum, status);
     return cudaGetLastError();
@@ -533,7 +556,8 @@ cudaError_t launch_split_hilo(bool exp_mode, const float* X, int H, int rows, in
 size_t apply_inverse_tc_scratch(int H, int64_t ldA, int d) { return (size_t)6 * H * ldA * (ldA + d); }
 
 cudaError_t launch_apply_inverse_tc(int d, const float* Minv, const float* R, const int32_t* offsets, int H,
-                                    int max_t, int64_t ldA, void* split, float* C, int32_t* status, cudaStream_t st) {
+                                    int max_t, int64_t ldA, void* split, float* C, int32_t* status,
+                                    long long wait_limit, cudaStream_t st) {
     __nv_bfloat16* Ms = static_cast<__nv_bfloat16*>(split);
     const int64_t tsm = (int64_t)H * ldA * ldA;
     __nv_bfloat16* Rs = Ms + 3 * tsm;
@@ -551,12 +575,14 @@ cudaError_t launch_apply_inverse_tc(int d, const float* Minv, const float* R, co
         constexpr int smem = apply3_smem<128>();
         cudaError_t e = cudaFuncSetAttribute(k_apply3_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        k_apply3_tc<128><<<grid, kGThreads, smem, st>>>(mm[0], mm[1], mm[2], mr[0], mr[1], mr[2], offsets, C, status);
+        k_apply3_tc<128><<<grid, kGThreads, smem, st>>>(mm[0], mm[1], mm[2], mr[0], mr[1], mr[2], offsets, C, status,
+                                                        wait_limit);
     } else {
         constexpr int smem = apply3_smem<64>();
         cudaError_t e = cudaFuncSetAttribute(k_apply3_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        k_apply3_tc<64><<<grid, kGThreads, smem, st>>>(mm[0], mm[1], mm[2], mr[0], mr[1], mr[2], offsets, C, status);
+        k_apply3_tc<64><<<grid, kGThreads, smem, st>>>(mm[0], mm[1], mm[2], mr[0], mr[1], mr[2], offsets, C, status,
+                                                        wait_limit);
     }
     return cudaGetLastError();
 }

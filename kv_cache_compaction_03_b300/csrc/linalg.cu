@@ -18,14 +18,15 @@
 //       free-set solution through the Schur complement (H^{-1})_ZZ of the
 //       explicit inverse (sweep.cu), the feasibility / optimality check and
 //       the exchange of violators
-//   k_rowmass / k_colresid / k_refine_apply
+//   k_refine_resid / k_colresid_sum / k_refine_apply
 //       iterative refinement of w with the residual A'^T(1 - A'w) + mu(1 - w)
-//       taken from A' itself (not from the rounded Gram)
+//       taken from A' itself (not from the rounded Gram), one pass over the
+//       log-masses per step
 //   k_beta_out
 //       beta = log w
 // Matrices are row-major fp32 with leading dimension ldA; only the lower
 // triangle of a symmetric matrix is read.
-#include "common.cuh"
+#include "tc.cuh"
 
 namespace kvc {
 
@@ -594,7 +595,11 @@ __device__ bool bpp_step_body(const BppArgs& a) {
     __shared__ int sflag, s_nbad, s_maxbad, s_full;
     __shared__ float sred[32];
     const int nz = a.nz[h];
-    for (int k = threadIdx.x; k < nz; k += blockDim.x) zl[k] = a.zlist[(int64_t)h * a.zmax + k];
+    if (!KVC_IN_RANGE(nz >= 0 && nz <= a.zmax, a.status, h)) return true;
+    for (int k = threadIdx.x; k < nz; k += blockDim.x) {
+        const int z = a.zlist[(int64_t)h * a.zmax + k];
+        zl[k] = KVC_IN_RANGE(z >= 0 && z < t, a.status, h) ? z : 0;
+    }
     for (int i = threadIdx.x; i < t; i += blockDim.x) ssrc[i] = a.x0[off + i];
     __syncthreads();
     if (!schur_solution(a, h, off, t, nz, zl, true, ssrc, sx, snu, sm_chol, &sflag)) {
@@ -714,62 +719,90 @@ __global__ void k_bpp_finish(BppArgs a, int H) {
     if (!a.piv[4 * h]) set_status(a.status, h, KVC_ERR_NNLS_MAXITER);
 }
 
-// v_q = sum_i A'_qi x_i (double-float), u_q = 1 - v_q.  grid (ceil(n/8), H), block 256.
-__global__ void __launch_bounds__(256) k_rowmass(const float* __restrict__ L2, const float* __restrict__ x,
-                                                 const int32_t* __restrict__ offsets, int n, int64_t ldA,
-                                                 float* __restrict__ u, const int32_t* __restrict__ status) {
+// The residual of the refinement, r_i = sum_q A'_qi u_q + mu (1 - x_i) with
+// u_q = 1 - sum_i A'_qi x_i, in one pass over the log-masses: a CTA takes
+// `qb` query rows of one head, brings them into shared memory with one bulk
+// copy per row (the copy engine keeps the whole block in flight), turns them
+// into A' = 2^l2, forms each row's u_q (a warp per row, double-float), then
+// adds its rows' share of every column, sum over its rows of A'_qi u_q (a
+// thread per column, double-float, from shared memory), and writes that
+// partial to part[block][off + i].  k_colresid_sum then adds the blocks'
+// partials in a fixed order, so the result does not depend on scheduling.
+// The copy wait is bounded; a CTA that gives up reports TIMEOUT for the head
+// after its copies have landed.
+// grid (ceil(n/qb), H), block 256, dynamic smem (qb * ldA + qb) floats + 16.
+__global__ void __launch_bounds__(256) k_refine_resid(const float* __restrict__ L2, const float* __restrict__ x,
+                                                      const int32_t* __restrict__ offsets, int n, int64_t ldA,
+                                                      int qb, int64_t part_stride, dfloat* __restrict__ part,
+                                                      int32_t* __restrict__ status) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
+    extern __shared__ __align__(16) float sa[];    // [qb][ldA] A', then [qb] u, then the barrier
+    float* su = sa + (int64_t)qb * ldA;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(su + round_up(qb, 4));
+    __shared__ int abort_flag;
     const int off = offsets[h];
     const int t = offsets[h + 1] - off;
-    const int q = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (q >= n) return;
-    const float* row = L2 + ((int64_t)h * n + q) * ldA;
-    dfloat acc{0.f, 0.f};
-    for (int i = lane; i < t; i += 32) df_fma(acc, exp2f(row[i]), x[off + i]);
-    acc = warp_sum_df(acc);
-    if (lane == 0) u[(int64_t)h * n + q] = (1.f - acc.hi) - acc.lo;
+    const int q0 = blockIdx.x * qb;
+    const int rows = min(qb, n - q0);
+    const uint32_t rowbytes = (uint32_t)round_up(t, 4) * 4u;   // columns t.. of a row hold -inf
+    if (threadIdx.x == 0) {
+        tc::mbar_init(bar, 1);
+        abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        tc::mbar_expect_tx(bar, (uint32_t)rows * rowbytes);
+        for (int r = 0; r < rows; ++r)
+            tc::bulk_load(sa + (int64_t)r * ldA, L2 + ((int64_t)h * n + q0 + r) * ldA, rowbytes, bar);
+    }
+    if (!tc::mbar_wait(bar, 0, &abort_flag)) {
+        int never = 0;
+        (void)tc::mbar_wait(bar, 0, &never);          // the copies must land before the CTA leaves
+        if (threadIdx.x == 0) set_status(status, h, KVC_ERR_TIMEOUT);
+        return;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int rr = warp; rr < qb; rr += 8) {
+        float* arow = sa + (int64_t)rr * ldA;
+        dfloat acc{0.f, 0.f};
+        if (rr < rows) {
+            for (int i = lane; i < t; i += 32) {
+                const float a = exp2f(arow[i]);
+                arow[i] = a;
+                df_fma(acc, a, x[off + i]);
+            }
+        } else {
+            for (int i = lane; i < t; i += 32) arow[i] = 0.f;
+        }
+        acc = warp_sum_df(acc);
+        if (lane == 0) su[rr] = rr < rows ? (1.f - acc.hi) - acc.lo : 0.f;
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < t; c += 256) {
+        dfloat acc{0.f, 0.f};
+        for (int rr = 0; rr < qb; ++rr) df_fma(acc, sa[(int64_t)rr * ldA + c], su[rr]);
+        part[(int64_t)blockIdx.x * part_stride + off + c] = acc;
+    }
 }
 
-// r_i = sum_q A'_qi u_q + mu (1 - x_i) on the free set, 0 on the zero set.
-// Pass 1 (k_colresid): grid (ceil(max_t/64), kResidSplit, H), block 256 (4 row
-// groups x 64 columns); split s sums the rows q = s, s + kResidSplit, ... in
-// double-float and writes its partial to part[s][off + c].  Pass 2
-// (k_colresid_sum) adds the partials in a fixed order, so the result does
-// not depend on scheduling.
-constexpr int kResidSplit = 8;
-
-__global__ void __launch_bounds__(256) k_colresid(const float* __restrict__ L2, const float* __restrict__ u,
-                                                  const int32_t* __restrict__ offsets, int n, int64_t ldA,
-                                                  int64_t part_stride, dfloat* __restrict__ part,
-                                                  const int32_t* __restrict__ status) {
-    const int h = blockIdx.z;
-    if (!head_ok(status, h)) return;
-    const int off = offsets[h];
-    const int t = offsets[h + 1] - off;
-    const int c = blockIdx.x * 64 + (threadIdx.x & 63);
-    const int rg = threadIdx.x >> 6;
-    const int sp = blockIdx.y;
-    __shared__ dfloat red[4][64];
-    dfloat acc{0.f, 0.f};
-    if (c < t) {
-        const float* col = L2 + (int64_t)h * n * ldA + c;
-        const float* uh = u + (int64_t)h * n;
-        for (int q = sp + kResidSplit * rg; q < n; q += 4 * kResidSplit)
-            df_fma(acc, exp2f(col[(int64_t)q * ldA]), uh[q]);
-    }
-    red[rg][threadIdx.x & 63] = acc;
-    __syncthreads();
-    if (rg == 0 && c < t) {
-        for (int g = 1; g < 4; ++g) df_add_df(acc, red[g][threadIdx.x]);
-        part[(int64_t)sp * part_stride + off + c] = acc;
-    }
+// Query rows per CTA of k_refine_resid: a multiple of the 8 warps, as many
+// as keep its shared-memory tile (rows x ldA floats) within 128 KB.
+int refine_rows(int64_t ldA) {
+    const int64_t r = 4096 / ldA;
+    return 8 * (int)(r < 1 ? 1 : (r > 8 ? 8 : r));
+}
+// Bytes of the per-block partial sums of k_refine_resid.
+size_t refine_part_bytes(int H, int n, int max_t, int64_t ldA) {
+    const int qb = refine_rows(ldA);
+    return (size_t)((n + qb - 1) / qb) * H * max_t * sizeof(dfloat);
 }
 
 // grid (ceil(max_t/256), H), block 256.
 __global__ void __launch_bounds__(256) k_colresid_sum(const dfloat* __restrict__ part, int64_t part_stride,
-                                                      const float* __restrict__ x, const int8_t* __restrict__ zflag,
+                                                      int nblk, const float* __restrict__ x,
+                                                      const int8_t* __restrict__ zflag,
                                                       const int32_t* __restrict__ offsets,
                                                       const HeadScalars* __restrict__ hs, float* __restrict__ r,
                                                       const uint8_t* __restrict__ fixed,
@@ -781,7 +814,7 @@ __global__ void __launch_bounds__(256) k_colresid_sum(const dfloat* __restrict__
     const int c = blockIdx.x * 256 + threadIdx.x;
     if (c >= t) return;
     dfloat acc = part[off + c];
-    for (int sp = 1; sp < kResidSplit; ++sp) df_add_df(acc, part[(int64_t)sp * part_stride + off + c]);
+    for (int sp = 1; sp < nblk; ++sp) df_add_df(acc, part[(int64_t)sp * part_stride + off + c]);
     df_fma(acc, hs[h].mu, 1.f - x[off + c]);
     // weights held fixed (thought-aware pivots) take no refinement step
     r[off + c] = (zflag[off + c] || (fixed && fixed[off + c])) ? 0.f : acc.hi + acc.lo;
@@ -802,7 +835,11 @@ __global__ void __launch_bounds__(512) k_refine_apply(BppArgs a, const float* __
     float* sm_chol = reinterpret_cast<float*>(zl + a.zmax);
     __shared__ int sflag;
     const int nz = a.nz[h];
-    for (int k = threadIdx.x; k < nz; k += blockDim.x) zl[k] = a.zlist[(int64_t)h * a.zmax + k];
+    if (!KVC_IN_RANGE(nz >= 0 && nz <= a.zmax, a.status, h)) return;
+    for (int k = threadIdx.x; k < nz; k += blockDim.x) {
+        const int z = a.zlist[(int64_t)h * a.zmax + k];
+        zl[k] = KVC_IN_RANGE(z >= 0 && z < t, a.status, h) ? z : 0;
+    }
     for (int i = threadIdx.x; i < t; i += blockDim.x) ssrc[i] = d0[off + i];
     __syncthreads();
     schur_solution(a, h, off, t, nz, zl, false, ssrc, sx, snu, sm_chol, &sflag);
@@ -810,9 +847,12 @@ __global__ void __launch_bounds__(512) k_refine_apply(BppArgs a, const float* __
         if (!a.zflag[off + i]) a.x[off + i] += sx[i];
 }
 
-// beta = log w (w clamped at 0; -inf where w = 0).  grid (ceil(max_t/256), H).
+// beta = log w (w clamped at 0; -inf where w = 0), plus the kept key's input
+// bias when the keys carry one (bias_in [H][T] natural units, positions
+// idx).  grid (ceil(max_t/256), H).
 __global__ void k_beta_out(float* __restrict__ x, const int32_t* __restrict__ offsets, float* __restrict__ beta,
-                           const int32_t* __restrict__ status) {
+                           const int32_t* __restrict__ status, const float* __restrict__ bias_in,
+                           const int32_t* __restrict__ idx, int T) {
     const int h = blockIdx.y;
     const int off = offsets[h];
     const int t = offsets[h + 1] - off;
@@ -820,7 +860,13 @@ __global__ void k_beta_out(float* __restrict__ x, const int32_t* __restrict__ of
     if (i >= t || !head_ok(status, h)) return;
     const float w = fmaxf(x[off + i], 0.f);
     x[off + i] = w;
-    beta[off + i] = (w > 0.f) ? logf(w) : -INFINITY;
+    float b0 = 0.f;
+    if (bias_in) {
+        const int j = idx[off + i];
+        if (!KVC_IN_RANGE(j >= 0 && j < T, status, h)) return;
+        b0 = bias_in[(int64_t)h * T + j];
+    }
+    beta[off + i] = (w > 0.f) ? b0 + logf(w) : -INFINITY;
 }
 
 // ------------------------------------------------------------ launchers
@@ -891,7 +937,7 @@ cudaError_t launch_symv(const float* Hinv, const float* v, const int32_t* offset
 // pivoting steps (each reads the zero-set rows of H^{-1}), refinement.
 cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* offsets, int H, int n, int max_t,
                             int64_t ldA, const float* L2, float* x, float* x0, int8_t* zflag, int32_t* zlist,
-                            int32_t* nz, float* S, int32_t* piv, float* u, float* r, float* d0, HeadScalars* hs,
+                            int32_t* nz, float* S, int32_t* piv, float* r, float* d0, HeadScalars* hs,
                             int zmax, int max_iter, int refine_iters, void* rpart_ws, const uint8_t* fixed,
                             int32_t* status, cudaStream_t st, int* launches) {
     dfloat* rpart = static_cast<dfloat*>(rpart_ws);
@@ -911,25 +957,28 @@ cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* of
     ++nl;
     k_bpp_finish<<<(H + 127) / 128, 128, 0, st>>>(b, H);
     ++nl;
+    const int qb = refine_rows(ldA);
+    const int nblk = (n + qb - 1) / qb;
+    const size_t rsmem = (size_t)(qb * ldA + round_up(qb, 4)) * sizeof(float) + 16;
+    e = cudaFuncSetAttribute(k_refine_resid, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsmem);
+    if (e != cudaSuccess) return e;
     for (int it = 0; it < refine_iters; ++it) {
-        k_rowmass<<<dim3((n + 7) / 8, H), 256, 0, st>>>(L2, x, offsets, n, ldA, u, status);
-        k_colresid<<<dim3((max_t + 63) / 64, kResidSplit, H), 256, 0, st>>>(L2, u, offsets, n, ldA, part_stride,
-                                                                           rpart, status);
-        k_colresid_sum<<<dim3((max_t + 255) / 256, H), 256, 0, st>>>(rpart, part_stride, x, zflag, offsets, hs, r, fixed,
-                                                                    status);
+        k_refine_resid<<<dim3(nblk, H), 256, rsmem, st>>>(L2, x, offsets, n, ldA, qb, part_stride, rpart, status);
+        k_colresid_sum<<<dim3((max_t + 255) / 256, H), 256, 0, st>>>(rpart, part_stride, nblk, x, zflag, offsets, hs, r,
+                                                                    fixed, status);
         e = launch_symv(Hinv, r, offsets, H, max_t, ldA, d0, nullptr, 0, status, st);
         if (e != cudaSuccess) return e;
         k_refine_apply<<<H, 512, smem, st>>>(b, d0);
-        nl += 5;
+        nl += 4;
     }
     if (launches) *launches = nl;
     return cudaGetLastError();
 }
 
 cudaError_t launch_beta_out(float* x, const int32_t* offsets, int H, int max_t, float* beta, const int32_t* status,
-                            cudaStream_t st) {
+                            const float* bias_in, const int32_t* idx, int T, cudaStream_t st) {
     dim3 grid((max_t + 255) / 256, H);
-    k_beta_out<<<grid, 256, 0, st>>>(x, offsets, beta, status);
+    k_beta_out<<<grid, 256, 0, st>>>(x, offsets, beta, status, bias_in, idx, T);
     return cudaGetLastError();
 }
 

@@ -196,15 +196,18 @@ __global__ void __launch_bounds__(1024) k_select_seg(const float* __restrict__ s
 // ---------------------------------------------------------------- gather
 // grid (ceil(max_t/8), H), block 256 (one warp per kept row).
 // C_k[off+i] = K[h][idx[off+i]] (storage dtype, 16-byte vectors) and
-// Vsel[off+i] = fp32(V[h][idx[off+i]]).  When Ckw is given, the kept keys
-// are also copied to Ckw[h][i] (rows padded per head to ldw), the layout the
-// tensor-core mass pass reads through TMA.
-template <typename TIn, int D>
-__global__ void __launch_bounds__(256) k_gather(const TIn* __restrict__ K, const TIn* __restrict__ V, int T,
+// Vsel[off+i] = fp32(V[h][idx[off+i]]) (V in the storage dtype, or fp32 for
+// the values of a compacted cache).  When Ckw is given, the kept keys are
+// also copied to Ckw[h][i] (rows padded per head to ldw), the layout the
+// tensor-core mass pass reads through TMA.  When bias2 is given (keys with
+// input biases, [H][Tb] log2 units), bk[off+i] = bias2[h][idx[off+i]].
+template <typename TIn, typename TV, int D>
+__global__ void __launch_bounds__(256) k_gather(const TIn* __restrict__ K, const TV* __restrict__ V, int T,
                                                 const int32_t* __restrict__ offsets, const int32_t* __restrict__ idx,
                                                 TIn* __restrict__ Ck, float* __restrict__ Vsel,
                                                 TIn* __restrict__ Ckw, int64_t ldw,
-                                                const int32_t* __restrict__ status) {
+                                                const int32_t* __restrict__ status, const float* __restrict__ bias2,
+                                                int64_t Tb, float* __restrict__ bk) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     const int off = offsets[h];
@@ -213,6 +216,7 @@ __global__ void __launch_bounds__(256) k_gather(const TIn* __restrict__ K, const
     const int lane = threadIdx.x & 31;
     if (i >= t) return;
     const int j = idx[off + i];
+    if (!KVC_IN_RANGE(j >= 0 && j < T, status, h)) return;
     constexpr int VEC = 16 / sizeof(TIn);          // elements per 16-byte vector
     constexpr int NV = D / VEC;
     const uint4* src = reinterpret_cast<const uint4*>(K + ((int64_t)h * T + j) * D);
@@ -223,9 +227,10 @@ __global__ void __launch_bounds__(256) k_gather(const TIn* __restrict__ K, const
         dst[v] = x;
         if (dw) dw[v] = x;
     }
-    const TIn* vr = V + ((int64_t)h * T + j) * D;
+    const TV* vr = V + ((int64_t)h * T + j) * D;
     float* vo = Vsel + ((int64_t)off + i) * D;
     for (int c = lane; c < D; c += 32) vo[c] = to_f32(vr[c]);
+    if (bias2 && lane == 0) bk[off + i] = bias2[(int64_t)h * Tb + j];
 }
 
 // ---------------------------------------------------------------- chunk shift
@@ -265,25 +270,40 @@ cudaError_t launch_shift_idx(int32_t* idx, const int32_t* offsets, int H, int T,
     k_shift_idx<<<dim3((max_t + 255) / 256, H), 256, 0, st>>>(idx, offsets, T, chunks, status);
     return cudaGetLastError();
 }
-template <typename TIn, int D>
+template <typename TIn, typename TV, int D>
 static cudaError_t launch_gather_t(const void* K, const void* V, int H, int T, int max_t, const int32_t* offsets,
                                    const int32_t* idx, void* Ck, float* Vsel, void* Ckw, int64_t ldw,
-                                   const int32_t* status, cudaStream_t st) {
+                                   const int32_t* status, const float* bias2, int64_t Tb, float* bk,
+                                   cudaStream_t st) {
     dim3 grid((max_t + 7) / 8, H);
-    k_gather<TIn, D><<<grid, 256, 0, st>>>((const TIn*)K, (const TIn*)V, T, offsets, idx, (TIn*)Ck, Vsel, (TIn*)Ckw,
-                                           ldw, status);
+    k_gather<TIn, TV, D><<<grid, 256, 0, st>>>((const TIn*)K, (const TV*)V, T, offsets, idx, (TIn*)Ck, Vsel,
+                                               (TIn*)Ckw, ldw, status, bias2, Tb, bk);
     return cudaGetLastError();
 }
-cudaError_t launch_gather(int dtype, int d, const void* K, const void* V, int H, int T, int max_t,
+template <typename TIn>
+static cudaError_t launch_gather_k(int d, bool v_f32, const void* K, const void* V, int H, int T, int max_t,
+                                   const int32_t* offsets, const int32_t* idx, void* Ck, float* Vsel, void* Ckw,
+                                   int64_t ldw, const int32_t* status, const float* bias2, int64_t Tb, float* bk,
+                                   cudaStream_t st) {
+    if (v_f32)
+        return d == 128 ? launch_gather_t<TIn, float, 128>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, Ckw, ldw, status,
+                                                           bias2, Tb, bk, st)
+                        : launch_gather_t<TIn, float, 64>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, Ckw, ldw, status,
+                                                          bias2, Tb, bk, st);
+    return d == 128 ? launch_gather_t<TIn, TIn, 128>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, Ckw, ldw, status,
+                                                     bias2, Tb, bk, st)
+                    : launch_gather_t<TIn, TIn, 64>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, Ckw, ldw, status,
+                                                    bias2, Tb, bk, st);
+}
+// v_f32: V is fp32 whatever the keys' dtype; bias2 / bk: optional key biases.
+cudaError_t launch_gather(int dtype, int d, const void* K, const void* V, bool v_f32, int H, int T, int max_t,
                           const int32_t* offsets, const int32_t* idx, void* Ck, float* Vsel, void* Ckw, int64_t ldw,
-                          const int32_t* status, cudaStream_t st) {
+                          const int32_t* status, const float* bias2, int64_t Tb, float* bk, cudaStream_t st) {
     if (dtype == KVC_DTYPE_BF16)
-        return d == 128 ? launch_gather_t<__nv_bfloat16, 128>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, Ckw, ldw,
-                                                              status, st)
-                        : launch_gather_t<__nv_bfloat16, 64>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, Ckw, ldw,
-                                                             status, st);
-    return d == 128 ? launch_gather_t<float, 128>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, nullptr, 0, status, st)
-                    : launch_gather_t<float, 64>(K, V, H, T, max_t, offsets, idx, Ck, Vsel, nullptr, 0, status, st);
+        return launch_gather_k<__nv_bfloat16>(d, v_f32, K, V, H, T, max_t, offsets, idx, Ck, Vsel, Ckw, ldw, status,
+                                              bias2, Tb, bk, st);
+    return launch_gather_k<float>(d, true, K, V, H, T, max_t, offsets, idx, Ck, Vsel, nullptr, 0, status, bias2, Tb,
+                                  bk, st);
 }
 
 }  // namespace kvc

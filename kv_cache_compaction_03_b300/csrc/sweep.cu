@@ -54,6 +54,7 @@ struct SweepArgs {
     int k0;                   // first row of the pivot block
     int32_t* status;
     int have_p;               // P of this step was formed by the previous update launch
+    long long wait_limit;     // bounded-wait limit of the tensor-core update, SM clock cycles
 };
 
 // x = hi + mid + lo exactly (three bf16 terms of 8 significant bits each;
@@ -388,6 +389,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
                       const __grid_constant__ CUtensorMap mU2, const __grid_constant__ CUtensorMap mV0,
                       const __grid_constant__ CUtensorMap mV1, const __grid_constant__ CUtensorMap mV2,
                       const __grid_constant__ CUtensorMap mA, SweepArgs s) {
+    const long long wait_limit = s.wait_limit;
     const int h = blockIdx.y;
     if (!head_ok(s.status, h)) return;
     const int t = s.offsets[h + 1] - s.offsets[h];
@@ -495,7 +497,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
                     tma_load_3d(sm + (6 + 2 * q + b) * kUBox, mv[q], full, J * UB + 64 * b, 0, h);
                 }
             // the A tile goes where the operands were, once the MMAs have read them
-            if (mbar_wait(acc_full, 0, abort_flag)) {
+            if (mbar_wait(acc_full, 0, abort_flag, wait_limit)) {
                 mbar_expect_tx(fullA, 16u * kABox);
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
@@ -504,12 +506,17 @@ __global__ void __launch_bounds__(kUThreads, 2)
                         tma_load_3d(smA + (4 * q + c) * kABox, &mA, fullA, J * UB + 32 * c, I * UB + 32 * q, h);
                 int never = 0;
                 (void)mbar_wait(fullA, 0, &never);
+            } else {
+                // given up: the operand copies issued above must still land
+                // before the CTA leaves
+                int never = 0;
+                (void)mbar_wait(full, 0, &never);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            if (mbar_wait(full, 0, abort_flag)) {
+            if (mbar_wait(full, 0, abort_flag, wait_limit)) {
                 fence_after_sync();
                 constexpr uint32_t idesc = idesc_bf16(128, 128, true, true);
                 const uint32_t base = smem_addr(sm);
@@ -542,7 +549,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
         const bool rowK = i0 >= k0 && i0 < k0 + SB;
         const float* Uh = s.U + (int64_t)h * SB * ld;
         const float* Ph = s.P + (int64_t)h * SB * SB;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag) && mbar_wait(fullA, 0, abort_flag));
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, wait_limit) && mbar_wait(fullA, 0, abort_flag, wait_limit));
         if (ok) {
             fence_after_sync();
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -674,7 +681,7 @@ bool make_map_f32(CUtensorMap* m, const void* base, int cols, int64_t ld, int ro
 // [4][H][64][64] (the step's pivot inverse, the next pivot block's two inputs,
 // its inverse).
 cudaError_t launch_sweep_inverse(float* A, const int32_t* offsets, int H, int max_t, int64_t ldA, float* U,
-                                 void* split, float* P, int32_t* status, cudaStream_t st) {
+                                 void* split, float* P, int32_t* status, long long wait_limit, cudaStream_t st) {
     const int nb = (max_t + SB - 1) / SB;
     const int ntri = nb * (nb + 1) / 2;
     const int nu = (max_t + UB - 1) / UB;
@@ -692,7 +699,7 @@ cudaError_t launch_sweep_inverse(float* A, const int32_t* offsets, int H, int ma
     float* Xn = P + (int64_t)H * SB * SB;
     float* Pn = P + 3 * (int64_t)H * SB * SB;
     for (int k = 0; k < nb; ++k) {
-        SweepArgs s{A, U, Us, Vs, P, Xn, Pn, offsets, ldA, ts, k * SB, status, k > 0};
+        SweepArgs s{A, U, Us, Vs, P, Xn, Pn, offsets, ldA, ts, k * SB, status, k > 0, wait_limit};
         k_sweep_pivot<<<dim3(nb, H), kPivThreads, 0, st>>>(s);
         // CTA 0 of each head forms and inverts the next pivot block
         k_sweep_update_tc<<<dim3(nu * (nu + 1) / 2 + 1, H), kUThreads, kUSmem, st>>>(mu[0], mu[1], mu[2], mv[0],

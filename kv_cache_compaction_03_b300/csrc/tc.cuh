@@ -40,22 +40,56 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking probe of the same phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_probe(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 
-// About one second at the B300's top SM clock.  A wait that runs longer
-// than this means a kernel bug; the waiting thread raises the CTA's abort
-// flag and every role winds down instead of spinning on.
+// Limits below this many cycles (about half a millisecond) are waited out by
+// non-blocking probes with the clock read at every probe: try_wait may
+// suspend a thread for a hardware-defined window, which could outlast such
+// a limit before the clock is looked at.
+constexpr long long kShortWait = 1LL << 20;
+
+// About one second at the B300's top SM clock: the limit of the waits a
+// kernel makes at teardown for its own copies and MMAs in flight, and the
+// default of the caller's limit (kvc_params.wait_timeout_us).  A wait that
+// runs longer than its limit means a kernel bug or an unusable device; the
+// waiting thread raises the CTA's abort flag and every role winds down
+// instead of spinning on.
 constexpr long long kWaitCycles = 2000000000LL;
 
-// Wait for the phase of `bar` with the given parity.  Returns false if the
-// wait gave up (time limit) or another thread of the CTA already gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// Wait for the phase of `bar` with the given parity, for at most `limit` SM
+// clock cycles.  Returns false if the wait gave up (time limit) or another
+// thread of the CTA already gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          long long limit = kWaitCycles) {
+    if (limit < kShortWait) {
+        const long long t0 = clock64();
+        for (;;) {
+            if (mbar_probe(bar, parity)) return true;
+            if (*abort_flag) return false;
+            if (clock64() - t0 > limit) {
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
     if (mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
         if (mbar_test(bar, parity)) return true;
         if ((it & 31u) == 0) {
             if (*abort_flag) return false;
-            if (clock64() - t0 > kWaitCycles) {
+            if (clock64() - t0 > limit) {
                 *abort_flag = 1;
                 return false;
             }
@@ -72,6 +106,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+// Plain bulk copy of `bytes` from global to shared memory (both addresses
+// 16-byte aligned, bytes a multiple of 16); completes that many bytes of
+// transaction count on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
 }
 // 3-D tiled store from shared memory (coordinates innermost first), in the
 // bulk-group completion scheme: commit, then wait until the shared memory
@@ -132,6 +175,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor of kind::f16 with fp16 A and B, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
@@ -174,6 +223,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
+// 32 lanes x 32 bits, 128 consecutive columns, and the wait for them in the
+// same statement: s[i] = column col + i of the thread's lane, valid on return.
+__device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, float (&s)[128]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x128.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%128];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=f"(s[0]), "=f"(s[1]), "=f"(s[2]), "=f"(s[3]), "=f"(s[4]), "=f"(s[5]), "=f"(s[6]), "=f"(s[7]), "=f"(s[8]), "=f"(s[9]), "=f"(s[10]), "=f"(s[11]), "=f"(s[12]), "=f"(s[13]), "=f"(s[14]), "=f"(s[15]), "=f"(s[16]), "=f"(s[17]), "=f"(s[18]), "=f"(s[19]), "=f"(s[20]), "=f"(s[21]), "=f"(s[22]), "=f"(s[23]), "=f"(s[24]), "=f"(s[25]), "=f"(s[26]), "=f"(s[27]), "=f"(s[28]), "=f"(s[29]), "=f"(s[30]), "=f"(s[31]), "=f"(s[32]), "=f"(s[33]), "=f"(s[34]), "=f"(s[35]), "=f"(s[36]), "=f"(s[37]), "=f"(s[38]), "=f"(s[39]), "=f"(s[40]), "=f"(s[41]), "=f"(s[42]), "=f"(s[43]), "=f"(s[44]), "=f"(s[45]), "=f"(s[46]), "=f"(s[47]), "=f"(s[48]), "=f"(s[49]), "=f"(s[50]), "=f"(s[51]), "=f"(s[52]), "=f"(s[53]), "=f"(s[54]), "=f"(s[55]), "=f"(s[56]), "=f"(s[57]), "=f"(s[58]), "=f"(s[59]), "=f"(s[60]), "=f"(s[61]), "=f"(s[62]), "=f"(s[63]), "=f"(s[64]), "=f"(s[65]), "=f"(s[66]), "=f"(s[67]), "=f"(s[68]), "=f"(s[69]), "=f"(s[70]), "=f"(s[71]), "=f"(s[72]), "=f"(s[73]), "=f"(s[74]), "=f"(s[75]), "=f"(s[76]), "=f"(s[77]), "=f"(s[78]), "=f"(s[79]), "=f"(s[80]), "=f"(s[81]), "=f"(s[82]), "=f"(s[83]), "=f"(s[84]), "=f"(s[85]), "=f"(s[86]), "=f"(s[87]), "=f"(s[88]), "=f"(s[89]), "=f"(s[90]), "=f"(s[91]), "=f"(s[92]), "=f"(s[93]), "=f"(s[94]), "=f"(s[95]), "=f"(s[96]), "=f"(s[97]), "=f"(s[98]), "=f"(s[99]), "=f"(s[100]), "=f"(s[101]), "=f"(s[102]), "=f"(s[103]), "=f"(s[104]), "=f"(s[105]), "=f"(s[106]), "=f"(s[107]), "=f"(s[108]), "=f"(s[109]), "=f"(s[110]), "=f"(s[111]), "=f"(s[112]), "=f"(s[113]), "=f"(s[114]), "=f"(s[115]), "=f"(s[116]), "=f"(s[117]), "=f"(s[118]), "=f"(s[119]), "=f"(s[120]), "=f"(s[121]), "=f"(s[122]), "=f"(s[123]), "=f"(s[124]), "=f"(s[125]), "=f"(s[126]), "=f"(s[127])
+        : "r"(taddr)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -196,6 +256,32 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Paired fp32 arithmetic (one instruction for two lanes of data) and the
+// three-input maximum: fewer issue slots per logit in the softmax loops.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 r;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 r;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // 2^x on the special-function unit (PTX ex2.approx, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -207,6 +293,12 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// Two fp32 -> one f16x2 word (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
 // Low half / high half of a bf16x2 word back to fp32 (exact).

@@ -5,10 +5,16 @@ Tolerances (float results) and their source:
 * selected indices: identical sets, except a swap between two keys whose
   oracle scores differ by less than 1e-6 relative (the stated exemption);
 * beta: |beta_gpu - beta_oracle| <= 1e-3 wherever the oracle weight
-  w_i >= 1e-2 * max w; below that weight, |w_gpu - w_oracle| <= 1e-5 * max w
-  (log w is not a well-conditioned function of a weight 100x below the
-  largest: fp32 inputs of A' already carry ~1e-6 relative error, which the
-  NNLS conditioning amplifies);
+  w_i >= 1e-6 * max w and beta_i is determined to that tolerance by fp32
+  logits.  The second condition is measured, per weight, by re-solving the
+  oracle's fit on the relative masses that fp32 logits give (the raw logit
+  and the log-mass rounded to float32 as a fp32 pipeline holds them,
+  everything else in float64): a weight whose beta that rounding alone moves
+  by more than a quarter of the tolerance is not determined by any fp32
+  computation of the logits, and is compared as a weight instead,
+  |w_gpu - w_oracle| <= 1e-5 * max w.  Where the oracle's w_i < 1e-6 max w,
+  the GPU's must be <= 2e-6 max w.  (When the caller passes no queries the
+  tolerance applies to every weight above the floor.)
 * C_v: relative Frobenius error <= 2e-3 per head;
 * compacted attention on held-out queries: relative Frobenius <= 1e-3 per head;
 * intermediates (O, lse, scores) against fp32 round-off bounds derived in the
@@ -28,8 +34,10 @@ from workloads.batch import generate
 
 IDX_REL_GAP = 1e-6
 BETA_ABS = 1e-3
-BETA_W_FLOOR = 1e-2
+BETA_W_FLOOR = 1e-6
+W_FLOOR_GPU = 2e-6
 W_ABS_BELOW = 1e-5
+FP32_SENS_SHARE = 0.25
 CV_REL = 2e-3
 OHAT_REL = 1e-3
 
@@ -91,6 +99,11 @@ def run_oracle_head(w, inputs, h, t, idx=None):
     return r, Ohat
 
 
+def head_queries(w, inputs, h):
+    """Float64 reference queries of head h (for compare_head's Q)."""
+    return oracle.decode(inputs["Q"][h], w.dtype)
+
+
 def continue_oracle(Q, K, V, r, idx, scale):
     """The oracle's result for one head continued from a given (valid)
     selection idx instead of its own."""
@@ -101,6 +114,28 @@ def continue_oracle(Q, K, V, r, idx, scale):
     Cv, lam = oracle.fit_values(X, r.O, V[idx])
     return oracle.HeadResult(idx=idx, score=r.score, lse=r.lse, O=r.O, Ck=Ck, w=wv, beta=beta, Cv=Cv, mu=mu,
                              lam=lam, mass=Ap @ wv)
+
+
+def fp32_logit_beta(Q, r, scale, refit=None, bias=None):
+    """beta of the oracle's fit re-solved on the relative masses that fp32
+    logits give: the raw logit q . C_k[i], the log-mass lse_q and the kept
+    keys' input biases (in log2 units) rounded to float32, the scaled sum
+    rounded once more (one fused multiply-add), everything else in float64.
+    refit(A) -> beta replaces the plain NNLS (for fits with pinned weights);
+    bias (float64 [t], the kept keys' input biases) is added to the fitted
+    log-weights as the biased compaction does."""
+    ln2 = math.log(2.0)
+    c2 = float(np.float32(scale / ln2))
+    S = (Q @ r.Ck.T).astype(np.float32).astype(np.float64)
+    lse2 = (r.lse / ln2).astype(np.float32).astype(np.float64)
+    b2 = np.zeros(S.shape[1]) if bias is None else (bias / ln2).astype(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        l2 = (S * c2 + b2[None, :] - lse2[:, None]).astype(np.float32).astype(np.float64)
+    A = np.exp2(l2)
+    if refit is not None:
+        return refit(A)
+    beta = oracle.fit_beta(A)[1]
+    return beta if bias is None else bias + beta
 
 
 def idx_check(gpu_idx, or_idx, or_score):
@@ -118,7 +153,10 @@ def idx_check(gpu_idx, or_idx, or_score):
     return ok, True
 
 
-def compare_head(g, h, r, Ohat_or, report):
+def compare_head(g, h, r, Ohat_or, report, Q=None, scale=None, refit=None, bias=None):
+    """Head h of the GPU's outputs g against the oracle's result r (tolerances
+    in the module docstring).  Q (float64 reference queries of the head) and
+    scale enable the per-weight fp32 determination of beta."""
     off0, off1 = g["offsets"][h], g["offsets"][h + 1]
     gi = g["idx"][off0:off1]
     ok, swapped = idx_check(gi, r.idx, r.score)
@@ -129,14 +167,30 @@ def compare_head(g, h, r, Ohat_or, report):
     bg = g["beta"][off0:off1]
     wo, bo = r.w, r.beta
     wmax = wo.max()
-    big = wo >= BETA_W_FLOOR * wmax
-    db = np.abs(bg[big] - bo[big])
+    live = wo >= BETA_W_FLOOR * wmax
+    determined = np.ones_like(live)
+    if Q is not None:
+        b32 = fp32_logit_beta(Q, r, scale if scale is not None else 1.0 / math.sqrt(Q.shape[1]), refit, bias)
+        with np.errstate(invalid="ignore"):
+            sens = np.where(np.isfinite(b32) & live, np.abs(b32 - bo), np.inf)
+        determined = sens <= FP32_SENS_SHARE * BETA_ABS
+    check = live & determined
+    db = np.abs(bg[check] - bo[check])
     report["beta_max_abs"] = float(db.max()) if db.size else 0.0
-    assert np.all(np.isfinite(bg[big])) and report["beta_max_abs"] <= BETA_ABS, f"head {h}: beta {report['beta_max_abs']}"
-    dw = np.abs(wg[~big] - wo[~big])
-    report["w_small_max_abs"] = float(dw.max() / wmax) if dw.size else 0.0
-    assert report["w_small_max_abs"] <= W_ABS_BELOW, f"head {h}: small weights {report['w_small_max_abs']}"
-    np.testing.assert_allclose(np.exp(bg[wg > 0]), wg[wg > 0], rtol=2e-6)
+    small = check & (wo < 1e-2 * wmax)
+    report["small_weights"] = int(small.sum())
+    report["beta_small_max_abs"] = float(np.abs(bg[small] - bo[small]).max()) if small.any() else 0.0
+    report["undetermined"] = int((live & ~determined).sum())
+    assert np.all(np.isfinite(bg[check])) and report["beta_max_abs"] <= BETA_ABS, f"head {h}: beta {report['beta_max_abs']}"
+    und = live & ~determined
+    dw = np.abs(wg[und] - wo[und])
+    report["w_undetermined_max_abs"] = float(dw.max() / wmax) if dw.size else 0.0
+    assert report["w_undetermined_max_abs"] <= W_ABS_BELOW, f"head {h}: weights {report['w_undetermined_max_abs']}"
+    report["w_below_floor_max"] = float(wg[~live].max() / wmax) if (~live).any() else 0.0
+    assert report["w_below_floor_max"] <= W_FLOOR_GPU, f"head {h}: weights below the floor {report['w_below_floor_max']}"
+    # beta = log w (plus the kept key's input bias on a biased cache)
+    b_in = np.zeros_like(bg) if bias is None else np.where(np.isfinite(bias), bias, 0.0)
+    np.testing.assert_allclose(np.exp(bg[wg > 0] - b_in[wg > 0]), wg[wg > 0], rtol=2e-6)
     assert np.all(np.isneginf(bg[wg == 0]))
     cv = g["Cv"][off0:off1]
     report["cv_rel"] = float(np.linalg.norm(cv - r.Cv) / np.linalg.norm(r.Cv))

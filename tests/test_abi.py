@@ -37,7 +37,7 @@ def test_exports_every_declared_symbol():
 
 def test_version_and_status_strings():
     assert "sm_103a" in kvc.version()
-    for code in (0, 1, 2, 3, 4, 5, 16, 17, 18, 19, 20):
+    for code in (0, 1, 2, 3, 4, 5, 16, 17, 18, 19, 20, 21):
         assert kvc.status_string(code) not in ("", "unknown status")
     assert kvc.status_string(12345) == "unknown status"
 
@@ -91,6 +91,7 @@ def test_rejects_bad_problems_on_host():
     assert _call(good, prm=kvc.default_params(eps_mu=0.0)) == kvc.ERR_INVALID_ARG
     assert _call(good, prm=kvc.default_params(flags=8)) == kvc.ERR_INVALID_ARG
     assert _call(good, prm=kvc.default_params(keep_first=200, keep_last=100)) == kvc.ERR_INVALID_ARG
+    assert _call(good, prm=kvc.default_params(wait_timeout_us=0)) == kvc.ERR_INVALID_ARG
 
 
 def test_chunked_rejects_bad_shapes_on_host():
@@ -132,5 +133,36 @@ def test_attend_rejects_bad_args_on_host():
 
 def test_struct_layouts_match_header():
     assert ctypes.sizeof(kvc.Problem) == 24
-    assert ctypes.sizeof(kvc.Params) == 36
+    assert ctypes.sizeof(kvc.Params) == 40
     assert ctypes.sizeof(kvc.HeadRecord) == 32
+
+
+def test_biased_rejects_bad_args_on_host():
+    p = kvc.make_problem(2, 64, 256, 128, kvc.DTYPE_BF16, 32)
+    ws = kvc.workspace_size_biased(p)
+    assert ws > kvc.workspace_size(p)          # room for the key biases
+    ptr = 0x100000
+
+    def call(prm=None, bias=ptr, V=ptr, ws_bytes=ws):
+        return kvc.compact_biased(p, prm, ptr, ptr, bias, V, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ws_bytes,
+                                  stream=0)
+    assert call(bias=None) == kvc.ERR_INVALID_ARG
+    assert call(bias=0x100002) == kvc.ERR_ALIGN
+    assert call(V=0x100004) == kvc.ERR_ALIGN
+    assert call(ws_bytes=16) == kvc.ERR_WORKSPACE
+    assert call(prm=kvc.default_params(flags=kvc.FLAG_SELECT_OMP)) == kvc.ERR_INVALID_ARG
+
+
+def test_debug_build_compiles_and_exports():
+    """The KVC_DEBUG build (kernels check data-derived indices and record
+    KVC_ERR_DEBUG_BOUNDS instead of accessing out of range) compiles for
+    sm_103a and exports the same interface."""
+    path = kbuild.build(debug=True)
+    L = ctypes.CDLL(path)
+    for n in _declared():
+        assert hasattr(L, n), n
+    L.kvc_version.restype = ctypes.c_char_p
+    assert L.kvc_version().decode().endswith("debug")
+    L.kvc_status_string.argtypes = [ctypes.c_int]
+    L.kvc_status_string.restype = ctypes.c_char_p
+    assert b"debug" in L.kvc_status_string(kvc.ERR_DEBUG_BOUNDS)

@@ -99,7 +99,7 @@ def _check_chunked(w, buds, keep_first=0, keep_last=0):
             np.testing.assert_array_equal(g["Ck"][o0:o1], Kh[pos])
             gc = {"offsets": np.array([0, o1 - o0]), "idx": local, "w": g["w"][o0:o1], "beta": g["beta"][o0:o1],
                   "Cv": g["Cv"][o0:o1]}
-            compare_head(gc, 0, r, None, {"head": h, "chunk": ch})
+            compare_head(gc, 0, r, None, {"head": h, "chunk": ch}, Q=Qh, scale=scale)
             parts.append(r)
         if not any_swap:
             h0, h1 = g["offsets"][h * C], g["offsets"][(h + 1) * C]

@@ -89,7 +89,7 @@ def _check(w, buds=None):
                                  mu=0.0, lam=0.0, mass=None)
         r_or = continue_oracle(Qh, Kh, Vh, stub, np.sort(og), scale)
         Ohat = oracle.attend(oracle.decode(inputs["Qt"][h], w.dtype), r_or.Ck, r_or.beta, r_or.Cv, scale)
-        compare_head(g, h, r_or, Ohat, {"head": h})
+        compare_head(g, h, r_or, Ohat, {"head": h}, Q=Qh, scale=scale)
     return exact
 
 

@@ -25,7 +25,7 @@ def _lib():
     kvc.lib()
 
 
-from parity import compare_head, run_gpu, run_oracle_head  # noqa: E402
+from parity import compare_head, head_queries, run_gpu, run_oracle_head  # noqa: E402
 
 
 def _check(w, heads=None, buds=None, check_intermediates=True):
@@ -53,7 +53,7 @@ def _check(w, heads=None, buds=None, check_intermediates=True):
         from oracle import decode
         K = decode(inputs["K"][h], w.dtype)
         np.testing.assert_array_equal(g["Ck"][o0:o1], K[g["idx"][o0:o1]])
-        rep = compare_head(g, h, r, Ohat, {"head": h})
+        rep = compare_head(g, h, r, Ohat, {"head": h}, Q=head_queries(w, inputs, h))
         reports.append(rep)
     return reports
 
@@ -73,7 +73,7 @@ def test_small_cholesky_cv_path():
     assert np.all(g["status"] == 0)
     for h in range(w.H):
         r, Ohat = run_oracle_head(w, inputs, h, w.t)
-        compare_head(g, h, r, Ohat, {"head": h})
+        compare_head(g, h, r, Ohat, {"head": h}, Q=head_queries(w, inputs, h))
 
 
 def test_config1_fp32_full():
@@ -121,15 +121,16 @@ def test_many_heads():
 
 
 def test_degenerate_tiny_shapes():
-    # a single key, a budget of one, very few queries
+    """A single key, a budget of one, one query, t = T: every output (kept
+    keys, beta, C_v, held-out attention) against the oracle."""
     for (n, T, t) in [(5, 1, 1), (3, 70, 1), (1, 64, 2), (7, 65, 65)]:
         w = small_variant(WORKLOADS[2], H=2, n=n, T=T, t=t, d=64)
         g, inputs = run_gpu(w)
         assert np.all(g["status"] == 0), (n, T, t, g["status"])
+        assert np.all(g["attend_status"] == 0), (n, T, t)
         for h in range(w.H):
             r, Ohat = run_oracle_head(w, inputs, h, t)
-            o0, o1 = g["offsets"][h], g["offsets"][h + 1]
-            assert set(g["idx"][o0:o1].tolist()) == set(r.idx.tolist())
+            compare_head(g, h, r, Ohat, {"head": h}, Q=head_queries(w, inputs, h))
 
 
 def test_bad_budgets_flagged_per_head():

@@ -32,7 +32,7 @@ def _lib():
 
 
 import oracle  # noqa: E402
-from oracle.tam import allocate_budgets, compact_head_tam, window_attention  # noqa: E402
+from oracle.tam import allocate_budgets, compact_head_tam, fit_beta_fixed, window_attention  # noqa: E402
 from parity import compare_head, to_torch  # noqa: E402
 from workloads.batch import generate  # noqa: E402
 
@@ -90,7 +90,8 @@ def _check(w, buds, R, c):
         np.testing.assert_array_equal(g["Cv"][o0:o1][kept_piv], Vh[g["idx"][o0:o1][kept_piv]])
         assert set(np.flatnonzero(piv[h])) <= set(g["idx"][o0:o1].tolist())
         Ohat = oracle.attend(oracle.decode(inputs["Qt"][h], w.dtype), r.Ck, r.beta, r.Cv, scale)
-        compare_head(g, h, r, Ohat, {"head": h})
+        kp = piv[h][r.idx]
+        compare_head(g, h, r, Ohat, {"head": h}, Q=Qh, scale=scale, refit=lambda A, kp=kp: fit_beta_fixed(A, kp)[1])
     return n_piv_total
 
 
