@@ -128,8 +128,10 @@ typedef struct kvc_params {
  * the target is 1 per query; a step adds the key with the largest
  * <p_j, r> / ||p_j|| (ties to the lower position) where r is the residual of
  * the least-squares fit of 1 on the keys chosen so far; forced positions come
- * first.  beta and C_v are then fitted as usual.  The workspace grows by the
- * fp32 P of every head (H * T * n * 4 bytes) and an orthonormal basis
+ * first.  beta and C_v are then fitted as usual.  With bf16 inputs every
+ * step recomputes the correlations <p_j, r> on the tensor cores (Q K^T
+ * again, weighted by r); with fp32 inputs the fp32 P of every head is kept
+ * (H * T * n * 4 bytes of workspace).  Both keep an orthonormal basis
  * (H * max_t * n * 4 bytes); the selection order is readable at
  * kvc_workspace_offset item 5.  The pursuit is sequential over t: expect it
  * to cost far more than the default selection.  Not for kvc_compact_chunked. */

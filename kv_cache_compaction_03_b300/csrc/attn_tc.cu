@@ -20,7 +20,9 @@
 //   k_colscore_tc   K-major pass: S^T = K Q^T per key tile, then every key
 //                   row sums exp(2 (S - lse)) over all queries: the RMS
 //                   attention score of each key (key selection aggregated
-//                   by RMS).
+//                   by RMS).  Its WEIGHTED form sums exp(S - lse_q) r_q
+//                   instead, <p_j, r> for every key j: the correlations of a
+//                   step of key selection by matching pursuit (omp.cu).
 //
 // Q heads: head h reads reference queries of head h / qdiv (qdiv > 1 when
 // several chunks of one cache share its queries).
@@ -381,12 +383,15 @@ struct ColLayout {
 // thread), frees the buffer and adds exp2(2 (S c2 - lse2_q)) over the 128
 // queries.  The log-masses are kept doubled and negated in shared memory so
 // that one FFMA (two, paired, per instruction) forms the exponent.
-template <int D, int NS, bool BIAS>
+template <int D, int NS, bool BIAS, bool WEIGHTED>
 __global__ void __launch_bounds__(kColThreads, 1)
     k_colscore_tc(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
                   const float* __restrict__ lse2, int n, int T, float c2, float* __restrict__ score,
                   int32_t* __restrict__ status, int qdiv, long long wait_limit, const float* __restrict__ bias2,
-                  int Tb) {
+                  int Tb, const float* __restrict__ rw, int64_t rstride) {
+    // WEIGHTED: the shared log-mass chunk holds half the queries, followed by
+    // their weights r_q
+    constexpr int kChunk = WEIGHTED ? kLseChunk / 2 : kLseChunk;
     using L = ColLayout<D, NS>;
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
@@ -496,13 +501,15 @@ __global__ void __launch_bounds__(kColThreads, 1)
         // reload is always reached by all eight warps.
         for (int i = 0; i < nq; ++i) {
             const int qb = i * TB;
-            if (qb % kLseChunk == 0) {
-                // doubled log-masses of the next chunk; +inf past n zeroes those columns
-                const int cnt = min(kLseChunk, ((n - qb + TB - 1) / TB) * TB);
+            if (qb % kChunk == 0) {
+                // the next chunk's log-masses, negated (doubled for P^2); -inf
+                // past n zeroes those columns; WEIGHTED: and the weights
+                const int cnt = min(kChunk, ((n - qb + TB - 1) / TB) * TB);
                 asm volatile("bar.sync 1, 256;" ::: "memory");
                 for (int e = ct; e < cnt; e += 256) {
                     const int q = qb + e;
-                    lse_s[e] = (q < n) ? -2.f * lse2[(int64_t)h * n + q] : -INFINITY;
+                    lse_s[e] = (q < n) ? (WEIGHTED ? -1.f : -2.f) * lse2[(int64_t)h * n + q] : -INFINITY;
+                    if (WEIGHTED) lse_s[kChunk + e] = (q < n) ? rw[(int64_t)h * rstride + q] : 0.f;
                 }
                 asm volatile("bar.sync 1, 256;" ::: "memory");
             }
@@ -515,9 +522,23 @@ __global__ void __launch_bounds__(kColThreads, 1)
             tmem_ld128_wait(sbase, s);          // the whole row in one load
             fence_before_sync();
             mbar_arrive(s_empty + b);
-            const float4* ls = reinterpret_cast<const float4*>(lse_s + (qb % kLseChunk));
-            const float2 cx2 = make_float2(c2x, c2x), kb = make_float2(kb2, kb2);
+            const float4* ls = reinterpret_cast<const float4*>(lse_s + (qb % kChunk));
             float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
+            if (WEIGHTED) {
+                const float4* rs = reinterpret_cast<const float4*>(lse_s + kChunk + (qb % kChunk));
+                const float2 cc2 = make_float2(c2, c2);
+#pragma unroll
+                for (int c = 0; c < 128; c += 4) {
+                    const float4 l4 = ls[c / 4], r4 = rs[c / 4];     // -lse2 and r of four queries
+                    const float2 x01 = ffma2(make_float2(s[c], s[c + 1]), cc2, make_float2(l4.x, l4.y));
+                    const float2 x23 = ffma2(make_float2(s[c + 2], s[c + 3]), cc2, make_float2(l4.z, l4.w));
+                    a01 = ffma2(make_float2(ex2(x01.x), ex2(x01.y)), make_float2(r4.x, r4.y), a01);
+                    a23 = ffma2(make_float2(ex2(x23.x), ex2(x23.y)), make_float2(r4.z, r4.w), a23);
+                }
+                acc += (double)((a01.x + a01.y) + (a23.x + a23.y));
+                continue;
+            }
+            const float2 cx2 = make_float2(c2x, c2x), kb = make_float2(kb2, kb2);
 #pragma unroll
             for (int c = 0; c < 128; c += 4) {
                 const float4 l4 = ls[c / 4];    // -2 lse2 of four queries
@@ -534,7 +555,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
             acc += (double)((a01.x + a01.y) + (a23.x + a23.y));
         }
         const int key = k0 + g * TB + row;
-        if (ok && key < T) score[(int64_t)h * T + key] = (float)sqrt(acc / (double)n);
+        if (ok && key < T) score[(int64_t)h * T + key] = WEIGHTED ? (float)acc : (float)sqrt(acc / (double)n);
     }
     if (threadIdx.x == 0 && *abort_flag) set_status(status, h, KVC_ERR_TIMEOUT);
     fence_before_sync();
@@ -784,19 +805,19 @@ cudaError_t launch_fwd_t(const void* Q, const void* K, const void* V, int H, int
     return cudaGetLastError();
 }
 
-template <int D, int NS, bool BIAS>
+template <int D, int NS, bool BIAS, bool WEIGHTED = false>
 cudaError_t launch_col_t(const void* Q, const void* K, const float* lse2, int H, int n, int T, float c2,
                          float* score, int32_t* status, int qdiv, long long wait_limit, const float* bias2,
-                         cudaStream_t st) {
+                         cudaStream_t st, const float* rw = nullptr, int64_t rstride = 0) {
     CUtensorMap mK, mQ;
     if (!make_map(&mK, K, D, T, H) || !make_map(&mQ, Q, D, n, H / qdiv)) return cudaErrorInvalidValue;
     constexpr int smem = ColLayout<D, NS>::kBytes;
-    auto kern = k_colscore_tc<D, NS, BIAS>;
+    auto kern = k_colscore_tc<D, NS, BIAS, WEIGHTED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((T + 2 * TB - 1) / (2 * TB), H);
     kern<<<grid, kColThreads, smem, st>>>(mK, mQ, lse2, n, T, c2, score, status, qdiv, wait_limit, bias2,
-                                          (int)round_up(T, 256));
+                                          (int)round_up(T, 256), rw, rstride);
     return cudaGetLastError();
 }
 
@@ -868,6 +889,18 @@ cudaError_t launch_colscore_tc(int d, const void* Q, const void* K, const float*
                                                   st)
                     : launch_col_t<64, 6, false>(Q, K, lse2, H, n, T, c2, score, status, qdiv, wait_limit, nullptr,
                                                  st);
+}
+
+// out[h][j] = sum_q exp2(S_qj c2 - lse2_q) r[h][q] for every key j (bf16
+// inputs, tensor cores): the matching-pursuit correlations <p_j, r>.  r has
+// row stride rstride.
+cudaError_t launch_corr_tc(int d, const void* Q, const void* K, const float* lse2, int H, int n, int T, float c2,
+                           const float* r, int64_t rstride, float* out, int32_t* status, long long wait_limit,
+                           cudaStream_t st) {
+    return d == 128 ? launch_col_t<128, 3, false, true>(Q, K, lse2, H, n, T, c2, out, status, 1, wait_limit, nullptr,
+                                                        st, r, rstride)
+                    : launch_col_t<64, 6, false, true>(Q, K, lse2, H, n, T, c2, out, status, 1, wait_limit, nullptr,
+                                                       st, r, rstride);
 }
 
 }  // namespace kvc

@@ -34,9 +34,9 @@ cudaError_t launch_attend(int, int, const void*, int, const void*, const float*,
 cudaError_t launch_attend_decode(int, int, const void*, int, const void*, const float*, const float*, const int32_t*,
                                  int, float, float*, int32_t*, cudaStream_t);
 int attend_decode_max_queries();
-size_t omp_workspace_bytes(int H, int n, int T, int max_t);
-size_t omp_order_offset(int H, int n, int T, int max_t);
-int omp_launches(int max_t);
+size_t omp_workspace_bytes(int dtype, int H, int n, int T, int max_t);
+size_t omp_order_offset(int dtype, int H, int n, int T, int max_t);
+int omp_launches(int dtype, int max_t);
 cudaError_t launch_colmean_simt(int dtype, int d, const void* Q, const void* K, const float* lse2, int H, int n, int T,
                                 float c2, float* out, const int32_t* status, cudaStream_t st);
 int tam_max_segments();
@@ -57,7 +57,7 @@ cudaError_t launch_select_seg(const float* score, int H, int T, const int32_t* o
                               int32_t* idx_out, int32_t* status, cudaStream_t st);
 cudaError_t launch_omp_select(int dtype, int d, const void* Q, const void* K, const float* lse2, float c2, int H,
                               int n, int T, int max_t, const int32_t* offsets, int keep_first, int keep_last,
-                              void* ws, int32_t* idx_out, int32_t* status, cudaStream_t st);
+                              void* ws, int32_t* idx_out, int32_t* status, long long wait_limit, cudaStream_t st);
 cudaError_t launch_gram_sym_tc(const void* Ah, const void* Al, const int32_t* offsets, int H, int n, int max_t,
                                int64_t ld, float* C, int64_t ldc, int32_t* status, long long wait_limit,
                                cudaStream_t st);
@@ -256,7 +256,7 @@ static Layout make_layout(const kvc_problem& p, const kvc_params& prm, TamShape 
         L.bk = carve(c, H * mt * 4);
     }
     // key selection by matching pursuit: the relative mass of every key and the pursuit's state
-    L.omp = (prm.flags & KVC_FLAG_SELECT_OMP) ? carve(c, omp_workspace_bytes(p.H, p.n, p.T, p.max_t)) : 0;
+    L.omp = (prm.flags & KVC_FLAG_SELECT_OMP) ? carve(c, omp_workspace_bytes(p.dtype, p.H, p.n, p.T, p.max_t)) : 0;
     if (ts.n_win > 0) {
         L.tO = carve(c, H * (size_t)ts.n_win * d * 4);
         L.tlse = carve(c, H * (size_t)ts.n_win * 4);
@@ -370,7 +370,7 @@ kvc_status kvc_workspace_offset(const kvc_problem* p, const kvc_params* prm, int
         case 4: *offset = L.hs; break;
         case 5:
             if (!(q.flags & KVC_FLAG_SELECT_OMP)) return KVC_ERR_INVALID_ARG;
-            *offset = L.omp + omp_order_offset(p->H, p->n, p->T, p->max_t);
+            *offset = L.omp + omp_order_offset(p->dtype, p->H, p->n, p->T, p->max_t);
             break;
         case 6: *offset = L.L2; break;
         default: return KVC_ERR_INVALID_ARG;
@@ -477,9 +477,9 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
                   launch_select_seg(score, H, T, offsets, tam->bounds, tam->nseg, tam->pivots, skeep, soff, idx_out,
                                     head_status, st));
     } else if (omp)
-        KVC_STAGE("omp", omp_launches(mt),
+        KVC_STAGE("omp", omp_launches(dt, mt),
                   launch_omp_select(dt, d, Q_ref, K, lse2, c2, H, n, T, mt, offsets, q.keep_first, q.keep_last,
-                                    ws + L.omp, idx_out, head_status, st));
+                                    ws + L.omp, idx_out, head_status, wl, st));
     else
         KVC_STAGE("select", 1,
                   launch_select(score, H, T, offsets, chunks, q.keep_first, q.keep_last, idx_out, head_status, st));

@@ -13,17 +13,29 @@
 // Gram-Schmidt, normalised and appended, and r loses its component along it.
 // A column whose remainder is below 1e-5 of its norm adds no direction.
 //
-// Layout (all per head, fp32): P key-major [T][ldn] (a column is contiguous),
-// norms [T], residual r [ldn], basis [max_t][ldn], working column v [ldn].
+// bf16 inputs recompute the dictionary instead of storing it: ||p_j|| is
+// sqrt(n) times the RMS key score, every step's <p_j, r> comes from the
+// weighted form of the tensor-core key-score pass (S = K Q^T again,
+// exp2(S c2 - lse2_q) weighted by r_q and summed; attn_tc.cu), and the
+// picked key's column is recomputed from Q and K_j.  fp32 inputs keep P.
+//
+// Layout (all per head, fp32): P key-major [T][ldn] (fp32 inputs; a column is
+// contiguous) or the correlations [T] (bf16 inputs), norms [T], residual r
+// [ldn], basis [max_t][ldn], working column v [ldn].
 // Kernels, all heads in parallel, one pursuit step per round of launches:
-//   k_omp_probs     P = exp2(Q K^T c2 - lse2), written key-major
-//   k_omp_norms     ||p_j||
+//   k_omp_probs     P = exp2(Q K^T c2 - lse2), written key-major (fp32)
+//   k_omp_norms     ||p_j|| from P (fp32); k_omp_init from the RMS score (bf16)
 //   k_omp_corr      <p_j, r> / ||p_j|| for the keys not chosen; CTA argmax
+//                   (fp32: warp per key over P; bf16: k_omp_corr_pre, thread
+//                   per key over the recomputed correlations)
 //   k_omp_pick      the step's key (forced position or argmax); v = p_j
+//                   (fp32: copied from P; bf16: k_omp_col recomputes it)
 //   k_omp_proj      c_k = <basis_k, v>
 //   k_omp_sub       v -= sum_k c_k basis_k
 //   k_omp_finish    basis_s = v / ||v||, r -= <basis_s, r> basis_s
 //   k_omp_idx       kept positions in ascending order
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace kvc {
@@ -31,7 +43,9 @@ namespace kvc {
 namespace {
 
 struct OmpArgs {
-    float* P;                  // [H][T][ldn]
+    float* P;                  // [H][T][ldn] (fp32 inputs; null for bf16)
+    float* corr;               // [H][T] correlations, first the RMS scores (bf16 inputs)
+    int32_t* pick;             // [H] the step's key
     float* norms;              // [H][T]
     uint8_t* chosen;           // [H][T]
     float* r;                  // [H][ldn]
@@ -238,8 +252,88 @@ __global__ void __launch_bounds__(256) k_omp_pick(OmpArgs a, int s, int nparts) 
         a.order[(int64_t)h * a.max_t + s] = j;
         a.pnorm[h] = a.norms[(int64_t)h * a.T + j];
     }
+    if (threadIdx.x == 0) a.pick[h] = j;
+    if (!a.P) return;                 // bf16: k_omp_col recomputes the column
     const float* col = a.P + ((int64_t)h * a.T + j) * a.ldn;
     for (int q = threadIdx.x; q < a.ldn; q += 256) a.v[(int64_t)h * a.ldn + q] = col[q];
+}
+
+// bf16 inputs: ||p_j|| = sqrt(n) * RMS score (the scores sit in corr), and the
+// pursuit's reset.  grid (ceil(T/256), H), block 256.
+__global__ void __launch_bounds__(256) k_omp_init(OmpArgs a) {
+    const int h = blockIdx.y;
+    if (!head_ok(a.status, h)) return;
+    if (blockIdx.x == 0) {
+        for (int q = threadIdx.x; q < a.ldn; q += 256) a.r[(int64_t)h * a.ldn + q] = q < a.n ? 1.f : 0.f;
+        if (threadIdx.x == 0) a.nbasis[h] = 0;
+    }
+    const int j = blockIdx.x * 256 + threadIdx.x;
+    if (j >= a.T) return;
+    a.norms[(int64_t)h * a.T + j] = a.corr[(int64_t)h * a.T + j] * sqrtf((float)a.n);
+    a.chosen[(int64_t)h * a.T + j] = 0;
+}
+
+// bf16 inputs: <p_j, r> / ||p_j|| from the recomputed correlations, a thread
+// per key; CTA argmax to part.  grid (ceil(T/256), H), block 256.
+__global__ void __launch_bounds__(256) k_omp_corr_pre(OmpArgs a, int s) {
+    const int h = blockIdx.y;
+    if (!head_ok(a.status, h)) return;
+    const int t = a.offsets[h + 1] - a.offsets[h];
+    if (s >= t || s < forced_count(a.T, a.keep_first, a.keep_last)) return;
+    __shared__ float sv[256];
+    __shared__ int si[256];
+    const int j = blockIdx.x * 256 + threadIdx.x;
+    float c = -INFINITY;
+    if (j < a.T && !a.chosen[(int64_t)h * a.T + j]) {
+        const float nj = a.norms[(int64_t)h * a.T + j];
+        if (nj > 0.f) c = a.corr[(int64_t)h * a.T + j] / nj;
+    }
+    sv[threadIdx.x] = c;
+    si[threadIdx.x] = c > -INFINITY ? j : INT32_MAX;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (threadIdx.x < o && sv[threadIdx.x + o] > -INFINITY) {
+            float v0 = sv[threadIdx.x];
+            int i0 = si[threadIdx.x];
+            better(v0, i0, sv[threadIdx.x + o], si[threadIdx.x + o]);
+            sv[threadIdx.x] = v0;
+            si[threadIdx.x] = i0;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) a.part[(int64_t)h * gridDim.x + blockIdx.x] = make_float2(sv[0], __int_as_float(si[0]));
+}
+
+// bf16 inputs: v = p_j for the picked key j, p_j[q] = exp2(q . K_j c2 -
+// lse2_q) for q < n (0 up to ldn).  grid (ceil(ldn/64), H), block 256: a
+// warp per 8 queries, lanes over the head dimension.
+template <int D>
+__global__ void __launch_bounds__(256) k_omp_col(OmpArgs a, int s, const __nv_bfloat16* __restrict__ Q,
+                                                 const __nv_bfloat16* __restrict__ K, const float* __restrict__ lse2,
+                                                 float c2) {
+    const int h = blockIdx.y;
+    if (!head_ok(a.status, h)) return;
+    const int t = a.offsets[h + 1] - a.offsets[h];
+    if (s >= t) return;
+    const int j = a.pick[h];
+    if (!KVC_IN_RANGE(j >= 0 && j < a.T, a.status, h)) return;
+    constexpr int E = D / 32;                       // elements per lane
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float kj[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) kj[e] = __bfloat162float(K[((int64_t)h * a.T + j) * D + lane * E + e]);
+    for (int qq = 0; qq < 8; ++qq) {
+        const int q = blockIdx.x * 64 + warp * 8 + qq;
+        if (q >= a.ldn) break;
+        float dot = 0.f;
+        if (q < a.n) {
+            const __nv_bfloat16* qr = Q + ((int64_t)h * a.n + q) * D + lane * E;
+#pragma unroll
+            for (int e = 0; e < E; ++e) dot = fmaf(__bfloat162float(qr[e]), kj[e], dot);
+        }
+        dot = warp_sum(dot);
+        if (lane == 0) a.v[(int64_t)h * a.ldn + q] = q < a.n ? exp2f(fmaf(dot, c2, -lse2[(int64_t)h * a.n + q])) : 0.f;
+    }
 }
 
 // grid (ceil(max_t/8), H), block 256: a warp per basis vector.
@@ -366,37 +460,54 @@ cudaError_t launch_probs_t(const void* Q, const void* K, const float* lse2, floa
 
 }  // namespace
 
+namespace {
+// Bytes of the dictionary region: P for fp32 inputs, the correlations for bf16.
+size_t omp_dict_bytes(int dtype, int H, int T, size_t ldn) {
+    return dtype == KVC_DTYPE_F32 ? (size_t)H * T * ldn * 4 : (size_t)H * T * 4;
+}
+}  // namespace
+
 // Workspace of the pursuit for a problem (bytes, 256-aligned pieces).
-size_t omp_workspace_bytes(int H, int n, int T, int max_t) {
+size_t omp_workspace_bytes(int dtype, int H, int n, int T, int max_t) {
     const size_t ldn = (size_t)round_up(n, 4);
     auto al = [](size_t b) { return (b + 255) / 256 * 256; };
-    return al((size_t)H * T * ldn * 4) + al((size_t)H * T * 4) + al((size_t)H * T) + 2 * al((size_t)H * ldn * 4) +
-           al((size_t)H * max_t * ldn * 4) + al((size_t)H * max_t * 4) + al((size_t)H * 4) +
-           al((size_t)H * ((T + 7) / 8) * 8) + al((size_t)H * max_t * 4) + al((size_t)H * 4);
+    return al(omp_dict_bytes(dtype, H, T, ldn)) + al((size_t)H * T * 4) + al((size_t)H * T) +
+           2 * al((size_t)H * ldn * 4) + al((size_t)H * max_t * ldn * 4) + al((size_t)H * max_t * 4) +
+           al((size_t)H * 4) + al((size_t)H * ((T + 7) / 8) * 8) + al((size_t)H * max_t * 4) + al((size_t)H * 4) +
+           al((size_t)H * 4);
 }
 
 // Byte offset of the selection order [H][max_t] inside that workspace.
-size_t omp_order_offset(int H, int n, int T, int max_t) {
+size_t omp_order_offset(int dtype, int H, int n, int T, int max_t) {
     const size_t ldn = (size_t)round_up(n, 4);
     auto al = [](size_t b) { return (b + 255) / 256 * 256; };
-    return al((size_t)H * T * ldn * 4) + al((size_t)H * T * 4) + al((size_t)H * T) + 2 * al((size_t)H * ldn * 4) +
-           al((size_t)H * max_t * ldn * 4) + al((size_t)H * max_t * 4) + al((size_t)H * 4) +
-           al((size_t)H * ((T + 7) / 8) * 8);
+    return al(omp_dict_bytes(dtype, H, T, ldn)) + al((size_t)H * T * 4) + al((size_t)H * T) +
+           2 * al((size_t)H * ldn * 4) + al((size_t)H * max_t * ldn * 4) + al((size_t)H * max_t * 4) +
+           al((size_t)H * 4) + al((size_t)H * ((T + 7) / 8) * 8);
 }
 
-int omp_launches(int max_t) { return 3 + 7 * max_t; }
+int omp_launches(int dtype, int max_t) { return dtype == KVC_DTYPE_F32 ? 3 + 7 * max_t : 2 + 9 * max_t; }
+
+cudaError_t launch_colscore_tc(int d, const void* Q, const void* K, const float* lse2, int H, int n, int T,
+                               float c2, float* score, int32_t* status, int qdiv, long long wait_limit,
+                               const float* bias2, cudaStream_t st);
+cudaError_t launch_corr_tc(int d, const void* Q, const void* K, const float* lse2, int H, int n, int T, float c2,
+                           const float* r, int64_t rstride, float* out, int32_t* status, long long wait_limit,
+                           cudaStream_t st);
 
 // The pursuit for every head: idx_out[off .. off + t) = chosen positions,
 // ascending.  lse2 from the attention pass; forced positions first.
 cudaError_t launch_omp_select(int dtype, int d, const void* Q, const void* K, const float* lse2, float c2, int H,
                               int n, int T, int max_t, const int32_t* offsets, int keep_first, int keep_last,
-                              void* ws, int32_t* idx_out, int32_t* status, cudaStream_t st) {
+                              void* ws, int32_t* idx_out, int32_t* status, long long wait_limit, cudaStream_t st) {
     const int ldn = (int)round_up(n, 4);
     auto al = [](size_t b) { return (b + 255) / 256 * 256; };
+    const bool rec = dtype == KVC_DTYPE_BF16;          // recompute the dictionary on the tensor cores
     char* p = static_cast<char*>(ws);
     OmpArgs a{};
-    a.P = (float*)p;
-    p += al((size_t)H * T * ldn * 4);
+    a.P = rec ? nullptr : (float*)p;
+    a.corr = rec ? (float*)p : nullptr;
+    p += al(omp_dict_bytes(dtype, H, T, (size_t)ldn));
     a.norms = (float*)p;
     p += al((size_t)H * T * 4);
     a.chosen = (uint8_t*)p;
@@ -416,6 +527,8 @@ cudaError_t launch_omp_select(int dtype, int d, const void* Q, const void* K, co
     a.order = (int32_t*)p;
     p += al((size_t)H * max_t * 4);
     a.pnorm = (float*)p;
+    p += al((size_t)H * 4);
+    a.pick = (int32_t*)p;
     a.offsets = offsets;
     a.n = n;
     a.T = T;
@@ -425,23 +538,45 @@ cudaError_t launch_omp_select(int dtype, int d, const void* Q, const void* K, co
     a.keep_last = keep_last;
     a.status = status;
     cudaError_t e;
-    if (dtype == KVC_DTYPE_BF16)
-        e = d == 128 ? launch_probs_t<__nv_bfloat16, 128>(Q, K, lse2, c2, a, H, st)
-                     : launch_probs_t<__nv_bfloat16, 64>(Q, K, lse2, c2, a, H, st);
-    else
+    int nparts;
+    if (rec) {
+        // ||p_j|| from the RMS key score (into corr first)
+        e = launch_colscore_tc(d, Q, K, lse2, H, n, T, c2, a.corr, status, 1, wait_limit, nullptr, st);
+        if (e != cudaSuccess) return e;
+        nparts = (T + 255) / 256;
+        k_omp_init<<<dim3(nparts, H), 256, 0, st>>>(a);
+    } else {
         e = d == 128 ? launch_probs_t<float, 128>(Q, K, lse2, c2, a, H, st)
                      : launch_probs_t<float, 64>(Q, K, lse2, c2, a, H, st);
-    if (e != cudaSuccess) return e;
-    const int nparts = (T + 7) / 8;
-    k_omp_norms<<<dim3(nparts, H), 256, 0, st>>>(a);
+        if (e != cudaSuccess) return e;
+        nparts = (T + 7) / 8;
+        k_omp_norms<<<dim3(nparts, H), 256, 0, st>>>(a);
+    }
     const size_t sub_smem = (size_t)max_t * 4;
     if (sub_smem > 48 * 1024) {
         e = cudaFuncSetAttribute(k_omp_sub, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sub_smem);
         if (e != cudaSuccess) return e;
     }
+    const int nf = (int)std::min<int64_t>(T, (int64_t)keep_first + keep_last);   // forced steps need no correlations
     for (int s = 0; s < max_t; ++s) {
-        k_omp_corr<<<dim3(nparts, H), 256, 0, st>>>(a, s);
+        if (rec) {
+            if (s >= nf) {
+                e = launch_corr_tc(d, Q, K, lse2, H, n, T, c2, a.r, ldn, a.corr, status, wait_limit, st);
+                if (e != cudaSuccess) return e;
+                k_omp_corr_pre<<<dim3(nparts, H), 256, 0, st>>>(a, s);
+            }
+        } else {
+            k_omp_corr<<<dim3(nparts, H), 256, 0, st>>>(a, s);
+        }
         k_omp_pick<<<H, 256, 0, st>>>(a, s, nparts);
+        if (rec) {
+            if (d == 128)
+                k_omp_col<128><<<dim3((ldn + 63) / 64, H), 256, 0, st>>>(a, s, (const __nv_bfloat16*)Q,
+                                                                       (const __nv_bfloat16*)K, lse2, c2);
+            else
+                k_omp_col<64><<<dim3((ldn + 63) / 64, H), 256, 0, st>>>(a, s, (const __nv_bfloat16*)Q,
+                                                                      (const __nv_bfloat16*)K, lse2, c2);
+        }
         for (int round = 0; round < 2; ++round) {
             k_omp_proj<<<dim3((max_t + 7) / 8, H), 256, 0, st>>>(a, s);
             k_omp_sub<<<dim3((ldn + 255) / 256, H), 256, sub_smem, st>>>(a, s);
