@@ -54,6 +54,7 @@ using namespace tc;
 bool make_map(CUtensorMap* m, const void* base, int d, int rows, int H);   // tmap.cu
 bool make_map_f32(CUtensorMap* m, const void* base, int cols, int64_t ld, int rows, int H);             // tmap.cu
 bool make_map_bf16_rows32(CUtensorMap* m, const void* base, int cols, int64_t ld, int rows, int H);     // tmap.cu
+bool make_map_rows256(CUtensorMap* m, const void* base, int d, int rows, int H);                         // tmap.cu
 
 namespace {
 
@@ -364,25 +365,36 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 }
 
 // ------------------------------------------------------------ key scores
-constexpr int kLseChunk = 8192;     // queries whose lse sits in shared memory at once
-constexpr int kColThreads = 320;    // TMA warp, MMA warp, two consumer warpgroups
+constexpr int kLseChunk = 4096;     // queries whose lse sits in shared memory at once
+constexpr int QB = 256;             // queries per block: the N of every key-score product
+constexpr int kColThreads = 576;    // TMA warp, MMA warp, four consumer warpgroups
 
 template <int D, int NS>
 struct ColLayout {
-    static constexpr int kTile = (D / 64) * kBox;
-    static constexpr int kK = 0;                  // two key tiles
-    static constexpr int kQ = kK + 2 * kTile;
-    static constexpr int kLse = kQ + NS * kTile;
-    static constexpr int kBar = kLse + kLseChunk * 4;
+    static constexpr int kTileK = (D / 64) * kBox;          // [128 keys][D]
+    static constexpr int kBoxQ = QB * 128;                  // [256 rows][64 bf16]
+    static constexpr int kTileQ = (D / 64) * kBoxQ;         // [256 queries][D]
+    static constexpr int kK = 0;                            // two key tiles
+    static constexpr int kQ = kK + 2 * kTileK;
+    static constexpr int kLse = kQ + NS * kTileQ;
+    static constexpr int kRed = kLse + kLseChunk * 4;       // [2 key tiles][128 rows] (hi, lo) fp32
+    static constexpr int kBar = kRed + 2 * 128 * 8;
     static constexpr int kBytes = kBar + 256 + 1024;
 };
 
-// One CTA = two key tiles g = 0, 1 of 128 keys.  For every query tile i the
-// MMA thread computes S^T_g = K_g Q_i^T into TMEM buffer (g, i % 2) (columns
-// 256 g + 128 (i % 2)); consumer warpgroup g reads its row (one key per
-// thread), frees the buffer and adds exp2(2 (S c2 - lse2_q)) over the 128
-// queries.  The log-masses are kept doubled and negated in shared memory so
-// that one FFMA (two, paired, per instruction) forms the exponent.
+// One CTA = two key tiles g = 0, 1 of 128 keys; the queries stream through in
+// blocks of 256.  For every block i the MMA thread computes S^T_g = K_g Q_i^T
+// (M = 128 keys, N = 256 queries: an N = 256 product runs the tensor pipe
+// about 1.7 times faster per flop on this part than two of N = 128) into
+// TMEM buffer g (columns 256 g .. 256 g + 255); the two buffers alternate, so
+// the product of one key tile overlaps the exponentials of the other.  Two
+// consumer warpgroups share each key tile: both take the same rows (one key
+// per thread), warpgroup half takes the queries 128 half .. 128 half + 127
+// of the block in two loads of 64 columns and frees the buffer after the
+// second.  Each adds exp2(2 (S c2 - lse2_q)) over its queries; the two
+// halves' sums meet in shared memory at the end.  The log-masses are kept
+// doubled and negated in shared memory so that one FFMA (two, paired, per
+// instruction) forms the exponent.
 template <int D, int NS, bool BIAS, bool WEIGHTED>
 __global__ void __launch_bounds__(kColThreads, 1)
     k_colscore_tc(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
@@ -392,6 +404,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
     // WEIGHTED: the shared log-mass chunk holds half the queries, followed by
     // their weights r_q
     constexpr int kChunk = WEIGHTED ? kLseChunk / 2 : kLseChunk;
+    static_assert(kChunk % QB == 0, "a log-mass chunk holds whole query blocks");
     using L = ColLayout<D, NS>;
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
@@ -403,9 +416,9 @@ __global__ void __launch_bounds__(kColThreads, 1)
     uint64_t* k_full = bars;
     uint64_t* q_full = bars + 1;          // [NS]
     uint64_t* q_empty = q_full + NS;      // [NS]
-    uint64_t* s_full = q_empty + NS;      // [2 tiles][2 buffers]
-    uint64_t* s_empty = s_full + 4;       // [2][2]
-    uint64_t* mma_done = s_empty + 4;
+    uint64_t* s_full = q_empty + NS;      // [2 key tiles]
+    uint64_t* s_empty = s_full + 2;       // [2]
+    uint64_t* mma_done = s_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -415,9 +428,9 @@ __global__ void __launch_bounds__(kColThreads, 1)
             mbar_init(q_full + s, 1);
             mbar_init(q_empty + s, 1);
         }
-        for (int b = 0; b < 4; ++b) {
-            mbar_init(s_full + b, 1);
-            mbar_init(s_empty + b, 128);
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(s_full + g, 1);
+            mbar_init(s_empty + g, 256);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -428,25 +441,24 @@ __global__ void __launch_bounds__(kColThreads, 1)
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const int nq = (n + TB - 1) / TB;
+    const int nq = (n + QB - 1) / QB;
     const int k0 = blockIdx.x * 2 * TB;
-    constexpr uint32_t kTileBytes = (uint32_t)L::kTile;
 
     if (warp == 0) {
         if (lane == 0) {
             prefetch_tmap(&mK);
             prefetch_tmap(&mQ);
-            mbar_expect_tx(k_full, 2 * kTileBytes);
+            mbar_expect_tx(k_full, 2 * (uint32_t)L::kTileK);
             for (int g = 0; g < 2; ++g)
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_3d(sm + L::kK + g * L::kTile + c * kBox, &mK, k_full, c * 64, k0 + g * TB, h);
+                    tma_load_3d(sm + L::kK + g * L::kTileK + c * kBox, &mK, k_full, c * 64, k0 + g * TB, h);
             int issued = 0;
             for (int i = 0; i < nq; ++i) {
                 const int s = i % NS;
                 if (i >= NS && !mbar_wait(q_empty + s, (uint32_t)((i / NS) - 1) & 1u, abort_flag, wait_limit)) break;
-                mbar_expect_tx(q_full + s, kTileBytes);
+                mbar_expect_tx(q_full + s, (uint32_t)L::kTileQ);
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_3d(sm + L::kQ + s * L::kTile + c * kBox, &mQ, q_full + s, c * 64, i * TB, h / qdiv);
+                    tma_load_3d(sm + L::kQ + s * L::kTileQ + c * L::kBoxQ, &mQ, q_full + s, c * 64, i * QB, h / qdiv);
                 issued = i + 1;
             }
             drain_wait(k_full, 0);
@@ -456,26 +468,28 @@ __global__ void __launch_bounds__(kColThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idesc = idesc_bf16(128, QB, false, false);
             const uint32_t aK0 = smem_addr(sm + L::kK);
             bool ok = mbar_wait(k_full, 0, abort_flag, wait_limit);
             for (int i = 0; ok && i < nq; ++i) {
                 const int s = i % NS;
                 if (!mbar_wait(q_full + s, (uint32_t)(i / NS) & 1u, abort_flag, wait_limit)) break;
-                const uint32_t aQ = smem_addr(sm + L::kQ + s * L::kTile);
+                const uint32_t aQ = smem_addr(sm + L::kQ + s * L::kTileQ);
                 for (int g = 0; g < 2; ++g) {
-                    const int b = g * 2 + (i & 1);
-                    if (i >= 2 && !mbar_wait(s_empty + b, (uint32_t)((i >> 1) - 1) & 1u, abort_flag, wait_limit)) {
+                    // buffer g is free once both warpgroups loaded block i - 1 from it
+                    if (i >= 1 && !mbar_wait(s_empty + g, (uint32_t)(i - 1) & 1u, abort_flag, wait_limit)) {
                         ok = false;
                         break;
                     }
                     fence_after_sync();
-                    const uint32_t aK = aK0 + (uint32_t)(g * L::kTile);
-                    const uint32_t dS = tmem + (uint32_t)(g * 256 + (i & 1) * 128);
+                    const uint32_t aK = aK0 + (uint32_t)(g * L::kTileK);
+                    const uint32_t dS = tmem + (uint32_t)(g * QB);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(dS, kmajor_desc(aK, kk), kmajor_desc(aQ, kk), idesc, kk > 0);
-                    mma_commit(s_full + b);
+                        mma_ss(dS, kmajor_desc(aK, kk),
+                               sdesc_sw128(aQ + (uint32_t)((kk >> 2) * L::kBoxQ + (kk & 3) * 32), 16, 1024), idesc,
+                               kk > 0);
+                    mma_commit(s_full + g);
                 }
                 if (!ok) break;
                 mma_commit(q_empty + s);
@@ -485,77 +499,93 @@ __global__ void __launch_bounds__(kColThreads, 1)
         }
         __syncwarp();
     } else {
-        // consumer warpgroup g: one key row per thread
-        const int g = (warp - 2) >> 2;
+        // consumer warpgroup (g, half): one key row per thread, half the queries
+        const int cw = (warp - 2) >> 2;
+        const int g = cw >> 1, half = cw & 1;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const int ct = threadIdx.x - 64;            // 0..255 over both warpgroups
+        const int ct = threadIdx.x - 64;            // 0..511 over the four warpgroups
         const float c2x = 2.f * c2;
         // this row's key bias, doubled like the logit (the grid covers Tb keys)
         const float kb2 = BIAS ? 2.f * bias2[(int64_t)h * Tb + k0 + g * TB + row] : 0.f;
-        double acc = 0.0;
+        // fp32 pairs (hi, lo) carry the sum over the queries: the fp64 pipe
+        // of this part is far too slow for a per-block double add
+        dfloat acc{0.f, 0.f};
         bool ok = true;
-        // Every consumer warp runs all iterations (after an abort it only
-        // skips the work) so that the named barrier around the log-mass
-        // reload is always reached by all eight warps.
+        // Every consumer warp runs all blocks (after an abort it only skips
+        // the work) so that the named barriers around the log-mass reload
+        // and the final combine are always reached by all sixteen.
         for (int i = 0; i < nq; ++i) {
-            const int qb = i * TB;
+            const int qb = i * QB;
             if (qb % kChunk == 0) {
                 // the next chunk's log-masses, negated (doubled for P^2); -inf
                 // past n zeroes those columns; WEIGHTED: and the weights
-                const int cnt = min(kChunk, ((n - qb + TB - 1) / TB) * TB);
-                asm volatile("bar.sync 1, 256;" ::: "memory");
-                for (int e = ct; e < cnt; e += 256) {
+                const int cnt = min(kChunk, ((n - qb + QB - 1) / QB) * QB);
+                asm volatile("bar.sync 1, 512;" ::: "memory");
+                for (int e = ct; e < cnt; e += 512) {
                     const int q = qb + e;
                     lse_s[e] = (q < n) ? (WEIGHTED ? -1.f : -2.f) * lse2[(int64_t)h * n + q] : -INFINITY;
                     if (WEIGHTED) lse_s[kChunk + e] = (q < n) ? rw[(int64_t)h * rstride + q] : 0.f;
                 }
-                asm volatile("bar.sync 1, 256;" ::: "memory");
+                asm volatile("bar.sync 1, 512;" ::: "memory");
             }
-            const int b = g * 2 + (i & 1);
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (uint32_t)(i >> 1) & 1u, abort_flag, wait_limit));
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full + g, (uint32_t)i & 1u, abort_flag, wait_limit));
             if (!ok) continue;
             fence_after_sync();
-            const uint32_t sbase = tmem + lane_off + (uint32_t)(g * 256 + (i & 1) * 128);
-            float s[128];
-            tmem_ld128_wait(sbase, s);          // the whole row in one load
-            fence_before_sync();
-            mbar_arrive(s_empty + b);
-            const float4* ls = reinterpret_cast<const float4*>(lse_s + (qb % kChunk));
-            float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
-            if (WEIGHTED) {
-                const float4* rs = reinterpret_cast<const float4*>(lse_s + kChunk + (qb % kChunk));
-                const float2 cc2 = make_float2(c2, c2);
-#pragma unroll
-                for (int c = 0; c < 128; c += 4) {
-                    const float4 l4 = ls[c / 4], r4 = rs[c / 4];     // -lse2 and r of four queries
-                    const float2 x01 = ffma2(make_float2(s[c], s[c + 1]), cc2, make_float2(l4.x, l4.y));
-                    const float2 x23 = ffma2(make_float2(s[c + 2], s[c + 3]), cc2, make_float2(l4.z, l4.w));
-                    a01 = ffma2(make_float2(ex2(x01.x), ex2(x01.y)), make_float2(r4.x, r4.y), a01);
-                    a23 = ffma2(make_float2(ex2(x23.x), ex2(x23.y)), make_float2(r4.z, r4.w), a23);
+#pragma unroll 1
+            for (int part = 0; part < 2; ++part) {
+                const int col = half * 128 + part * 64;          // query column within the block
+                float s[64];
+                tmem_ld64_wait(tmem + lane_off + (uint32_t)(g * QB + col), s);
+                if (part == 1) {
+                    fence_before_sync();
+                    mbar_arrive(s_empty + g);
                 }
-                acc += (double)((a01.x + a01.y) + (a23.x + a23.y));
-                continue;
-            }
-            const float2 cx2 = make_float2(c2x, c2x), kb = make_float2(kb2, kb2);
+                const int c0 = qb % kChunk + col;
+                const float4* ls = reinterpret_cast<const float4*>(lse_s + c0);
+                float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
+                if (WEIGHTED) {
+                    const float4* rs = reinterpret_cast<const float4*>(lse_s + kChunk + c0);
+                    const float2 cc2 = make_float2(c2, c2);
 #pragma unroll
-            for (int c = 0; c < 128; c += 4) {
-                const float4 l4 = ls[c / 4];    // -2 lse2 of four queries
-                float2 n01 = make_float2(l4.x, l4.y), n23 = make_float2(l4.z, l4.w);
-                if (BIAS) {
-                    n01 = fadd2(n01, kb);
-                    n23 = fadd2(n23, kb);
+                    for (int c = 0; c < 64; c += 4) {
+                        const float4 l4 = ls[c / 4], r4 = rs[c / 4];     // -lse2 and r of four queries
+                        const float2 x01 = ffma2(make_float2(s[c], s[c + 1]), cc2, make_float2(l4.x, l4.y));
+                        const float2 x23 = ffma2(make_float2(s[c + 2], s[c + 3]), cc2, make_float2(l4.z, l4.w));
+                        a01 = ffma2(make_float2(ex2(x01.x), ex2(x01.y)), make_float2(r4.x, r4.y), a01);
+                        a23 = ffma2(make_float2(ex2(x23.x), ex2(x23.y)), make_float2(r4.z, r4.w), a23);
+                    }
+                } else {
+                    const float2 cx2 = make_float2(c2x, c2x), kb = make_float2(kb2, kb2);
+#pragma unroll
+                    for (int c = 0; c < 64; c += 4) {
+                        const float4 l4 = ls[c / 4];    // -2 lse2 of four queries
+                        float2 n01 = make_float2(l4.x, l4.y), n23 = make_float2(l4.z, l4.w);
+                        if (BIAS) {
+                            n01 = fadd2(n01, kb);
+                            n23 = fadd2(n23, kb);
+                        }
+                        const float2 x01 = ffma2(make_float2(s[c], s[c + 1]), cx2, n01);
+                        const float2 x23 = ffma2(make_float2(s[c + 2], s[c + 3]), cx2, n23);
+                        a01 = fadd2(a01, make_float2(ex2(x01.x), ex2(x01.y)));
+                        a23 = fadd2(a23, make_float2(ex2(x23.x), ex2(x23.y)));
+                    }
                 }
-                const float2 x01 = ffma2(make_float2(s[c], s[c + 1]), cx2, n01);
-                const float2 x23 = ffma2(make_float2(s[c + 2], s[c + 3]), cx2, n23);
-                a01 = fadd2(a01, make_float2(ex2(x01.x), ex2(x01.y)));
-                a23 = fadd2(a23, make_float2(ex2(x23.x), ex2(x23.y)));
+                df_add(acc, (a01.x + a01.y) + (a23.x + a23.y));
             }
-            acc += (double)((a01.x + a01.y) + (a23.x + a23.y));
         }
-        const int key = k0 + g * TB + row;
-        if (ok && key < T) score[(int64_t)h * T + key] = WEIGHTED ? (float)acc : (float)sqrt(acc / (double)n);
+        // the second half's sum joins the first's (a fixed order)
+        float2* red = reinterpret_cast<float2*>(sm + L::kRed);
+        if (half == 1) red[g * 128 + row] = ok ? make_float2(acc.hi, acc.lo) : make_float2(NAN, 0.f);
+        asm volatile("bar.sync 1, 512;" ::: "memory");
+        if (half == 0) {
+            const float2 o = red[g * 128 + row];
+            df_add_df(acc, dfloat{o.x, o.y});
+            const double tot = (double)acc.hi + (double)acc.lo;
+            const int key = k0 + g * TB + row;
+            if (ok && key < T) score[(int64_t)h * T + key] = WEIGHTED ? (float)tot : (float)sqrt(tot / (double)n);
+        }
     }
     if (threadIdx.x == 0 && *abort_flag) set_status(status, h, KVC_ERR_TIMEOUT);
     fence_before_sync();
@@ -623,7 +653,7 @@ __device__ __forceinline__ void colsum_step(float (&v)[32], int lane) {
 // lo * lo products (~2^-18 of each square, always the same sign) and would
 // shift mu, and so the solution of the refinement, by ~1e-5.
 template <int D>
-__global__ void __launch_bounds__(kMassThreads, 1)
+__global__ void __launch_bounds__(kMassThreads, 3)
     k_masslogits_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mC,
                     const __grid_constant__ CUtensorMap mL2, const __grid_constant__ CUtensorMap mAh,
                     const __grid_constant__ CUtensorMap mAl, const float* __restrict__ lse2,
@@ -810,8 +840,9 @@ cudaError_t launch_col_t(const void* Q, const void* K, const float* lse2, int H,
                          float* score, int32_t* status, int qdiv, long long wait_limit, const float* bias2,
                          cudaStream_t st, const float* rw = nullptr, int64_t rstride = 0) {
     CUtensorMap mK, mQ;
-    if (!make_map(&mK, K, D, T, H) || !make_map(&mQ, Q, D, n, H / qdiv)) return cudaErrorInvalidValue;
+    if (!make_map(&mK, K, D, T, H) || !make_map_rows256(&mQ, Q, D, n, H / qdiv)) return cudaErrorInvalidValue;
     constexpr int smem = ColLayout<D, NS>::kBytes;
+    static_assert(smem <= 227 * 1024, "key-score shared memory");
     auto kern = k_colscore_tc<D, NS, BIAS, WEIGHTED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -881,13 +912,13 @@ cudaError_t launch_colscore_tc(int d, const void* Q, const void* K, const float*
                                float c2, float* score, int32_t* status, int qdiv, long long wait_limit,
                                const float* bias2, cudaStream_t st) {
     if (bias2)
-        return d == 128 ? launch_col_t<128, 3, true>(Q, K, lse2, H, n, T, c2, score, status, qdiv, wait_limit, bias2,
+        return d == 128 ? launch_col_t<128, 2, true>(Q, K, lse2, H, n, T, c2, score, status, qdiv, wait_limit, bias2,
                                                      st)
-                        : launch_col_t<64, 6, true>(Q, K, lse2, H, n, T, c2, score, status, qdiv, wait_limit, bias2,
+                        : launch_col_t<64, 4, true>(Q, K, lse2, H, n, T, c2, score, status, qdiv, wait_limit, bias2,
                                                     st);
-    return d == 128 ? launch_col_t<128, 3, false>(Q, K, lse2, H, n, T, c2, score, status, qdiv, wait_limit, nullptr,
+    return d == 128 ? launch_col_t<128, 2, false>(Q, K, lse2, H, n, T, c2, score, status, qdiv, wait_limit, nullptr,
                                                   st)
-                    : launch_col_t<64, 6, false>(Q, K, lse2, H, n, T, c2, score, status, qdiv, wait_limit, nullptr,
+                    : launch_col_t<64, 4, false>(Q, K, lse2, H, n, T, c2, score, status, qdiv, wait_limit, nullptr,
                                                  st);
 }
 
@@ -897,9 +928,9 @@ cudaError_t launch_colscore_tc(int d, const void* Q, const void* K, const float*
 cudaError_t launch_corr_tc(int d, const void* Q, const void* K, const float* lse2, int H, int n, int T, float c2,
                            const float* r, int64_t rstride, float* out, int32_t* status, long long wait_limit,
                            cudaStream_t st) {
-    return d == 128 ? launch_col_t<128, 3, false, true>(Q, K, lse2, H, n, T, c2, out, status, 1, wait_limit, nullptr,
+    return d == 128 ? launch_col_t<128, 2, false, true>(Q, K, lse2, H, n, T, c2, out, status, 1, wait_limit, nullptr,
                                                         st, r, rstride)
-                    : launch_col_t<64, 6, false, true>(Q, K, lse2, H, n, T, c2, out, status, 1, wait_limit, nullptr,
+                    : launch_col_t<64, 4, false, true>(Q, K, lse2, H, n, T, c2, out, status, 1, wait_limit, nullptr,
                                                        st, r, rstride);
 }
 

@@ -18,10 +18,16 @@
 // queries keeps close to fp32 accuracy.  (Both operands are MN-major: the
 // queries are the contraction and the outer dimension of the stored arrays.)
 //
-// One CTA per 128 x 128 output tile (x head).  Warp roles:
+// One CTA per output tile (x head).  The symmetric products pair the lower
+// 128 x 128 blocks of a block row: a CTA computes blocks (I, J) and (I, J + 1)
+// as one M = 128, N = 256 product (an N = 256 product runs the tensor pipe
+// about 1.4 times faster per flop on this part than two of N = 128, and
+// reads A_I once); a row with an odd block count ends in a single N = 128
+// tile.  The rectangular product has one 128 x NB tile per row block.
+// Warp roles:
 //   warp 0       TMA producer: [64 queries][64 columns] bf16 boxes with
-//                128-byte swizzle (the MN-major operand layout), 8 per stage
-//   warp 1       MMA issuer; owns the TMEM accumulator (128 columns)
+//                128-byte swizzle (the MN-major operand layout)
+//   warp 1       MMA issuer; owns the TMEM accumulator (256 columns)
 //   warps 2..5   epilogue (TMEM -> global)
 #include "tc.cuh"
 
@@ -33,8 +39,12 @@ namespace {
 constexpr int GB = 128;                 // output tile
 constexpr int GK = 64;                  // queries per pipeline stage
 constexpr int kGBox = GK * 128;         // one [64 queries][64 columns] bf16 box: 8 KB
-constexpr int kStages = 3;
 constexpr int kGThreads = 192;
+
+// Pipeline stages: a symmetric stage holds A_I and up to 256 columns of B
+// (96 KB), a rectangular one A_I and NB columns of B (64 KB at most).
+template <bool SYM>
+__host__ __device__ constexpr int gram_stages() { return SYM ? 2 : 3; }
 
 __device__ __forceinline__ uint8_t* align1024g(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -45,12 +55,20 @@ __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
     (void)mbar_wait(bar, parity, &never);
 }
 
-__device__ __forceinline__ void tri_tile(int p, int& I, int& J) {
-    int i = (int)((sqrtf(8.f * (float)p + 1.f) - 1.f) * 0.5f);
-    while (i * (i + 1) / 2 > p) --i;
-    while ((i + 1) * (i + 2) / 2 <= p) ++i;
+// Paired lower tiles: block row I holds I / 2 + 1 tiles, so the rows before
+// I hold m (m + 1) tiles for I = 2m and (m + 1)^2 for I = 2m + 1.  Tile p ->
+// block row I, first block column J, width 1 or 2 blocks.
+__host__ __device__ inline int paired_before(int I) {
+    const int m = I / 2;
+    return (I & 1) ? (m + 1) * (m + 1) : m * (m + 1);
+}
+__device__ __forceinline__ void paired_tile(int p, int& I, int& J, int& width) {
+    int i = max(0, 2 * (int)sqrtf((float)p) - 2);    // paired_before(i) <= p for this start
+    while (i > 0 && paired_before(i) > p) --i;
+    while (paired_before(i + 1) <= p) ++i;
     I = i;
-    J = p - i * (i + 1) / 2;
+    J = 2 * (p - paired_before(i));
+    width = (J + 1 <= I) ? 2 : 1;
 }
 
 struct GramArgs {
@@ -63,10 +81,11 @@ struct GramArgs {
     long long wait_limit;        // bounded-wait limit, SM clock cycles
 };
 
-// grid (tiles, H), block 192.  SYM: lower tiles of the t x t product of A
-// with itself (B maps = A maps), written to C[h] with leading dimension ldc
-// and mirrored into the upper triangle.  RECT: tiles (I, 0) of A^T B with B
-// [n][nb], written to C[off + i][j].  Maps: bf16 hi / lo arrays.
+// grid (tiles, H), block 192.  SYM: the paired lower tiles of the t x t
+// product of A with itself (B maps = A maps), written to C[h] with leading
+// dimension ldc and mirrored into the upper triangle (NB = 256, the widest
+// tile).  RECT: tiles (I, 0) of A^T B with B [n][nb], written to C[off +
+// i][j].  Maps: bf16 hi / lo arrays.
 template <bool SYM, int NB>
 __global__ void __launch_bounds__(kGThreads, 1)
     k_gram_tc(const __grid_constant__ CUtensorMap mAh, const __grid_constant__ CUtensorMap mAl,
@@ -76,13 +95,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (!head_ok(g.status, h)) return;
     const int off = g.offsets[h];
     const int t = g.offsets[h + 1] - off;
-    int I, J;
-    if (SYM) tri_tile(blockIdx.x, I, J);
+    int I, J, width = 1;
+    if (SYM) paired_tile(blockIdx.x, I, J, width);
     else {
         I = blockIdx.x;
         J = 0;
     }
     if (I * GB >= t) return;
+    constexpr int kStages = gram_stages<SYM>();
+    const int nbw = SYM ? width * GB : NB;        // this tile's B columns (the MMA's N)
     constexpr int kA = 2 * kGBox;                 // one 128-column operand term
     constexpr int kB = (NB / 64) * kGBox;
     constexpr int kAH = 0, kAL = kA, kBH = 2 * kA, kBL = 2 * kA + kB;
@@ -105,7 +126,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(tmem_slot, 128);
+    if (warp == 1) tmem_alloc(tmem_slot, 256);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -123,12 +144,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 const int s = k % kStages;
                 if (k >= kStages && !mbar_wait(empty + s, (uint32_t)((k / kStages) - 1) & 1u, abort_flag, wait_limit)) break;
                 uint8_t* st = sm + s * kStage;
-                mbar_expect_tx(full + s, (uint32_t)kStage);
+                mbar_expect_tx(full + s, (uint32_t)(2 * kA + 2 * (nbw / 64) * kGBox));
                 for (int b = 0; b < 2; ++b) {
                     tma_load_3d(st + kAH + b * kGBox, &mAh, full + s, I * GB + 64 * b, k * GK, h);
                     tma_load_3d(st + kAL + b * kGBox, &mAl, full + s, I * GB + 64 * b, k * GK, h);
                 }
-                for (int b = 0; b < NB / 64; ++b) {
+                for (int b = 0; b < nbw / 64; ++b) {
                     tma_load_3d(st + kBH + b * kGBox, &mBh, full + s, J * GB + 64 * b, k * GK, h);
                     tma_load_3d(st + kBL + b * kGBox, &mBl, full + s, J * GB + 64 * b, k * GK, h);
                 }
@@ -140,7 +161,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(128, NB, true, true);
+            const uint32_t idesc = idesc_bf16(128, nbw, true, true);
             for (int k = 0; k < nk; ++k) {
                 const int s = k % kStages;
                 if (!mbar_wait(full + s, (uint32_t)(k / kStages) & 1u, abort_flag, wait_limit)) break;
@@ -174,10 +195,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
             const int i = I * GB + row;
             const int jmax = SYM ? t : g.nb;
 #pragma unroll 1
-            for (int c = 0; c < NB / 32; ++c) {
+            for (int c = 0; c < nbw / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_off + c * 32, r);
                 tmem_ld_wait();
+                const int jb = J + c / 4;             // block column of these 32 (SYM)
                 if (i < t) {
                     float* dst = SYM ? g.C + ((int64_t)h * g.ldc + i) * g.ldc + J * GB + c * 32
                                      : g.C + ((int64_t)off + i) * g.ldc + c * 32;
@@ -193,7 +215,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                         for (int q = 0; q < 32; ++q)
                             if (j0 + q < jmax) dst[q] = __uint_as_float(r[q]);
                     }
-                    if (SYM && I != J) {
+                    if (SYM && I != jb) {
                         // mirror into the upper triangle (the sweep inverse reads
                         // both); for a fixed column a warp writes 32 consecutive rows
                         float* dT = g.C + ((int64_t)h * g.ldc + j0) * g.ldc + i;
@@ -209,12 +231,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    if (warp == 1) tmem_dealloc(tmem, 128);
+    if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
-template <int NB>
+template <bool SYM, int NB>
 constexpr int gram_smem() {
-    return kStages * (4 * kGBox + 2 * (NB / 64) * kGBox) + 256 + 1024;
+    return gram_stages<SYM>() * (4 * kGBox + 2 * (NB / 64) * kGBox) + 256 + 1024;
 }
 
 // fp32 [H][rows][ld] (first `cols` columns) -> bf16 hi / lo arrays of the same
@@ -485,12 +507,13 @@ cudaError_t launch_gram_sym_tc(const void* Ah, const void* Al, const int32_t* of
     CUtensorMap mh, ml;
     if (!make_map_bf16(&mh, Ah, (int)ld, ld, n, H) || !make_map_bf16(&ml, Al, (int)ld, ld, n, H))
         return cudaErrorInvalidValue;
-    constexpr int smem = gram_smem<128>();
-    cudaError_t e = cudaFuncSetAttribute(k_gram_tc<true, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    constexpr int smem = gram_smem<true, 256>();
+    static_assert(smem <= 227 * 1024, "Gram shared memory");
+    cudaError_t e = cudaFuncSetAttribute(k_gram_tc<true, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int nt = (max_t + GB - 1) / GB;
     GramArgs g{C, offsets, ldc, n, 0, status, wait_limit};
-    k_gram_tc<true, 128><<<dim3(nt * (nt + 1) / 2, H), kGThreads, smem, st>>>(mh, ml, mh, ml, g);
+    k_gram_tc<true, 256><<<dim3(paired_before(nt), H), kGThreads, smem, st>>>(mh, ml, mh, ml, g);
     return cudaGetLastError();
 }
 
@@ -505,12 +528,12 @@ cudaError_t launch_gram_rect_tc(int d, const void* Ah, const void* Al, const voi
     GramArgs g{C, offsets, d, n, d, status, wait_limit};
     dim3 grid((max_t + GB - 1) / GB, H);
     if (d == 128) {
-        constexpr int smem = gram_smem<128>();
+        constexpr int smem = gram_smem<false, 128>();
         cudaError_t e = cudaFuncSetAttribute(k_gram_tc<false, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         k_gram_tc<false, 128><<<grid, kGThreads, smem, st>>>(mah, mal, mbh, mbl, g);
     } else {
-        constexpr int smem = gram_smem<64>();
+        constexpr int smem = gram_smem<false, 64>();
         cudaError_t e = cudaFuncSetAttribute(k_gram_tc<false, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         k_gram_tc<false, 64><<<grid, kGThreads, smem, st>>>(mah, mal, mbh, mbl, g);

@@ -46,6 +46,12 @@ bool make_map(CUtensorMap* m, const void* base, int d, int rows, int H) {
     return encode3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, d, d, rows, H, 64, 128);
 }
 
+// The same with boxes of [256 rows][64 elements]: the 256-query operand
+// blocks of the key-score pass.
+bool make_map_rows256(CUtensorMap* m, const void* base, int d, int rows, int H) {
+    return encode3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, d, d, rows, H, 64, 256);
+}
+
 // [H][rows][ld] fp32 (first `cols` columns addressed) as a 3-D tensor: boxes
 // of [32 rows][32 columns] (128 bytes) with 128-byte swizzle; reads past the
 // addressed columns or rows return 0.
