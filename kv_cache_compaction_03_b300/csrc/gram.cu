@@ -6,7 +6,7 @@
 //   k_xsoftmax     X_qi = softmax_i(l2_qi + log2 w_i), as bf16 hi / lo terms
 // Matrices are per head, row-major with leading dimension ldA (a multiple
 // of 64); only the lower triangle of G / M is read.
-#include "common.cuh"
+#include "tc.cuh"
 
 namespace kvc {
 
@@ -108,18 +108,14 @@ __global__ void k_ridge_m_diag(float* __restrict__ M, const int32_t* __restrict_
 // X_qi = softmax_i(l2_qi + log2 w_i) over i < t, written as bf16 hi / lo
 // terms (the Gram operand format, see gram_tc.cu); padding columns up to the
 // next multiple of 64 are 0.  log2 w_i from the fitted weights (-inf where
-// w = 0).  grid (ceil(n/32), H), block 256: a warp per row, four rows
-// per warp; the CTA's 32 rows share one staged copy of log2 w.  Each lane
-// takes four adjacent columns per step (one 16-byte load, two 8-byte
-// stores): a first pass keeps a running maximum and the sum rescaled to it,
-// a second pass writes the normalised terms.
-__device__ __forceinline__ void online_add(float& m, float& s, float v0, float v1, float v2, float v3) {
-    const float mn = fmaxf(fmaxf(m, fmaxf(v0, v1)), fmaxf(v2, v3));
-    if (mn == -INFINITY) return;                     // nothing finite seen yet
-    s = s * exp2f(m - mn) + ((exp2f(v0 - mn) + exp2f(v1 - mn)) + (exp2f(v2 - mn) + exp2f(v3 - mn)));
-    m = mn;
-}
-
+// w = 0; the log-masses hold -inf past t as well).  grid (ceil(n/32), H),
+// block 256: a warp per row, four rows per warp; the CTA's 32 rows share one
+// staged copy of log2 w.  Each lane takes four adjacent columns per step
+// (one 16-byte load, two 8-byte stores) in three passes over the row (the
+// second and third read it from L1): the maximum, the sum of 2^(v - max),
+// and the normalised terms.  The exponentials are the special-function
+// unit's (ex2.approx, relative error ~2^-22), well inside the 2^-17 of the
+// hi / lo split they feed.
 __global__ void __launch_bounds__(256) k_xsoftmax(const float* __restrict__ L2, const float* __restrict__ wfit,
                                                   const int32_t* __restrict__ offsets, int n, int64_t ldA,
                                                   __nv_bfloat16* __restrict__ Xh, __nv_bfloat16* __restrict__ Xl,
@@ -144,34 +140,40 @@ __global__ void __launch_bounds__(256) k_xsoftmax(const float* __restrict__ L2, 
         if (q >= n) break;
         const int64_t ro = ((int64_t)h * n + q) * ldA;
         const float4* row = reinterpret_cast<const float4*>(L2 + ro);
-        float m = -INFINITY, s = 0.f;
-        for (int i = 4 * lane; i < t; i += 128) {
+        float m = -INFINITY;
+        for (int i = 4 * lane; i < tp; i += 128) {
             const float4 a = row[i >> 2], w = lw4[i >> 2];
-            // columns past t carry log2 w = -inf
-            online_add(m, s, a.x + w.x, i + 1 < t ? a.y + w.y : -INFINITY, i + 2 < t ? a.z + w.z : -INFINITY,
-                       i + 3 < t ? a.w + w.w : -INFINITY);
+            m = tc::fmax3(m, tc::fmax3(a.x + w.x, a.y + w.y, a.z + w.z), a.w + w.w);
         }
         const float mx = warp_max(m);
-        s = (m == -INFINITY) ? 0.f : s * exp2f(m - mx);
-        s = warp_sum(s);
-        const float inv = (s > 0.f && mx > -INFINITY) ? 1.f / s : 0.f;
+        const float nmx = mx > -INFINITY ? -mx : 0.f;
+        const float2 nm2 = make_float2(nmx, nmx);
+        float2 s2 = make_float2(0.f, 0.f);
         for (int i = 4 * lane; i < tp; i += 128) {
-            float x[4] = {0.f, 0.f, 0.f, 0.f};
-            if (inv > 0.f && i < t) {
-                const float4 a = row[i >> 2], w = lw4[i >> 2];
-                const float v[4] = {a.x + w.x, a.y + w.y, a.z + w.z, a.w + w.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (i + j < t) x[j] = exp2f(v[j] - mx) * inv;
-            }
-            __align__(8) __nv_bfloat16 hv[4], lv[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                hv[j] = __float2bfloat16_rn(x[j]);
-                lv[j] = __float2bfloat16_rn(x[j] - __bfloat162float(hv[j]));
-            }
-            *reinterpret_cast<uint2*>(Xh + ro + i) = *reinterpret_cast<const uint2*>(hv);
-            *reinterpret_cast<uint2*>(Xl + ro + i) = *reinterpret_cast<const uint2*>(lv);
+            const float4 a = row[i >> 2], w = lw4[i >> 2];
+            const float2 v01 = tc::fadd2(tc::fadd2(make_float2(a.x, a.y), make_float2(w.x, w.y)), nm2);
+            const float2 v23 = tc::fadd2(tc::fadd2(make_float2(a.z, a.w), make_float2(w.z, w.w)), nm2);
+            const float2 e01 = make_float2(tc::ex2(v01.x), tc::ex2(v01.y));
+            const float2 e23 = make_float2(tc::ex2(v23.x), tc::ex2(v23.y));
+            s2 = tc::fadd2(s2, tc::fadd2(e01, e23));
+        }
+        const float s = warp_sum(s2.x + s2.y);
+        const float inv = (s > 0.f && mx > -INFINITY) ? 1.f / s : 0.f;
+        const float2 inv2 = make_float2(inv, inv);
+        for (int i = 4 * lane; i < tp; i += 128) {
+            const float4 a = row[i >> 2], w = lw4[i >> 2];
+            const float2 v01 = tc::fadd2(tc::fadd2(make_float2(a.x, a.y), make_float2(w.x, w.y)), nm2);
+            const float2 v23 = tc::fadd2(tc::fadd2(make_float2(a.z, a.w), make_float2(w.z, w.w)), nm2);
+            float2 x01 = make_float2(tc::ex2(v01.x), tc::ex2(v01.y));
+            float2 x23 = make_float2(tc::ex2(v23.x), tc::ex2(v23.y));
+            x01.x *= inv2.x; x01.y *= inv2.y; x23.x *= inv2.x; x23.y *= inv2.y;
+            uint2 hv, lv;
+            hv.x = tc::pack_bf16(x01.x, x01.y);
+            hv.y = tc::pack_bf16(x23.x, x23.y);
+            lv.x = tc::pack_bf16(x01.x - tc::bf16_lo(hv.x), x01.y - tc::bf16_hi(hv.x));
+            lv.y = tc::pack_bf16(x23.x - tc::bf16_lo(hv.y), x23.y - tc::bf16_hi(hv.y));
+            *reinterpret_cast<uint2*>(Xh + ro + i) = hv;
+            *reinterpret_cast<uint2*>(Xl + ro + i) = lv;
         }
     }
 }

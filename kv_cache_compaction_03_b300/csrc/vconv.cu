@@ -4,9 +4,11 @@
 // Values: P enters P V as one fp16 term (11 significant bits; a single bf16
 // term would leave O ~1e-3 off), and a tcgen05 product takes both operands
 // in the same type, so V is rewritten in fp16 once per call:
-// V16 = fp16(V * 2^-e_h), with e_h >= 0 the smallest power of two that
-// brings max |V| of head h below 2^15 (the fp16 range ends at 65504).  The
-// scaling is exact; the attention epilogue multiplies O by 2^e_h again.  V
+// V16 = fp16(V * 2^-e_h).  e_h = 0 when 2^-3 <= max |V| < 2^15 for head h:
+// the fp16 range ends at 65504, and every value down to max |V| 2^-11 is a
+// normal fp16 number with its full 11 bits.  Outside that band e_h brings
+// max |V| into [2^14, 2^15).  The scaling is exact; the attention epilogue
+// multiplies O by 2^e_h again.  V
 // is bf16 (a fresh cache) or fp32 (the refitted values of a compacted
 // cache).  A head whose values hold a NaN or an infinity gets
 // KVC_ERR_NONFINITE.
@@ -41,15 +43,19 @@ __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-// Per-head max |V| as the bits of a non-negative float (those order like
-// unsigned integers); +inf marks a non-finite value.  vmax must be zeroed.
+// V16 = fp16(V) for every head, and the per-head max |V| as the bits of a
+// non-negative float (those order like unsigned integers; +inf marks a
+// non-finite value) into vmax, which must be zeroed.  One pass with the
+// scale 1 (e_h = 0, the common case); k_v_fixup rewrites the heads whose
+// max |V| falls outside [2^-3, 2^15).
 // grid (ceil(per_head / kGroup), H), block 256.
 template <typename TIn>
-__global__ void __launch_bounds__(256) k_vabsmax(const TIn* __restrict__ V, int64_t per_head,
-                                                 uint32_t* __restrict__ vmax, const int32_t* __restrict__ status) {
+__global__ void __launch_bounds__(256) k_v_to_f16(const TIn* __restrict__ V, int64_t per_head, uint32_t* __restrict__ vmax,
+                                                  __half* __restrict__ V16, const int32_t* __restrict__ status) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     const TIn* Vh = V + (int64_t)h * per_head;
+    __half* Oh = V16 + (int64_t)h * per_head;
     float m = 0.f;
     bool bad = false;
     const int64_t base = (int64_t)blockIdx.x * kGroup;
@@ -59,6 +65,10 @@ __global__ void __launch_bounds__(256) k_vabsmax(const TIn* __restrict__ V, int6
         if (e < per_head) {
             float v[8];
             load8(Vh + e, v);
+            __half2 o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) o[q] = __floats2half2_rn(v[2 * q], v[2 * q + 1]);
+            *reinterpret_cast<uint4*>(Oh + e) = *reinterpret_cast<const uint4*>(o);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const float a = fabsf(v[q]);
@@ -79,11 +89,12 @@ __global__ void __launch_bounds__(256) k_vabsmax(const TIn* __restrict__ V, int6
     }
 }
 
-// V16 = fp16(V * 2^-e_h); e_h to vexp[h].  Same grid as k_vabsmax.
+// e_h to vexp[h]; heads with e_h != 0 are converted again as fp16(V 2^-e_h);
+// a non-finite value gives KVC_ERR_NONFINITE.  Same grid as k_v_to_f16.
 template <typename TIn>
-__global__ void __launch_bounds__(256) k_v_to_f16(const TIn* __restrict__ V, int64_t per_head,
-                                                  const uint32_t* __restrict__ vmax, __half* __restrict__ V16,
-                                                  int32_t* __restrict__ vexp, int32_t* __restrict__ status) {
+__global__ void __launch_bounds__(256) k_v_fixup(const TIn* __restrict__ V, int64_t per_head,
+                                                 const uint32_t* __restrict__ vmax, __half* __restrict__ V16,
+                                                 int32_t* __restrict__ vexp, int32_t* __restrict__ status) {
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     const float mx = __uint_as_float(vmax[h]);
@@ -92,10 +103,13 @@ __global__ void __launch_bounds__(256) k_v_to_f16(const TIn* __restrict__ V, int
         return;
     }
     int E2 = 0;
-    (void)frexpf(mx, &E2);                   // mx < 2^E2
-    const int e = max(0, E2 - 15);           // mx * 2^-e < 2^15
+    (void)frexpf(mx, &E2);                   // 2^(E2-1) <= mx < 2^E2 (E2 = 0 for mx = 0)
+    // e = 0 for mx in [2^-3, 2^15), else mx 2^-e in [2^14, 2^15); the
+    // clamp keeps 2^-e and 2^e normal fp32 numbers
+    const int e = (E2 >= -2 && E2 <= 15) ? 0 : min(113, max(-100, E2 - 15));
     if (blockIdx.x == 0 && threadIdx.x == 0) vexp[h] = e;
-    const float sc = __uint_as_float((uint32_t)(127 - e) << 23);      // 2^-e, e <= 113
+    if (e == 0) return;
+    const float sc = __uint_as_float((uint32_t)(127 - e) << 23);      // 2^-e
     const TIn* Vh = V + (int64_t)h * per_head;
     __half* Oh = V16 + (int64_t)h * per_head;
     const int64_t base = (int64_t)blockIdx.x * kGroup;
@@ -133,8 +147,8 @@ cudaError_t launch_v_to_f16_t(const void* V, int H, int64_t per_head, uint32_t* 
     cudaError_t e = cudaMemsetAsync(vmax, 0, sizeof(uint32_t) * H, st);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((per_head + kGroup - 1) / kGroup), H);
-    k_vabsmax<TIn><<<grid, 256, 0, st>>>((const TIn*)V, per_head, vmax, status);
-    k_v_to_f16<TIn><<<grid, 256, 0, st>>>((const TIn*)V, per_head, vmax, (__half*)V16, vexp, status);
+    k_v_to_f16<TIn><<<grid, 256, 0, st>>>((const TIn*)V, per_head, vmax, (__half*)V16, status);
+    k_v_fixup<TIn><<<grid, 256, 0, st>>>((const TIn*)V, per_head, vmax, (__half*)V16, vexp, status);
     return cudaGetLastError();
 }
 

@@ -170,6 +170,28 @@ def test_nonfinite_input_flagged():
     assert st[0] == 0 and st[1] == kvc.ERR_NONFINITE
 
 
+def test_values_beyond_fp16_range():
+    """V of one head scaled by 2^20 (max |V| ~ 5e6, past the fp16 range of
+    the attention's P V operand) and of another by 2^-20 (max |V| ~ 5e-6,
+    fp16 subnormals): the pass rewrites both heads' values under a power-of-
+    two scale, and both match the oracle like an unscaled head."""
+    from oracle import decode
+    from workloads.batch import generate
+    from workloads.gen import round_to_bf16_bits
+    w = small_variant(WORKLOADS[2], H=3, n=320, T=1000, t=100)
+    x = generate(w, workers=1)
+    for h, f in ((1, 2.0 ** 20), (2, 2.0 ** -20)):
+        x["V"][h] = round_to_bf16_bits(decode(x["V"][h], w.dtype) * f)
+    g, inputs = run_gpu(w, inputs=x)
+    assert np.all(g["status"] == 0), g["status"]
+    buds = budgets(w)
+    for h in range(w.H):
+        r, Ohat = run_oracle_head(w, inputs, h, int(buds[h]))
+        o_rel = np.linalg.norm(g["O"][h] - r.O) / np.linalg.norm(r.O)
+        assert o_rel <= 2e-4, (h, o_rel)
+        compare_head(g, h, r, Ohat, {"head": h}, Q=head_queries(w, inputs, h))
+
+
 @pytest.mark.parametrize("cfg,sample", [(2, None), (5, [0, 37, 77, 127]), (4, [0, 55, 111]), (3, [0, 131, 255])])
 def test_full_config_sampled_heads(cfg, sample):
     w = WORKLOADS[cfg]
