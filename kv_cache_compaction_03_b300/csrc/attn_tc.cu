@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
     k_colscore_tc(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
                   const float* __restrict__ lse2, int n, int T, float c2, float* __restrict__ score,
                   int32_t* __restrict__ status, int qdiv, long long wait_limit, const float* __restrict__ bias2,
-                  int Tb, const float* __restrict__ rw, int64_t rstride) {
+                  int Tb, const float* __restrict__ rw, int64_t rstride, float2* __restrict__ part) {
     // WEIGHTED: the shared log-mass chunk holds half the queries, followed by
     // their weights r_q
     constexpr int kChunk = WEIGHTED ? kLseChunk / 2 : kLseChunk;
@@ -441,7 +441,12 @@ __global__ void __launch_bounds__(kColThreads, 1)
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const int nq = (n + QB - 1) / QB;
+    // this CTA's query blocks: the gridDim.z parts of the n queries
+    // (WEIGHTED only; the key scores take all queries in one CTA)
+    const int nq_all = (n + QB - 1) / QB;
+    const int per = WEIGHTED ? (nq_all + (int)gridDim.z - 1) / (int)gridDim.z : nq_all;
+    const int ib = WEIGHTED ? min(nq_all, (int)blockIdx.z * per) : 0;
+    const int nq = min(nq_all, ib + per) - ib;
     const int k0 = blockIdx.x * 2 * TB;
 
     if (warp == 0) {
@@ -458,7 +463,8 @@ __global__ void __launch_bounds__(kColThreads, 1)
                 if (i >= NS && !mbar_wait(q_empty + s, (uint32_t)((i / NS) - 1) & 1u, abort_flag, wait_limit)) break;
                 mbar_expect_tx(q_full + s, (uint32_t)L::kTileQ);
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_3d(sm + L::kQ + s * L::kTileQ + c * L::kBoxQ, &mQ, q_full + s, c * 64, i * QB, h / qdiv);
+                    tma_load_3d(sm + L::kQ + s * L::kTileQ + c * L::kBoxQ, &mQ, q_full + s, c * 64, (ib + i) * QB,
+                                h / qdiv);
                 issued = i + 1;
             }
             drain_wait(k_full, 0);
@@ -516,9 +522,11 @@ __global__ void __launch_bounds__(kColThreads, 1)
         // Every consumer warp runs all blocks (after an abort it only skips
         // the work) so that the named barriers around the log-mass reload
         // and the final combine are always reached by all sixteen.
+        int cbase = 0;                              // first query of the log-mass chunk in shared memory
         for (int i = 0; i < nq; ++i) {
-            const int qb = i * QB;
-            if (qb % kChunk == 0) {
+            const int qb = (ib + i) * QB;
+            if (WEIGHTED ? (i == 0 || qb - cbase >= kChunk) : (qb % kChunk == 0)) {
+                cbase = qb;
                 // the next chunk's log-masses, negated (doubled for P^2); -inf
                 // past n zeroes those columns; WEIGHTED: and the weights
                 const int cnt = min(kChunk, ((n - qb + QB - 1) / QB) * QB);
@@ -542,7 +550,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
                     fence_before_sync();
                     mbar_arrive(s_empty + g);
                 }
-                const int c0 = qb % kChunk + col;
+                const int c0 = (WEIGHTED ? qb - cbase : qb % kChunk) + col;
                 const float4* ls = reinterpret_cast<const float4*>(lse_s + c0);
                 float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
                 if (WEIGHTED) {
@@ -584,7 +592,12 @@ __global__ void __launch_bounds__(kColThreads, 1)
             df_add_df(acc, dfloat{o.x, o.y});
             const double tot = (double)acc.hi + (double)acc.lo;
             const int key = k0 + g * TB + row;
-            if (ok && key < T) score[(int64_t)h * T + key] = WEIGHTED ? (float)tot : (float)sqrt(tot / (double)n);
+            if (ok && key < T) {
+                if (part)
+                    part[((int64_t)blockIdx.z * gridDim.y + h) * T + key] = make_float2(acc.hi, acc.lo);
+                else
+                    score[(int64_t)h * T + key] = WEIGHTED ? (float)tot : (float)sqrt(tot / (double)n);
+            }
         }
     }
     if (threadIdx.x == 0 && *abort_flag) set_status(status, h, KVC_ERR_TIMEOUT);
@@ -838,7 +851,8 @@ cudaError_t launch_fwd_t(const void* Q, const void* K, const void* V, int H, int
 template <int D, int NS, bool BIAS, bool WEIGHTED = false>
 cudaError_t launch_col_t(const void* Q, const void* K, const float* lse2, int H, int n, int T, float c2,
                          float* score, int32_t* status, int qdiv, long long wait_limit, const float* bias2,
-                         cudaStream_t st, const float* rw = nullptr, int64_t rstride = 0) {
+                         cudaStream_t st, const float* rw = nullptr, int64_t rstride = 0, float2* part = nullptr,
+                         int nz = 1) {
     CUtensorMap mK, mQ;
     if (!make_map(&mK, K, D, T, H) || !make_map_rows256(&mQ, Q, D, n, H / qdiv)) return cudaErrorInvalidValue;
     constexpr int smem = ColLayout<D, NS>::kBytes;
@@ -846,9 +860,9 @@ cudaError_t launch_col_t(const void* Q, const void* K, const float* lse2, int H,
     auto kern = k_colscore_tc<D, NS, BIAS, WEIGHTED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((T + 2 * TB - 1) / (2 * TB), H);
+    dim3 grid((T + 2 * TB - 1) / (2 * TB), H, nz);
     kern<<<grid, kColThreads, smem, st>>>(mK, mQ, lse2, n, T, c2, score, status, qdiv, wait_limit, bias2,
-                                          (int)round_up(T, 256), rw, rstride);
+                                          (int)round_up(T, 256), rw, rstride, part);
     return cudaGetLastError();
 }
 
@@ -922,16 +936,18 @@ cudaError_t launch_colscore_tc(int d, const void* Q, const void* K, const float*
                                                  st);
 }
 
-// out[h][j] = sum_q exp2(S_qj c2 - lse2_q) r[h][q] for every key j (bf16
-// inputs, tensor cores): the matching-pursuit correlations <p_j, r>.  r has
-// row stride rstride.
+// part[z][h][j] = the z-th of nz parts (query blocks split evenly) of
+// sum_q exp2(S_qj c2 - lse2_q) r[h][q] for every key j, as an fp32 pair
+// (hi, lo) (bf16 inputs, tensor cores): the matching-pursuit correlations
+// <p_j, r> are the parts' sum.  Splitting the queries gives small problems
+// more CTAs.  r has row stride rstride.
 cudaError_t launch_corr_tc(int d, const void* Q, const void* K, const float* lse2, int H, int n, int T, float c2,
-                           const float* r, int64_t rstride, float* out, int32_t* status, long long wait_limit,
-                           cudaStream_t st) {
-    return d == 128 ? launch_col_t<128, 2, false, true>(Q, K, lse2, H, n, T, c2, out, status, 1, wait_limit, nullptr,
-                                                        st, r, rstride)
-                    : launch_col_t<64, 4, false, true>(Q, K, lse2, H, n, T, c2, out, status, 1, wait_limit, nullptr,
-                                                       st, r, rstride);
+                           const float* r, int64_t rstride, float2* part, int nz, int32_t* status,
+                           long long wait_limit, cudaStream_t st) {
+    return d == 128 ? launch_col_t<128, 2, false, true>(Q, K, lse2, H, n, T, c2, nullptr, status, 1, wait_limit,
+                                                        nullptr, st, r, rstride, part, nz)
+                    : launch_col_t<64, 4, false, true>(Q, K, lse2, H, n, T, c2, nullptr, status, 1, wait_limit,
+                                                       nullptr, st, r, rstride, part, nz);
 }
 
 }  // namespace kvc

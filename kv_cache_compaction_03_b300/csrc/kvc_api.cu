@@ -36,7 +36,7 @@ cudaError_t launch_attend_decode(int, int, const void*, int, const void*, const 
 int attend_decode_max_queries();
 size_t omp_workspace_bytes(int dtype, int H, int n, int T, int max_t);
 size_t omp_order_offset(int dtype, int H, int n, int T, int max_t);
-int omp_launches(int dtype, int max_t);
+int omp_launches(int dtype, int max_t, int nf);
 cudaError_t launch_colmean_simt(int dtype, int d, const void* Q, const void* K, const float* lse2, int H, int n, int T,
                                 float c2, float* out, const int32_t* status, cudaStream_t st);
 int tam_max_segments();
@@ -477,7 +477,7 @@ static kvc_status enqueue_compact(const kvc_problem* p, const kvc_params& q, int
                   launch_select_seg(score, H, T, offsets, tam->bounds, tam->nseg, tam->pivots, skeep, soff, idx_out,
                                     head_status, st));
     } else if (omp)
-        KVC_STAGE("omp", omp_launches(dt, mt),
+        KVC_STAGE("omp", omp_launches(dt, mt, (int)std::min<int64_t>(T, (int64_t)q.keep_first + q.keep_last)),
                   launch_omp_select(dt, d, Q_ref, K, lse2, c2, H, n, T, mt, offsets, q.keep_first, q.keep_last,
                                     ws + L.omp, idx_out, head_status, wl, st));
     else
