@@ -122,7 +122,7 @@ def stage_work(w, buds):
     t = [int(x) for x in buds]
     st = sum(t)
     return {
-        "v_f16": ("bytes", 3.0 * 2 * T * d * H),
+        "v_f16": ("bytes", 2.0 * 2 * T * d * H),        # reads V (bf16), writes fp16 once
         "attn_fwd": ("flops", 4.0 * n * T * d * H),
         "colscore": ("flops", 2.0 * n * T * d * H),
         "select": ("bytes", 4.0 * T * H + 4.0 * st),
