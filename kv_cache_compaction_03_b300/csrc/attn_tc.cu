@@ -757,7 +757,9 @@ __global__ void __launch_bounds__(kMassThreads, 3)
                 for (int k = 0; k < 32; ++k) {
                     const float bkk = bk ? __shfl_sync(0xffffffffu, bl, k) : 0.f;
                     const float v = (ib + k < th) ? fmaf(__uint_as_float(r[k]), c2, bkk - lq) : -INFINITY;
-                    x[k] = (q < n && ib + k < th) ? exp2f(v) : 0.f;
+                    // the special-function unit's 2^v (relative error ~2^-22), far
+                    // inside the 2^-17 of the hi / lo terms it feeds
+                    x[k] = (q < n && ib + k < th) ? ex2(v) : 0.f;
                     r[k] = __float_as_uint(v);
                     sqc = fmaf(x[k], x[k], sqc);
                 }
