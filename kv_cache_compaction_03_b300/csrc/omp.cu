@@ -344,14 +344,16 @@ __global__ void __launch_bounds__(kStepThreads, 1)
         for (int w = 0; w < kStepWarps; ++w) tot += red_v[w];
         return tot;
     };
-    // sum over the cluster of one float per CTA, in rank order
+    // sum over the cluster of one float per CTA: lane c of every warp reads
+    // rank c's value (the remote loads overlap), then a fixed shuffle tree
+    // adds them, the same tree in every CTA
     auto cluster_sum = [&](float mine) {
         if (tid == 0) part_s = mine;
         cluster.sync();
-        float tot = 0.f;
-        for (int c = 0; c < CL; ++c) tot += *cluster.map_shared_rank(&part_s, c);
+        float x = lane < CL ? *cluster.map_shared_rank(&part_s, lane) : 0.f;
+        x = warp_sum(x);
         cluster.sync();                                // part_s may be rewritten after this
-        return tot;
+        return x;
     };
 
     // ---- the key
@@ -393,12 +395,19 @@ __global__ void __launch_bounds__(kStepThreads, 1)
             part_i = red_i[0];
         }
         cluster.sync();
+        // lane c reads rank c's candidate; the (largest, then lowest position)
+        // rule does not depend on the order the candidates meet in
         float gv = -INFINITY;
         int gi = INT32_MAX;
-        for (int c = 0; c < CL; ++c) {
-            const float pv = *cluster.map_shared_rank(&part_v, c);
-            const int pi = *cluster.map_shared_rank(&part_i, c);
-            if (pv > -INFINITY) better(gv, gi, pv, pi);
+        if (lane < CL) {
+            gv = *cluster.map_shared_rank(&part_v, lane);
+            gi = *cluster.map_shared_rank(&part_i, lane);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, gv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, gi, o);
+            if (ov > -INFINITY) better(gv, gi, ov, oi);
         }
         if (!(gv > -INFINITY)) {
             // no candidate with a positive norm: the lowest position not chosen
