@@ -92,6 +92,15 @@ def test_decode_ragged(dtype, d, nq):
     _check(1000 + nq, 6, nq, [1, 7, 33, 260, 1000, 4099], d, dtype)
 
 
+def test_decode_many_heads():
+    """160 heads (the four-CTA cluster taken when the heads outnumber the
+    SMs), ragged lengths including 1 and 0-to-few keys per cluster CTA."""
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(1, 700, 160)]
+    lens[3], lens[77] = 1, 3
+    _check(31, 160, 4, lens, 128, "bf16")
+
+
 def test_query_tile_path_ragged():
     """n_q = 17 and 200 take the query-tile kernel."""
     _check(7, 3, 17, [5, 300, 1100], 128, "bf16")
