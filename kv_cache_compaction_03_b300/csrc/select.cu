@@ -99,19 +99,40 @@ __device__ bool radix_select_range(KeyFn key, int lo, int hi, int keep, int32_t*
             if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
-            int cum = 0, kr = s_krem;
-            uint32_t dg = 0;
-            for (int b = 255; b >= 0; --b) {
-                if (cum + hist[b] >= kr) {
-                    dg = (uint32_t)b;
-                    kr -= cum;
-                    break;
-                }
-                cum += hist[b];
+        if (threadIdx.x < 32) {
+            // the highest digit whose keys (with all higher ones) reach s_krem:
+            // lane l sums bins 255 - 8 l .. 248 - 8 l, a warp scan finds the
+            // lane, and that lane walks its eight bins
+            const int lane = threadIdx.x;
+            const int kr = s_krem;
+            int c[8], sum = 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                c[u] = hist[255 - (lane * 8 + u)];
+                sum += c[u];
             }
-            s_digit = dg;
-            s_krem = kr;
+            int inc = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, inc >= kr);
+            const int L = hit ? __ffs(hit) - 1 : -1;
+            if (lane == L) {
+                int cum = inc - sum;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (cum + c[u] >= kr) {
+                        s_digit = (uint32_t)(255 - (lane * 8 + u));
+                        s_krem = kr - cum;
+                        break;
+                    }
+                    cum += c[u];
+                }
+            } else if (L < 0 && lane == 0) {
+                s_digit = 0;                     // unreachable for a valid budget
+            }
         }
         __syncthreads();
         prefix |= s_digit << shift;
