@@ -807,14 +807,24 @@ __global__ void __launch_bounds__(256) k_colresid_sum(const dfloat* __restrict__
                                                       const HeadScalars* __restrict__ hs, float* __restrict__ r,
                                                       const uint8_t* __restrict__ fixed,
                                                       const int32_t* __restrict__ status) {
+    // thread (g, cl): column blockIdx.x * 32 + cl, partials [g nb8, (g + 1) nb8);
+    // the eight group sums then meet in group order (a fixed order)
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
+    __shared__ dfloat gs[8][32];
     const int off = offsets[h];
     const int t = offsets[h + 1] - off;
-    const int c = blockIdx.x * 256 + threadIdx.x;
-    if (c >= t) return;
-    dfloat acc = part[off + c];
-    for (int sp = 1; sp < nblk; ++sp) df_add_df(acc, part[(int64_t)sp * part_stride + off + c]);
+    const int cl = threadIdx.x & 31, g = threadIdx.x >> 5;
+    const int c = blockIdx.x * 32 + cl;
+    const int nb8 = (nblk + 7) / 8;
+    const int s0 = min(nblk, g * nb8), s1 = min(nblk, s0 + nb8);
+    dfloat acc{0.f, 0.f};
+    if (c < t)
+        for (int sp = s0; sp < s1; ++sp) df_add_df(acc, part[(int64_t)sp * part_stride + off + c]);
+    gs[g][cl] = acc;
+    __syncthreads();
+    if (g != 0 || c >= t) return;
+    for (int k = 1; k < 8; ++k) df_add_df(acc, gs[k][cl]);
     df_fma(acc, hs[h].mu, 1.f - x[off + c]);
     // weights held fixed (thought-aware pivots) take no refinement step
     r[off + c] = (zflag[off + c] || (fixed && fixed[off + c])) ? 0.f : acc.hi + acc.lo;
@@ -964,7 +974,7 @@ cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* of
     if (e != cudaSuccess) return e;
     for (int it = 0; it < refine_iters; ++it) {
         k_refine_resid<<<dim3(nblk, H), 256, rsmem, st>>>(L2, x, offsets, n, ldA, qb, part_stride, rpart, status);
-        k_colresid_sum<<<dim3((max_t + 255) / 256, H), 256, 0, st>>>(rpart, part_stride, nblk, x, zflag, offsets, hs, r,
+        k_colresid_sum<<<dim3((max_t + 31) / 32, H), 256, 0, st>>>(rpart, part_stride, nblk, x, zflag, offsets, hs, r,
                                                                     fixed, status);
         e = launch_symv(Hinv, r, offsets, H, max_t, ldA, d0, nullptr, 0, status, st);
         if (e != cudaSuccess) return e;
