@@ -99,6 +99,31 @@ __device__ __forceinline__ dfloat warp_sum_df(dfloat v) {
 
 __host__ __device__ constexpr int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+// Programmatic dependent launch.  The short kernels of the solver chains are
+// launched with launch_dep: a launch may be set up while the previous one
+// drains, and its CTAs call grid_dependency_wait() first, which returns once
+// the previous launch has completed and its writes are visible (no kernel
+// triggers its dependents early, so a waiting CTA never holds a slot that a
+// CTA of the launch it waits for still needs).  Launched normally, the wait
+// returns at once.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dep(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Per-head scalars kept in the workspace.
 struct HeadScalars {
     float mu;        // NNLS ridge

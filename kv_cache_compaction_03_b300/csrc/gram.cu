@@ -44,6 +44,7 @@ __device__ double block_parts(const double* p, int64_t count, double* sred) {
 __global__ void k_ridge_g(float* __restrict__ G, const float* __restrict__ b, const int32_t* __restrict__ offsets,
                           int64_t ldA, float eps, const double* __restrict__ sqpart, int64_t sq_count,
                           float* __restrict__ f, HeadScalars* __restrict__ hs, int32_t* __restrict__ status) {
+    grid_dependency_wait();
     const int h = blockIdx.x;
     if (!head_ok(status, h)) return;
     __shared__ double sred[32];
@@ -75,6 +76,7 @@ template <int D>
 __global__ void k_ridge_m(float* __restrict__ M, float* __restrict__ R, const float* __restrict__ Vsel,
                           const int32_t* __restrict__ offsets, int64_t ldA, float eps, HeadScalars* __restrict__ hs,
                           int32_t* __restrict__ status) {
+    grid_dependency_wait();
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     __shared__ double sred[32];
@@ -97,6 +99,7 @@ __global__ void k_ridge_m(float* __restrict__ M, float* __restrict__ R, const fl
 // grid H, block 256.
 __global__ void k_ridge_m_diag(float* __restrict__ M, const int32_t* __restrict__ offsets, int64_t ldA,
                                const HeadScalars* __restrict__ hs, const int32_t* __restrict__ status) {
+    grid_dependency_wait();
     const int h = blockIdx.x;
     if (!head_ok(status, h)) return;
     const int t = offsets[h + 1] - offsets[h];
@@ -120,6 +123,7 @@ __global__ void __launch_bounds__(256) k_xsoftmax(const float* __restrict__ L2, 
                                                   const int32_t* __restrict__ offsets, int n, int64_t ldA,
                                                   __nv_bfloat16* __restrict__ Xh, __nv_bfloat16* __restrict__ Xl,
                                                   const int32_t* __restrict__ status) {
+    grid_dependency_wait();
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     extern __shared__ float4 lw4[];
@@ -182,7 +186,11 @@ __global__ void __launch_bounds__(256) k_xsoftmax(const float* __restrict__ L2, 
 cudaError_t launch_ridge_g(float* G, const float* b, const int32_t* offsets, int H, int64_t ldA, float eps,
                            const double* sqpart, int64_t sq_count, float* f,
                            HeadScalars* hs, int32_t* status, cudaStream_t st) {
-    k_ridge_g<<<H, 256, 0, st>>>(G, b, offsets, ldA, eps, sqpart, sq_count, f, hs, status);
+    {
+        const cudaError_t le = launch_dep(k_ridge_g, dim3(H), dim3(256), 0, st, G, b, offsets, ldA, eps, sqpart,
+                                          sq_count, f, hs, status);
+        if (le != cudaSuccess) return le;
+    }
     return cudaGetLastError();
 }
 cudaError_t launch_ridge_m(int d, float* M, float* R, const float* Vsel, const int32_t* offsets, int H, int64_t ldA,
@@ -190,10 +198,21 @@ cudaError_t launch_ridge_m(int d, float* M, float* R, const float* Vsel, const i
     // launched before M is factored, after R is complete; the max_t bound is ldA
     const int chunks = (int)(((int64_t)ldA * d + kRidgeChunk - 1) / kRidgeChunk);
     if (d == 128)
-        k_ridge_m<128><<<dim3(chunks, H), 256, 0, st>>>(M, R, Vsel, offsets, ldA, eps, hs, status);
+        {
+            const cudaError_t le = launch_dep(k_ridge_m<128>, dim3(dim3(chunks, H)), dim3(256), 0, st, M, R, Vsel,
+                                              offsets, ldA, eps, hs, status);
+            if (le != cudaSuccess) return le;
+        }
     else
-        k_ridge_m<64><<<dim3(chunks, H), 256, 0, st>>>(M, R, Vsel, offsets, ldA, eps, hs, status);
-    k_ridge_m_diag<<<H, 256, 0, st>>>(M, offsets, ldA, hs, status);
+        {
+            const cudaError_t le = launch_dep(k_ridge_m<64>, dim3(dim3(chunks, H)), dim3(256), 0, st, M, R, Vsel,
+                                              offsets, ldA, eps, hs, status);
+            if (le != cudaSuccess) return le;
+        }
+    {
+        const cudaError_t le = launch_dep(k_ridge_m_diag, dim3(H), dim3(256), 0, st, M, offsets, ldA, hs, status);
+        if (le != cudaSuccess) return le;
+    }
     return cudaGetLastError();
 }
 // wfit: the fitted NNLS weights (clamped at 0), [sum t].
@@ -203,7 +222,11 @@ cudaError_t launch_xsoftmax(const float* L2, const float* wfit, const int32_t* o
     const size_t smem = (size_t)ldA * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(k_xsoftmax, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_xsoftmax<<<grid, 256, smem, st>>>(L2, wfit, offsets, n, ldA, (__nv_bfloat16*)Xh, (__nv_bfloat16*)Xl, status);
+    {
+        const cudaError_t le = launch_dep(k_xsoftmax, dim3(grid), dim3(256), smem, st, L2, wfit, offsets, n, ldA,
+                                          (__nv_bfloat16*)Xh, (__nv_bfloat16*)Xl, status);
+        if (le != cudaSuccess) return le;
+    }
     return cudaGetLastError();
 }
 

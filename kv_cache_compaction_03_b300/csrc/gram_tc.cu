@@ -252,6 +252,7 @@ __global__ void __launch_bounds__(256) k_split_hilo(const float* __restrict__ X,
                                                     __nv_bfloat16* __restrict__ Xh, __nv_bfloat16* __restrict__ Xl,
                                                     float* __restrict__ colsum, int64_t colsum_stride,
                                                     double* __restrict__ sqpart, const int32_t* __restrict__ status) {
+    grid_dependency_wait();
     const int h = blockIdx.z;
     if (!head_ok(status, h)) return;
     const int off = offsets ? offsets[h] : 0;
@@ -298,6 +299,7 @@ __global__ void __launch_bounds__(256) k_split_hilo(const float* __restrict__ X,
 __global__ void k_colsum_total(const float* __restrict__ colsum, int ntiles, int64_t stride,
                                const int32_t* __restrict__ offsets, float* __restrict__ b,
                                const int32_t* __restrict__ status) {
+    grid_dependency_wait();
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     const int off = offsets[h];
@@ -329,6 +331,7 @@ __device__ __forceinline__ void split3(float x, __nv_bfloat16& hi, __nv_bfloat16
 // grid (ceil(ldA/256), ldA, H): Minv rows/columns < t_h -> [3][H][ldA][ldA], 0 elsewhere.
 __global__ void k_split3_square(const float* __restrict__ Minv, int64_t ldA, const int32_t* __restrict__ offsets,
                                 __nv_bfloat16* __restrict__ out, int64_t ts, const int32_t* __restrict__ status) {
+    grid_dependency_wait();
     const int h = blockIdx.z;
     if (!head_ok(status, h)) return;
     const int t = offsets[h + 1] - offsets[h];
@@ -346,6 +349,7 @@ __global__ void k_split3_square(const float* __restrict__ Minv, int64_t ldA, con
 // grid (ldA, H), block d: R [sum t][d] -> [3][H][ldA][d], rows past t_h zero.
 __global__ void k_split3_rows(const float* __restrict__ R, int d, int64_t ldA, const int32_t* __restrict__ offsets,
                               __nv_bfloat16* __restrict__ out, int64_t ts, const int32_t* __restrict__ status) {
+    grid_dependency_wait();
     const int h = blockIdx.y, r = blockIdx.x, c = threadIdx.x;
     if (!head_ok(status, h)) return;
     const int off = offsets[h];
@@ -544,7 +548,11 @@ cudaError_t launch_gram_rect_tc(int d, const void* Ah, const void* Al, const voi
 // b[off + c] = sum over the row-tile partials (fixed order).
 cudaError_t launch_colsum_total(const float* part, int ntiles, int64_t stride, const int32_t* offsets, float* b,
                                 int H, int max_cols, const int32_t* status, cudaStream_t st) {
-    k_colsum_total<<<dim3((max_cols + 255) / 256, H), 256, 0, st>>>(part, ntiles, stride, offsets, b, status);
+    {
+        const cudaError_t le = launch_dep(k_colsum_total, dim3(dim3((max_cols + 255) / 256, H)), dim3(256), 0, st,
+                                          part, ntiles, stride, offsets, b, status);
+        if (le != cudaSuccess) return le;
+    }
     return cudaGetLastError();
 }
 
@@ -563,13 +571,25 @@ cudaError_t launch_split_hilo(bool exp_mode, const float* X, int H, int rows, in
         if (e != cudaSuccess) return e;
     }
     if (exp_mode)
-        k_split_hilo<true><<<grid, 256, 0, st>>>(X, rows, ld, offsets, cols, (__nv_bfloat16*)Xh, (__nv_bfloat16*)Xl,
-                                                 colsum ? part : nullptr, stride, sqpart, status);
+        {
+            const cudaError_t le = launch_dep(k_split_hilo<true>, dim3(grid), dim3(256), 0, st, X, rows, ld, offsets,
+                                              cols, (__nv_bfloat16*)Xh, (__nv_bfloat16*)Xl, colsum ? part : nullptr,
+                                              stride, sqpart, status);
+            if (le != cudaSuccess) return le;
+        }
     else
-        k_split_hilo<false><<<grid, 256, 0, st>>>(X, rows, ld, offsets, cols, (__nv_bfloat16*)Xh, (__nv_bfloat16*)Xl,
-                                                  colsum ? part : nullptr, stride, sqpart, status);
+        {
+            const cudaError_t le = launch_dep(k_split_hilo<false>, dim3(grid), dim3(256), 0, st, X, rows, ld, offsets,
+                                              cols, (__nv_bfloat16*)Xh, (__nv_bfloat16*)Xl, colsum ? part : nullptr,
+                                              stride, sqpart, status);
+            if (le != cudaSuccess) return le;
+        }
     if (colsum && offsets)
-        k_colsum_total<<<dim3((max_cols + 255) / 256, H), 256, 0, st>>>(part, rt, stride, offsets, colsum, status);
+        {
+            const cudaError_t le = launch_dep(k_colsum_total, dim3(dim3((max_cols + 255) / 256, H)), dim3(256), 0, st,
+                                              part, rt, stride, offsets, colsum, status);
+            if (le != cudaSuccess) return le;
+        }
     return cudaGetLastError();
 }
 
@@ -585,9 +605,16 @@ cudaError_t launch_apply_inverse_tc(int d, const float* Minv, const float* R, co
     const int64_t tsm = (int64_t)H * ldA * ldA;
     __nv_bfloat16* Rs = Ms + 3 * tsm;
     const int64_t tsr = (int64_t)H * ldA * d;
-    k_split3_square<<<dim3((unsigned)((ldA + 255) / 256), (unsigned)ldA, H), 256, 0, st>>>(Minv, ldA, offsets, Ms, tsm,
-                                                                                         status);
-    k_split3_rows<<<dim3((unsigned)ldA, H), d, 0, st>>>(R, d, ldA, offsets, Rs, tsr, status);
+    {
+        const cudaError_t le = launch_dep(k_split3_square, dim3(dim3((unsigned)((ldA + 255) / 256), (unsigned)ldA,
+                                          H)), dim3(256), 0, st, Minv, ldA, offsets, Ms, tsm, status);
+        if (le != cudaSuccess) return le;
+    }
+    {
+        const cudaError_t le = launch_dep(k_split3_rows, dim3(dim3((unsigned)ldA, H)), dim3(d), 0, st, R, d, ldA,
+                                          offsets, Rs, tsr, status);
+        if (le != cudaSuccess) return le;
+    }
     CUtensorMap mm[3], mr[3];
     for (int q = 0; q < 3; ++q)
         if (!make_map_bf16(&mm[q], Ms + q * tsm, (int)ldA, ldA, (int)ldA, H) ||

@@ -688,6 +688,7 @@ __device__ bool bpp_step_body(const BppArgs& a) {
 // counters) lives in global memory between steps and is re-read after a
 // block barrier.  grid H, block 512.
 __global__ void __launch_bounds__(512) k_bpp_solve(BppArgs a, int max_iter) {
+    grid_dependency_wait();
     for (int it = 0; it < max_iter; ++it) {
         if (bpp_step_body(a)) break;
         __syncthreads();
@@ -696,6 +697,7 @@ __global__ void __launch_bounds__(512) k_bpp_solve(BppArgs a, int max_iter) {
 
 // Reset the pivoting state (grid ceil(sum/256) x H); also zero the zero set.
 __global__ void k_bpp_init(BppArgs a) {
+    grid_dependency_wait();
     const int h = blockIdx.y;
     const int off = a.offsets[h];
     const int t = a.offsets[h + 1] - off;
@@ -714,6 +716,7 @@ __global__ void k_bpp_init(BppArgs a) {
 
 // Heads still pivoting after the last step hit the iteration cap.
 __global__ void k_bpp_finish(BppArgs a, int H) {
+    grid_dependency_wait();
     const int h = blockIdx.x * blockDim.x + threadIdx.x;
     if (h >= H || !head_ok(a.status, h)) return;
     if (!a.piv[4 * h]) set_status(a.status, h, KVC_ERR_NNLS_MAXITER);
@@ -735,6 +738,7 @@ __global__ void __launch_bounds__(256) k_refine_resid(const float* __restrict__ 
                                                       const int32_t* __restrict__ offsets, int n, int64_t ldA,
                                                       int qb, int64_t part_stride, dfloat* __restrict__ part,
                                                       int32_t* __restrict__ status) {
+    grid_dependency_wait();
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     extern __shared__ __align__(16) float sa[];    // [qb][ldA] A', then [qb] u, then the barrier
@@ -807,6 +811,7 @@ __global__ void __launch_bounds__(256) k_colresid_sum(const dfloat* __restrict__
                                                       const HeadScalars* __restrict__ hs, float* __restrict__ r,
                                                       const uint8_t* __restrict__ fixed,
                                                       const int32_t* __restrict__ status) {
+    grid_dependency_wait();
     // thread (g, cl): column blockIdx.x * 32 + cl, partials [g nb8, (g + 1) nb8);
     // the eight group sums then meet in group order (a fixed order)
     const int h = blockIdx.y;
@@ -833,6 +838,7 @@ __global__ void __launch_bounds__(256) k_colresid_sum(const dfloat* __restrict__
 // x += H_FF^{-1} r_F: d0 = H^{-1} r is in `d0`; apply the Schur correction
 // with the stored factor of (H^{-1})_ZZ.  grid H, block 512.
 __global__ void __launch_bounds__(512) k_refine_apply(BppArgs a, const float* __restrict__ d0) {
+    grid_dependency_wait();
     const int h = blockIdx.x;
     if (!head_ok(a.status, h)) return;
     extern __shared__ float sm[];
@@ -863,6 +869,7 @@ __global__ void __launch_bounds__(512) k_refine_apply(BppArgs a, const float* __
 __global__ void k_beta_out(float* __restrict__ x, const int32_t* __restrict__ offsets, float* __restrict__ beta,
                            const int32_t* __restrict__ status, const float* __restrict__ bias_in,
                            const int32_t* __restrict__ idx, int T) {
+    grid_dependency_wait();
     const int h = blockIdx.y;
     const int off = offsets[h];
     const int t = offsets[h + 1] - off;
@@ -954,7 +961,10 @@ cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* of
     const int64_t part_stride = (int64_t)H * max_t;
     BppArgs b{x0, x, zflag, zlist, nz, Hinv, S, piv, offsets, f, ldA, zmax, hs, status};
     int nl = 0;
-    k_bpp_init<<<dim3((max_t + 255) / 256, H), 256, 0, st>>>(b);
+    {
+        const cudaError_t le = launch_dep(k_bpp_init, dim3(dim3((max_t + 255) / 256, H)), dim3(256), 0, st, b);
+        if (le != cudaSuccess) return le;
+    }
     cudaError_t e = launch_symv(Hinv, f, offsets, H, max_t, ldA, x0, nullptr, 0, status, st);
     if (e != cudaSuccess) return e;
     nl += 2;
@@ -963,9 +973,15 @@ cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* of
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_refine_apply, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_bpp_solve<<<H, 512, smem, st>>>(b, max_iter);
+    {
+        const cudaError_t le = launch_dep(k_bpp_solve, dim3(H), dim3(512), smem, st, b, max_iter);
+        if (le != cudaSuccess) return le;
+    }
     ++nl;
-    k_bpp_finish<<<(H + 127) / 128, 128, 0, st>>>(b, H);
+    {
+        const cudaError_t le = launch_dep(k_bpp_finish, dim3((H + 127) / 128), dim3(128), 0, st, b, H);
+        if (le != cudaSuccess) return le;
+    }
     ++nl;
     const int qb = refine_rows(ldA);
     const int nblk = (n + qb - 1) / qb;
@@ -973,12 +989,22 @@ cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* of
     e = cudaFuncSetAttribute(k_refine_resid, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsmem);
     if (e != cudaSuccess) return e;
     for (int it = 0; it < refine_iters; ++it) {
-        k_refine_resid<<<dim3(nblk, H), 256, rsmem, st>>>(L2, x, offsets, n, ldA, qb, part_stride, rpart, status);
-        k_colresid_sum<<<dim3((max_t + 31) / 32, H), 256, 0, st>>>(rpart, part_stride, nblk, x, zflag, offsets, hs, r,
-                                                                    fixed, status);
+        {
+            const cudaError_t le = launch_dep(k_refine_resid, dim3(dim3(nblk, H)), dim3(256), rsmem, st, L2, x,
+                                              offsets, n, ldA, qb, part_stride, rpart, status);
+            if (le != cudaSuccess) return le;
+        }
+        {
+            const cudaError_t le = launch_dep(k_colresid_sum, dim3(dim3((max_t + 31) / 32, H)), dim3(256), 0, st,
+                                              rpart, part_stride, nblk, x, zflag, offsets, hs, r, fixed, status);
+            if (le != cudaSuccess) return le;
+        }
         e = launch_symv(Hinv, r, offsets, H, max_t, ldA, d0, nullptr, 0, status, st);
         if (e != cudaSuccess) return e;
-        k_refine_apply<<<H, 512, smem, st>>>(b, d0);
+        {
+            const cudaError_t le = launch_dep(k_refine_apply, dim3(H), dim3(512), smem, st, b, d0);
+            if (le != cudaSuccess) return le;
+        }
         nl += 4;
     }
     if (launches) *launches = nl;
@@ -988,7 +1014,11 @@ cudaError_t launch_nnls_all(const float* Hinv, const float* f, const int32_t* of
 cudaError_t launch_beta_out(float* x, const int32_t* offsets, int H, int max_t, float* beta, const int32_t* status,
                             const float* bias_in, const int32_t* idx, int T, cudaStream_t st) {
     dim3 grid((max_t + 255) / 256, H);
-    k_beta_out<<<grid, 256, 0, st>>>(x, offsets, beta, status, bias_in, idx, T);
+    {
+        const cudaError_t le = launch_dep(k_beta_out, dim3(grid), dim3(256), 0, st, x, offsets, beta, status, bias_in,
+                                          idx, T);
+        if (le != cudaSuccess) return le;
+    }
     return cudaGetLastError();
 }
 

@@ -40,6 +40,7 @@ using namespace tc;
 namespace {
 constexpr int SB = 64;     // sweep block
 
+
 struct SweepArgs {
     float* A;                 // [H][ldA][ldA]
     float* U;                 // [H][64][ldA]  U^T: U[p][r] = (A_ik P)[r][p]
@@ -210,6 +211,7 @@ __device__ __forceinline__ void chain_invert(float (*Dn)[kPS], float (*grp)[4][S
 // them (the other CTAs rewrite A meanwhile) and inverts it.
 __global__ void __launch_bounds__(kPivThreads) k_sweep_pivot(SweepArgs s) {
     constexpr int NT = kPivThreads;
+    grid_dependency_wait();
     const int h = blockIdx.y;
     if (!head_ok(s.status, h)) return;
     const int t = s.offsets[h + 1] - s.offsets[h];
@@ -389,6 +391,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
                       const __grid_constant__ CUtensorMap mU2, const __grid_constant__ CUtensorMap mV0,
                       const __grid_constant__ CUtensorMap mV1, const __grid_constant__ CUtensorMap mV2,
                       const __grid_constant__ CUtensorMap mA, SweepArgs s) {
+    grid_dependency_wait();
     const long long wait_limit = s.wait_limit;
     const int h = blockIdx.y;
     if (!head_ok(s.status, h)) return;
@@ -623,6 +626,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
 // Upper triangle <- lower triangle.  grid (blocks * (blocks - 1) / 2 + blocks, H), block 256.
 __global__ void __launch_bounds__(256) k_sweep_mirror(float* __restrict__ Am, const int32_t* __restrict__ offsets,
                                                       int64_t ldA, const int32_t* __restrict__ status) {
+    grid_dependency_wait();
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     const int t = offsets[h + 1] - offsets[h];
@@ -648,6 +652,7 @@ __global__ void __launch_bounds__(256) k_symv(const float* __restrict__ Hinv, co
                                               const int32_t* __restrict__ offsets, int64_t ldA,
                                               float* __restrict__ y, const int32_t* __restrict__ done,
                                               int done_stride, const int32_t* __restrict__ status) {
+    grid_dependency_wait();
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     if (done && done[(int64_t)h * done_stride]) return;
@@ -700,18 +705,30 @@ cudaError_t launch_sweep_inverse(float* A, const int32_t* offsets, int H, int ma
     float* Pn = P + 3 * (int64_t)H * SB * SB;
     for (int k = 0; k < nb; ++k) {
         SweepArgs s{A, U, Us, Vs, P, Xn, Pn, offsets, ldA, ts, k * SB, status, k > 0, wait_limit};
-        k_sweep_pivot<<<dim3(nb, H), kPivThreads, 0, st>>>(s);
+        // pivot and update launches follow one another with programmatic
+        // dependent launch (common.cuh)
+        e = launch_dep(k_sweep_pivot, dim3(nb, H), dim3(kPivThreads), 0, st, s);
+        if (e != cudaSuccess) return e;
         // CTA 0 of each head forms and inverts the next pivot block
-        k_sweep_update_tc<<<dim3(nu * (nu + 1) / 2 + 1, H), kUThreads, kUSmem, st>>>(mu[0], mu[1], mu[2], mv[0],
-                                                                                      mv[1], mv[2], ma, s);
+        e = launch_dep(k_sweep_update_tc, dim3(nu * (nu + 1) / 2 + 1, H), dim3(kUThreads), kUSmem, st, mu[0], mu[1],
+                       mu[2], mv[0], mv[1], mv[2], ma, s);
+        if (e != cudaSuccess) return e;
     }
-    k_sweep_mirror<<<dim3(ntri, H), 256, 0, st>>>(A, offsets, ldA, status);
+    {
+        const cudaError_t le = launch_dep(k_sweep_mirror, dim3(dim3(ntri, H)), dim3(256), 0, st, A, offsets, ldA,
+                                          status);
+        if (le != cudaSuccess) return le;
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_symv(const float* Hinv, const float* v, const int32_t* offsets, int H, int max_t, int64_t ldA,
                         float* y, const int32_t* done, int done_stride, const int32_t* status, cudaStream_t st) {
-    k_symv<<<dim3((max_t + 7) / 8, H), 256, 0, st>>>(Hinv, v, offsets, ldA, y, done, done_stride, status);
+    {
+        const cudaError_t le = launch_dep(k_symv, dim3(dim3((max_t + 7) / 8, H)), dim3(256), 0, st, Hinv, v, offsets,
+                                          ldA, y, done, done_stride, status);
+        if (le != cudaSuccess) return le;
+    }
     return cudaGetLastError();
 }
 
