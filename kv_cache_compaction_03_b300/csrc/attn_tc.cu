@@ -406,6 +406,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
     constexpr int kChunk = WEIGHTED ? kLseChunk / 2 : kLseChunk;
     static_assert(kChunk % QB == 0, "a log-mass chunk holds whole query blocks");
     using L = ColLayout<D, NS>;
+    grid_dependency_wait();   // launched dependent on the previous kernel (launch_dep)
     const int h = blockIdx.y;
     if (!head_ok(status, h)) return;
     extern __shared__ uint8_t smem_raw[];
@@ -862,10 +863,10 @@ cudaError_t launch_col_t(const void* Q, const void* K, const float* lse2, int H,
     auto kern = k_colscore_tc<D, NS, BIAS, WEIGHTED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((T + 2 * TB - 1) / (2 * TB), H, nz);
-    kern<<<grid, kColThreads, smem, st>>>(mK, mQ, lse2, n, T, c2, score, status, qdiv, wait_limit, bias2,
-                                          (int)round_up(T, 256), rw, rstride, part);
-    return cudaGetLastError();
+    // programmatic dependent launch: in the matching pursuit this pass
+    // alternates with the step kernel, hundreds of times per call
+    return launch_dep(kern, dim3((T + 2 * TB - 1) / (2 * TB), H, nz), dim3(kColThreads), smem, st, mK, mQ, lse2, n,
+                      T, c2, score, status, qdiv, wait_limit, bias2, (int)round_up(T, 256), rw, rstride, part);
 }
 
 template <int D>

@@ -792,9 +792,11 @@ __global__ void __launch_bounds__(256) k_refine_resid(const float* __restrict__ 
 }
 
 // Query rows per CTA of k_refine_resid: a multiple of the 8 warps, as many
-// as keep its shared-memory tile (rows x ldA floats) within 128 KB.
+// as keep its shared-memory tile (rows x ldA floats) within 72 KB, so that
+// three CTAs share an SM and one's copies overlap the others' arithmetic
+// (ldA up to 2304; beyond that 8 rows, up to 128 KB at the largest budget).
 int refine_rows(int64_t ldA) {
-    const int64_t r = 4096 / ldA;
+    const int64_t r = 2304 / ldA;
     return 8 * (int)(r < 1 ? 1 : (r > 8 ? 8 : r));
 }
 // Bytes of the per-block partial sums of k_refine_resid.

@@ -307,6 +307,7 @@ __global__ void __launch_bounds__(kStepThreads, 1)
     k_omp_step(OmpArgs a, int s, const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
                const float* __restrict__ lse2, float c2) {
     cg::cluster_group cluster = cg::this_cluster();
+    grid_dependency_wait();                            // launched dependent on the correlation pass
     const int h = blockIdx.y;
     if (!head_ok(a.status, h)) return;                 // the same for every CTA of the cluster
     const int t = a.offsets[h + 1] - a.offsets[h];
@@ -822,15 +823,17 @@ cudaError_t launch_omp_select(int dtype, int d, const void* Q, const void* K, co
         e = cudaFuncSetAttribute(step, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.blockDim = dim3(kStepThreads);
         cfg.dynamicSmemBytes = step_smem;
         cfg.stream = st;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 1;                                  // the occupancy query sees the cluster alone
         // a cluster of 16 CTAs per head where one can be placed, else 8
         int cl = 16, nclusters = 0;
         attr[0].val.clusterDim.x = cl;
@@ -841,6 +844,7 @@ cudaError_t launch_omp_select(int dtype, int d, const void* Q, const void* K, co
             attr[0].val.clusterDim.x = cl;
             cfg.gridDim = dim3(cl, H);
         }
+        cfg.numAttrs = 2;                                  // steps launched dependent on their predecessor
         const __nv_bfloat16* Qb = (const __nv_bfloat16*)Q;
         const __nv_bfloat16* Kb = (const __nv_bfloat16*)K;
         for (int s = 0; s < max_t; ++s) {
