@@ -531,12 +531,46 @@ __device__ int build_zlist(const int8_t* zf, int t, int* zl, int zmax, int* sbuf
 // Free-set solution for the current Z: x = x0 + W nu with (H^{-1})_ZZ nu = -x0_Z.
 // sx: [t] smem (out), snu: [nz] smem (out: nu = gradient on Z).  Factors S when
 // `factor` is set.  Returns false if (H^{-1})_ZZ is not numerically SPD.
+// A zero set of at most CB indices (the usual case: a few dozen weights at
+// zero) is factored and solved in shared memory (the Cholesky scratch, row
+// stride CB + 1); the factor also goes to S for later calls without
+// `factor`, which bring it back into shared memory.  Larger zero sets work
+// on S in global memory.
 __device__ bool schur_solution(const BppArgs& a, int h, int off, int t, int nz, const int* zl, bool factor,
                                const float* src, float* sx, float* snu, float* sm_chol, int* sflag) {
     const float* Hi = a.Hinv + (int64_t)h * a.ldA * a.ldA;    // row z = H^{-1} e_z (symmetric)
     float* S = a.S + (int64_t)h * a.zmax * a.zmax;
     if (nz > 0) {
-        if (factor) {
+        const float* Ls = S;
+        int64_t lds = a.zmax;
+        if (nz <= CB) {
+            float* D = sm_chol;
+            if (factor) {
+                for (int e = threadIdx.x; e < nz * nz; e += blockDim.x) {
+                    const int r = e / nz, c = e % nz;
+                    D[r * (CB + 1) + c] = c <= r ? Hi[(int64_t)zl[c] * a.ldA + zl[r]] : 0.f;
+                }
+                if (threadIdx.x == 0) *sflag = 0;
+                __syncthreads();
+                if (threadIdx.x < 32) {
+                    const bool ok = warp_chol_block(D, nz);
+                    if (!ok && threadIdx.x == 0) *sflag = 1;
+                }
+                __syncthreads();
+                if (*sflag) return false;
+                for (int e = threadIdx.x; e < nz * nz; e += blockDim.x) {
+                    const int r = e / nz, c = e % nz;
+                    if (c <= r) S[(int64_t)r * a.zmax + c] = D[r * (CB + 1) + c];
+                }
+            } else {
+                for (int e = threadIdx.x; e < nz * nz; e += blockDim.x) {
+                    const int r = e / nz, c = e % nz;
+                    D[r * (CB + 1) + c] = c <= r ? S[(int64_t)r * a.zmax + c] : 0.f;
+                }
+            }
+            Ls = D;
+            lds = CB + 1;
+        } else if (factor) {
             for (int e = threadIdx.x; e < nz * nz; e += blockDim.x) {
                 const int r = e / nz, c = e % nz;
                 S[(int64_t)r * a.zmax + c] = Hi[(int64_t)zl[c] * a.ldA + zl[r]];
@@ -547,27 +581,47 @@ __device__ bool schur_solution(const BppArgs& a, int h, int off, int t, int nz, 
         for (int k = threadIdx.x; k < nz; k += blockDim.x) snu[k] = -src[zl[k]];
         __syncthreads();
         if (threadIdx.x < 32) {
-            // (L L^T) nu = rhs for the small system, one warp (dot products by lanes)
+            // (L L^T) nu = rhs for the small system, one warp
             const int lane = threadIdx.x;
-            for (int i = 0; i < nz; ++i) {
-                float acc = 0.f;
-                for (int p = lane; p < i; p += 32) acc += S[(int64_t)i * a.zmax + p] * snu[p];
-                acc = warp_sum(acc);
-                if (lane == 0) snu[i] = (snu[i] - acc) / S[(int64_t)i * a.zmax + i];
-                __syncwarp();
-            }
-            for (int i = nz - 1; i >= 0; --i) {
-                float acc = 0.f;
-                for (int p = i + 1 + lane; p < nz; p += 32) acc += S[(int64_t)p * a.zmax + i] * snu[p];
-                acc = warp_sum(acc);
-                if (lane == 0) snu[i] = (snu[i] - acc) / S[(int64_t)i * a.zmax + i];
-                __syncwarp();
+            if (nz <= 32) {
+                // lane i holds entry i; column by column: the pivot lane
+                // divides, the lanes below (forward) or above (backward)
+                // take its value off their own entries
+                float y = lane < nz ? snu[lane] : 0.f;
+                for (int j = 0; j < nz; ++j) {
+                    const float yj = __shfl_sync(0xffffffffu, y / Ls[(int64_t)j * lds + j], j);
+                    if (lane == j) y = yj;
+                    else if (lane > j && lane < nz) y = fmaf(-Ls[(int64_t)lane * lds + j], yj, y);
+                }
+                for (int j = nz - 1; j >= 0; --j) {
+                    const float xj = __shfl_sync(0xffffffffu, y / Ls[(int64_t)j * lds + j], j);
+                    if (lane == j) y = xj;
+                    else if (lane < j) y = fmaf(-Ls[(int64_t)j * lds + lane], xj, y);
+                }
+                if (lane < nz) snu[lane] = y;
+            } else {
+                // dot products by lanes
+                for (int i = 0; i < nz; ++i) {
+                    float acc = 0.f;
+                    for (int p = lane; p < i; p += 32) acc += Ls[(int64_t)i * lds + p] * snu[p];
+                    acc = warp_sum(acc);
+                    if (lane == 0) snu[i] = (snu[i] - acc) / Ls[(int64_t)i * lds + i];
+                    __syncwarp();
+                }
+                for (int i = nz - 1; i >= 0; --i) {
+                    float acc = 0.f;
+                    for (int p = i + 1 + lane; p < nz; p += 32) acc += Ls[(int64_t)p * lds + i] * snu[p];
+                    acc = warp_sum(acc);
+                    if (lane == 0) snu[i] = (snu[i] - acc) / Ls[(int64_t)i * lds + i];
+                    __syncwarp();
+                }
             }
         }
         __syncthreads();
     }
     for (int i = threadIdx.x; i < t; i += blockDim.x) {
         float v = src[i];
+#pragma unroll 4
         for (int k = 0; k < nz; ++k) v = fmaf(Hi[(int64_t)zl[k] * a.ldA + i], snu[k], v);
         sx[i] = v;
     }

@@ -85,16 +85,17 @@ def run_gpu(w, inputs=None, buds=None, params=None):
     return out, inputs
 
 
-def run_oracle_head(w, inputs, h, t, idx=None):
+def run_oracle_head(w, inputs, h, t, idx=None, eps_mu=None):
     Q = oracle.decode(inputs["Q"][h], w.dtype)
     K = oracle.decode(inputs["K"][h], w.dtype)
     V = oracle.decode(inputs["V"][h], w.dtype)
     Qt = oracle.decode(inputs["Qt"][h], w.dtype)
     scale = 1.0 / math.sqrt(w.d)
     forced = forced_mask(w) if (w.keep_first or w.keep_last) else None
-    r = oracle.compact_head(Q, K, V, t, forced=forced)
+    mu_kw = {} if eps_mu is None else {"eps_mu": eps_mu}
+    r = oracle.compact_head(Q, K, V, t, forced=forced, **mu_kw)
     if idx is not None and not np.array_equal(idx, r.idx):
-        r = continue_oracle(Q, K, V, r, idx, scale)
+        r = continue_oracle(Q, K, V, r, idx, scale, eps_mu)
     Ohat = oracle.attend(Qt, r.Ck, r.beta, r.Cv, scale)
     return r, Ohat
 
@@ -104,19 +105,19 @@ def head_queries(w, inputs, h):
     return oracle.decode(inputs["Q"][h], w.dtype)
 
 
-def continue_oracle(Q, K, V, r, idx, scale):
+def continue_oracle(Q, K, V, r, idx, scale, eps_mu=None):
     """The oracle's result for one head continued from a given (valid)
     selection idx instead of its own."""
     Ck = K[idx]
     Ap = oracle.mass_matrix(Q, Ck, r.lse, scale)
-    wv, beta, mu, _, _ = oracle.fit_beta(Ap)
+    wv, beta, mu, _, _ = oracle.fit_beta(Ap) if eps_mu is None else oracle.fit_beta(Ap, eps_mu)
     X = oracle.biased_softmax(Ap, wv)
     Cv, lam = oracle.fit_values(X, r.O, V[idx])
     return oracle.HeadResult(idx=idx, score=r.score, lse=r.lse, O=r.O, Ck=Ck, w=wv, beta=beta, Cv=Cv, mu=mu,
                              lam=lam, mass=Ap @ wv)
 
 
-def fp32_logit_beta(Q, r, scale, refit=None, bias=None):
+def fp32_logit_beta(Q, r, scale, refit=None, bias=None, eps_mu=None):
     """beta of the oracle's fit re-solved on the relative masses that fp32
     logits give: the raw logit q . C_k[i], the log-mass lse_q and the kept
     keys' input biases (in log2 units) rounded to float32, the scaled sum
@@ -134,7 +135,7 @@ def fp32_logit_beta(Q, r, scale, refit=None, bias=None):
     A = np.exp2(l2)
     if refit is not None:
         return refit(A)
-    beta = oracle.fit_beta(A)[1]
+    beta = (oracle.fit_beta(A) if eps_mu is None else oracle.fit_beta(A, eps_mu))[1]
     return beta if bias is None else bias + beta
 
 
@@ -153,7 +154,7 @@ def idx_check(gpu_idx, or_idx, or_score):
     return ok, True
 
 
-def compare_head(g, h, r, Ohat_or, report, Q=None, scale=None, refit=None, bias=None):
+def compare_head(g, h, r, Ohat_or, report, Q=None, scale=None, refit=None, bias=None, eps_mu=None):
     """Head h of the GPU's outputs g against the oracle's result r (tolerances
     in the module docstring).  Q (float64 reference queries of the head) and
     scale enable the per-weight fp32 determination of beta."""
@@ -170,7 +171,7 @@ def compare_head(g, h, r, Ohat_or, report, Q=None, scale=None, refit=None, bias=
     live = wo >= BETA_W_FLOOR * wmax
     determined = np.ones_like(live)
     if Q is not None:
-        b32 = fp32_logit_beta(Q, r, scale if scale is not None else 1.0 / math.sqrt(Q.shape[1]), refit, bias)
+        b32 = fp32_logit_beta(Q, r, scale if scale is not None else 1.0 / math.sqrt(Q.shape[1]), refit, bias, eps_mu)
         with np.errstate(invalid="ignore"):
             sens = np.where(np.isfinite(b32) & live, np.abs(b32 - bo), np.inf)
         determined = sens <= FP32_SENS_SHARE * BETA_ABS
