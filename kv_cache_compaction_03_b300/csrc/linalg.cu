@@ -776,6 +776,23 @@ __global__ void k_bpp_finish(BppArgs a, int H) {
     if (!a.piv[4 * h]) set_status(a.status, h, KVC_ERR_NNLS_MAXITER);
 }
 
+// df_fma on two independent accumulators (hi, lo) at once, with paired fp32
+// instructions: the same error-free product and sum in the same order, each
+// difference x - y written as fma(y, -1, x).  Being inline assembly, none of
+// it can be fused by the compiler.
+__device__ __forceinline__ void df_fma2(float2& hi, float2& lo, float2 a, float2 b) {
+    const float2 m1 = make_float2(-1.f, -1.f), z = make_float2(0.f, 0.f);
+    const float2 p = tc::ffma2(a, b, z);
+    const float2 pe = tc::ffma2(a, b, tc::ffma2(p, m1, z));
+    const float2 s = tc::fadd2(hi, p);
+    const float2 bb = tc::ffma2(hi, m1, s);                                   // s - hi
+    const float2 e0 = tc::fadd2(tc::ffma2(tc::ffma2(bb, m1, s), m1, hi),      // hi - (s - bb)
+                                tc::ffma2(bb, m1, p));                        // p - bb
+    const float2 e = tc::fadd2(e0, tc::fadd2(lo, pe));
+    hi = tc::fadd2(s, e);
+    lo = tc::ffma2(tc::ffma2(s, m1, hi), m1, e);                              // e - (hi - s)
+}
+
 // The residual of the refinement, r_i = sum_q A'_qi u_q + mu (1 - x_i) with
 // u_q = 1 - sum_i A'_qi x_i, in one pass over the log-masses: a CTA takes
 // `qb` query rows of one head, brings them into shared memory with one bulk
@@ -824,24 +841,38 @@ __global__ void __launch_bounds__(256) k_refine_resid(const float* __restrict__ 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int rr = warp; rr < qb; rr += 8) {
         float* arow = sa + (int64_t)rr * ldA;
-        dfloat acc{0.f, 0.f};
+        // a lane takes pairs of adjacent columns (paired arithmetic); with t
+        // odd the pair's second column, t, is set to 0 (ldA > t then)
+        float2 hi = make_float2(0.f, 0.f), lo = make_float2(0.f, 0.f);
         if (rr < rows) {
-            for (int i = lane; i < t; i += 32) {
-                const float a = exp2f(arow[i]);
-                arow[i] = a;
-                df_fma(acc, a, x[off + i]);
+            for (int i = 2 * lane; i < t; i += 64) {
+                const bool two = i + 1 < t;
+                const float2 l = *reinterpret_cast<const float2*>(arow + i);
+                const float2 a = make_float2(exp2f(l.x), two ? exp2f(l.y) : 0.f);
+                *reinterpret_cast<float2*>(arow + i) = a;
+                df_fma2(hi, lo, a, make_float2(x[off + i], two ? x[off + i + 1] : 0.f));
             }
         } else {
             for (int i = lane; i < t; i += 32) arow[i] = 0.f;
         }
+        dfloat acc{hi.x, lo.x};
+        df_add_df(acc, dfloat{hi.y, lo.y});
         acc = warp_sum_df(acc);
         if (lane == 0) su[rr] = rr < rows ? (1.f - acc.hi) - acc.lo : 0.f;
     }
     __syncthreads();
-    for (int c = threadIdx.x; c < t; c += 256) {
-        dfloat acc{0.f, 0.f};
-        for (int rr = 0; rr < qb; ++rr) df_fma(acc, sa[(int64_t)rr * ldA + c], su[rr]);
-        part[(int64_t)blockIdx.x * part_stride + off + c] = acc;
+    // a thread per pair of adjacent columns, paired arithmetic
+    const int npair = (t + 1) >> 1;
+    for (int cp = threadIdx.x; cp < npair; cp += 256) {
+        const int c = 2 * cp;
+        float2 hi = make_float2(0.f, 0.f), lo = make_float2(0.f, 0.f);
+        for (int rr = 0; rr < qb; ++rr) {
+            const float u = su[rr];
+            df_fma2(hi, lo, *reinterpret_cast<const float2*>(sa + (int64_t)rr * ldA + c), make_float2(u, u));
+        }
+        dfloat* pp = part + (int64_t)blockIdx.x * part_stride + off + c;
+        pp[0] = dfloat{hi.x, lo.x};
+        if (c + 1 < t) pp[1] = dfloat{hi.y, lo.y};
     }
 }
 
